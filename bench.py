@@ -1,0 +1,395 @@
+"""Benchmark of the DFlash block-draft cycle on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+on the full DFlash geometry (5 layers, hidden 2560, 24Q/2KV x 256, MLP 7680,
+vocab 151936) with an 8192-position context and an 8-row block:
+  fuse the taps of 8 committed positions [p-8, p) into every layer's FP16
+  K/V  ->  draft the block at p (5 layers + final norm + LM head + argmax)
+  ->  greedy acceptance against synthetic verifier ids.
+All of it runs in libdflash's CUDA kernels through the C ABI.  The anchor
+position stays at p = 8192 so every step does identical work.
+
+Printed (rank 0): one JSON line with the metric, device-timed passes/s, the
+end-to-end number through the C ABI with host buffers, the dominant kernel's
+roofline, the CPU oracle timed on the host cores as a baseline, SM clocks
+sampled during the timed region and the kernel-launch count.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  (N > 1: launched by torch.distributed.run; every rank runs an independent
+  replica on its own GPU -- the sequences are independent, there is no
+  data-path collective.)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dflash_synth as synth  # noqa: E402
+
+METRIC = "draft passes/s and drafted tok/s at 8K ctx, block 8; HBM GB/s vs roofline"
+UNIT = "draft passes/s"
+WORKLOAD = "full_bf16"
+FUSE_PER_STEP = 8
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(cfg, ctx: int, B: int, n_fuse: int) -> dict:
+    """Bytes the cycle must move (each weight byte and each context K/V cell
+    read once, outputs written once)."""
+    H, d, nkv, L = cfg.hidden, cfg.head_dim, cfg.n_kv_heads, cfg.n_layers
+    shapes = cfg.matrix_shapes()
+    bpw = {"bf16": 2.0, "q8_0": 34 / 32, "q5_0": 22 / 32, "q4_0": 18 / 32}[cfg.weight_type]
+    layer_params = sum(a * b for n, (a, b) in shapes.items() if n != "fc")
+    kv_params = sum(a * b for n, (a, b) in shapes.items() if n.endswith((".wk", ".wv")))
+    head = cfg.vocab * H * 2
+    kv_read = L * 2 * nkv * (ctx + B) * d * 2
+    kv_write_block = L * 2 * nkv * B * d * 2
+    draft = layer_params * bpw + head + kv_read + kv_write_block + B * H * 2
+    fuse = (shapes["fc"][0] * shapes["fc"][1] + kv_params) * bpw + n_fuse * cfg.tap_width * 2 \
+        + L * 2 * nkv * n_fuse * d * 2
+    return {"draft": int(draft), "fuse": int(fuse), "head": int(head), "step": int(draft + fuse)}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (also the reference arm)
+# --------------------------------------------------------------------------
+def oracle_baseline(ckpt, cfg, budget_s: float = 12.0, max_steps: int = 1000):
+    """The CPU oracle, as it stands, timed on this host's cores over a bounded
+    sample of the same cycle (fuse 8 positions + draft + accept) at the same
+    shapes.  Its 8192-position context is pre-filled with seeded FP16 values
+    (fusing 8192 positions in float64 is not part of the timed cycle)."""
+    from oracle import dflash_oracle as O
+    cores = len(os.sched_getaffinity(0))
+    ctx, B = cfg.ctx, cfg.block
+    om = O.Model(cfg, ckpt)
+    st = O.State(cfg, ctx + B)
+    st.fill(synth.make_kv_fill(cfg, ctx, seed=1), ctx)
+    taps = synth.make_taps(cfg, FUSE_PER_STEP, seed=2)
+    fpos = np.arange(ctx - FUSE_PER_STEP, ctx)
+    anchor = int(synth.make_token_ids(cfg, 1, seed=3)[0])
+    tgt = synth.make_target_ids(np.zeros(B - 1, np.int32), cfg.vocab, seed=4, p_agree=0.0)
+
+    def step():
+        O.fuse_context(om, st, taps, fpos)
+        r = O.draft_block(om, st, anchor, ctx, B)
+        O.accept(r.drafts, tgt, B)
+
+    t0 = time.perf_counter()
+    step()  # first call decodes the weights to float64 (a one-time load)
+    load_s = time.perf_counter() - t0
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps:
+        step()
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} oracle cycles (fuse 8 + draft + accept) at the full shape after one warm-up cycle "
+                      f"({load_s:.1f} s incl. weight decode); context K/V pre-filled",
+            "seconds": dt}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[WORKLOAD]
+    ckpt = synth.make_checkpoint(cfg, seed=0)
+    budget = max(5.0, min(120.0, 0.5 * (args.steps + args.warmup)))
+    base = oracle_baseline(ckpt, cfg, budget_s=budget, max_steps=args.steps + args.warmup)
+    v = base["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v if v else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(cfg),
+            "drafted_tok_per_s": v * (cfg.block - 1),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
+                             "sample": base["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg):
+    return {"workload": "DFlash draft cycle: fuse 8 committed positions + draft an 8-row block at p = 8192 "
+                        "+ greedy accept; 5 layers, hidden 2560, 24Q/2KV x 256, MLP 7680, vocab 151936, "
+                        f"{cfg.weight_type.upper()} backbone",
+            "ctx": cfg.ctx, "block": cfg.block, "fuse_per_step": FUSE_PER_STEP, "weight_type": cfg.weight_type,
+            "sequences_per_gpu": 1,
+            "l2": "inputs larger than L2: every step streams ~1.9 GB of weights and K/V (L2 is 129 MB)"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def run_gpu(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import dflash_block_drafter_gb300 as D
+    from dflash_block_drafter_gb300.runtime import DraftModel, DraftState, accept
+
+    D.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS[WORKLOAD]
+    if args.weight_type:
+        cfg = cfg.with_(weight_type=args.weight_type)
+    ctx, B = cfg.ctx, cfg.block
+    t_setup = time.perf_counter()
+    ckpt = synth.make_checkpoint(cfg, seed=0)
+    model = DraftModel(cfg, ckpt, device=dev)
+    st = DraftState(model, n_slots=1, capacity=ctx + B)
+    # build the 8192-position context by fusion (128-position tiles)
+    for base in range(0, ctx, 1024):
+        taps = synth.make_taps(cfg, 1024, seed=5, stream=base)
+        st.fuse(0, torch.as_tensor(taps.view(np.int16), device=dev),
+                torch.arange(base, base + 1024, dtype=torch.int32, device=dev))
+    torch.cuda.synchronize(dev)
+    setup_s = time.perf_counter() - t_setup
+
+    fuse_taps = torch.as_tensor(synth.make_taps(cfg, FUSE_PER_STEP, seed=2).view(np.int16), device=dev)
+    fuse_pos = torch.arange(ctx - FUSE_PER_STEP, ctx, dtype=torch.int32, device=dev)
+    anchor = int(synth.make_token_ids(cfg, 1, seed=3)[0])
+    st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = anchor, ctx, B
+    tgt_np = synth.make_target_ids(np.zeros(B - 1, np.int32), cfg.vocab, seed=4, p_agree=0.0)[None]
+    tgt = torch.as_tensor(tgt_np, device=dev)
+    acc_len = torch.zeros(1, dtype=torch.int32, device=dev)
+    next_anchor = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        st.fuse(0, fuse_taps, fuse_pos, stream=stream)
+        st.draft(1, want_hidden=False, stream=stream)
+        accept(st.drafts, tgt, st.block_len, acc_len, next_anchor, stream=stream)
+
+    launches = D.dflash_fuse_launches(st.handle, FUSE_PER_STEP) + D.dflash_draft_launches(st.handle, 1) + 1
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    status = st.take_status()
+    if status:
+        raise RuntimeError(f"device status {status} during warm-up")
+
+    # ---- device-timed region: K steps, head kernel timed with events inside
+    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for a, b in head_ev:  # CUDA events are created lazily on first record
+            a.record(stream)
+            b.record(stream)
+    stream.synchronize()
+    t_beg = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        time.sleep(0.15)
+        with torch.cuda.stream(stream):
+            t_beg.record(stream)
+            for i in range(args.steps):
+                D.dflash_state_set_head_events(st.handle, head_ev[i][0].cuda_event, head_ev[i][1].cuda_event)
+                step()
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        time.sleep(0.15)
+    D.dflash_state_set_head_events(st.handle, 0, 0)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_beg.elapsed_time(t_end)
+    head_ms = [a.elapsed_time(b) for a, b in head_ev]
+    status = st.take_status()
+    if status:
+        raise RuntimeError(f"device status {status} during the timed region")
+
+    # ---- draft-only device timing (context for the reader)
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_draft = max(20, args.steps // 4)
+        e0.record(stream)
+        for _ in range(n_draft):
+            st.draft(1, want_hidden=False, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    draft_only_ms = e0.elapsed_time(e1) / n_draft
+
+    # ---- end to end through the C ABI with host buffers
+    h_taps = torch.empty_like(fuse_taps, device="cpu").pin_memory()
+    h_taps.copy_(fuse_taps.cpu())
+    h_pos = fuse_pos.cpu().pin_memory()
+    h_scalars = torch.tensor([anchor, ctx, B], dtype=torch.int32).pin_memory()
+    h_tgt = tgt.cpu().pin_memory()
+    h_out = torch.empty(7 + 2, dtype=torch.int32).pin_memory()
+    d_scalars = torch.empty(3, dtype=torch.int32, device=dev)
+    n_e2e = max(20, min(args.steps, 500))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(n_e2e):
+            fuse_taps.copy_(h_taps, non_blocking=True)
+            fuse_pos.copy_(h_pos, non_blocking=True)
+            d_scalars.copy_(h_scalars, non_blocking=True)
+            st.anchor_tok[:1].copy_(d_scalars[0:1])
+            st.anchor_pos[:1].copy_(d_scalars[1:2])
+            st.block_len[:1].copy_(d_scalars[2:3])
+            tgt.copy_(h_tgt, non_blocking=True)
+            step()
+            h_out[:7].copy_(st.drafts[0], non_blocking=True)
+            h_out[7:8].copy_(acc_len, non_blocking=True)
+            h_out[8:9].copy_(next_anchor, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    h2d = fuse_taps.numel() * 2 + fuse_pos.numel() * 4 + 12 + tgt.numel() * 4
+    d2h = 9 * 4
+
+    # ---- gather over ranks (max time), replicas only
+    times = torch.tensor([elapsed_ms, e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_s = float(times[0]), float(times[1])
+    if rank != 0:
+        return
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1000.0)
+    ab = algorithmic_bytes(cfg, ctx, B, FUSE_PER_STEP)
+    peak, peak_kind = load_peaks()
+    head_avg_ms = statistics.mean(head_ms)
+    head_gbs = ab["head"] / (head_avg_ms * 1e-3) / 1e9
+    step_gbs = ab["step"] / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.weight_type, "data": "synthetic (seeded; random-init weights of the "
+        "DFlash geometry, N(0,1) taps)",
+        "config": config_block(cfg),
+        "drafted_tok_per_s": value * (B - 1),
+        "draft_only_ms": draft_only_ms,
+        "achieved_gbs_step": step_gbs,
+        "algorithmic_bytes_per_step": ab["step"],
+        "roofline": {"bound": "hbm", "kernel": "lm_head_argmax (gemv_kernel<WT_HEAD>)",
+                     "achieved": head_gbs, "peak": peak, "unit": "GB/s", "frac": head_gbs / peak,
+                     "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": ab["head"],
+                     "avg_launch_ms": head_avg_ms},
+        "step_roofline": {"achieved": step_gbs, "peak": peak, "frac": step_gbs / peak, "unit": "GB/s"},
+        "e2e": {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": n_e2e},
+        "gpu_launches": launches * args.steps,
+        "launches_per_step": launches,
+        "clocks": clocks.summary(),
+        "setup_s": setup_s,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in oracle_baseline(ckpt, cfg).items() if k != "seconds"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--weight-type", default=None, choices=[None, "bf16", "q8_0", "q5_0", "q4_0"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

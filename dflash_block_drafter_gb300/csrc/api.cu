@@ -1,0 +1,817 @@
+// C ABI of libdflash (include/dflash.h): argument validation, model and state
+// creation (weight repacking, tensor maps, workspace) and the launch sequence
+// of each step of the DFlash block-draft pass.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemv_launch.cuh"
+#include "kernels.h"
+
+namespace dflash {
+// GEMV launchers, instantiated in gemv_<type>.cu
+#define DFLASH_DECLARE_GEMV(WT)                                                                           \
+  extern template cudaError_t gemv_store<WT>(int, const GemvArgs&, const EpiStore&, const LaunchCfg&);  \
+  extern template cudaError_t gemv_resid<WT>(int, const GemvArgs&, const EpiResid&, const LaunchCfg&);  \
+  extern template cudaError_t gemv_swiglu<WT>(int, const GemvArgs&, void*, int, const LaunchCfg&);      \
+  extern template cudaError_t gemv_heads<WT>(int, const GemvArgs&, const EpiHeads&, const LaunchCfg&);
+DFLASH_DECLARE_GEMV(WT_BF16)
+DFLASH_DECLARE_GEMV(WT_Q8_0)
+DFLASH_DECLARE_GEMV(WT_Q5_0)
+DFLASH_DECLARE_GEMV(WT_Q4_0)
+cudaError_t gemv_argmax(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc);
+
+}  // namespace dflash
+
+using namespace dflash;
+
+struct dflash_model : public Model {};
+struct dflash_state : public State {};
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", what, cudaGetErrorString(e));
+  if (e == cudaErrorMemoryAllocation) return DFLASH_ERR_OUT_OF_MEMORY;
+  return DFLASH_ERR_CUDA;
+}
+
+#define CK(call)                                    \
+  do {                                              \
+    cudaError_t e_ = (call);                        \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+int cb_of(int wt) { return wt == WT_BF16 ? Fmt<WT_BF16>::CB : Fmt<WT_Q8_0>::CB; }
+
+__global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ in, float* __restrict__ out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __uint_as_float(static_cast<uint32_t>(in[i]) << 16);
+}
+
+int convert_norm(const void* src, float* dst, int n, cudaStream_t st) {
+  bf16_to_f32_kernel<<<(n + 255) / 256, 256, 0, st>>>(static_cast<const uint16_t*>(src), dst, n);
+  CK(cudaGetLastError());
+  return DFLASH_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major 16-bit tensor [rows, cols] with 64 x 64 boxes, 128-byte swizzle.
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, CUtensorMapDataType dt) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled unavailable");
+    return DFLASH_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return DFLASH_ERR_CUDA;
+  }
+  return DFLASH_OK;
+}
+
+template <class T>
+int dev_alloc(T** p, size_t bytes, size_t* total) {
+  void* v = nullptr;
+  CK(cudaMalloc(&v, bytes ? bytes : 16));
+  *p = static_cast<T*>(v);
+  *total += bytes;
+  return DFLASH_OK;
+}
+
+#define TRY(x)                    \
+  do {                            \
+    int rc_ = (x);                \
+    if (rc_ != DFLASH_OK) return rc_; \
+  } while (0)
+
+size_t src_bytes(int wt, int rows, int k) {
+  if (wt == WT_BF16) return size_t(rows) * k * 2;
+  const int bs = wt == WT_Q8_0 ? 34 : (wt == WT_Q4_0 ? 18 : 22);
+  return size_t(rows) * (k / 32) * bs;
+}
+
+int alloc_packed(PackedMatrix& pm, int wt, int n, int k, size_t* total) {
+  pm.wtype = wt;
+  pm.n = n;
+  pm.k = k;
+  pm.bytes = packed_bytes(wt, n, k);
+  TRY(dev_alloc(&pm.data, pm.bytes, total));
+  CK(cudaMemset(pm.data, 0, pm.bytes));
+  return DFLASH_OK;
+}
+
+int repack_into(PackedMatrix& pm, const void* src, int rows, int row_off, int interleave) {
+  CK(launch_repack(pm.wtype, src, rows, pm.k, pm.data, row_off, interleave, 0));
+  return DFLASH_OK;
+}
+
+void free_model(Model* m) {
+  if (!m) return;
+  auto f = [](void* p) { if (p) cudaFree(p); };
+  f(m->fc.data);
+  f(m->kv_all.data);
+  for (int l = 0; l < DFLASH_MAX_LAYERS; ++l) {
+    f(m->qkv[l].data);
+    f(m->o[l].data);
+    f(m->gu[l].data);
+    f(m->down[l].data);
+  }
+  f(m->hidden_norm);
+  f(m->attn_norm);
+  f(m->q_norm);
+  f(m->k_norm);
+  f(m->mlp_norm);
+  f(m->final_norm);
+  f(m->rope_turns);
+}
+
+void free_state(State* s) {
+  if (!s) return;
+  auto f = [](void* p) { if (p) cudaFree(p); };
+  f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
+  f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
+  f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->status);
+}
+
+int pow2ceil(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* status) {
+  GemvArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.W = pm.data;
+  a.N = pm.n;
+  a.K = pm.k;
+  a.UPG = pm.k / (32 * cb_of(pm.wtype));
+  a.U = (pm.n / 64) * a.UPG;
+  a.partials = st.partials;
+  a.counters = st.counters + static_cast<size_t>(region) * st.counter_stride;
+  a.status = status;
+  return a;
+}
+
+int grid_for(const Model& m, const GemvArgs& a) {
+  int g = m.sm_count;
+  if (g > a.U) g = a.U;
+  return g < 1 ? 1 : g;
+}
+
+int check_gemv(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DFLASH_OK;
+}
+
+cudaError_t gemv_store_any(int wt, int nt, const GemvArgs& a, const EpiStore& e, const LaunchCfg& lc) {
+  switch (wt) {
+    case WT_BF16: return gemv_store<WT_BF16>(nt, a, e, lc);
+    case WT_Q8_0: return gemv_store<WT_Q8_0>(nt, a, e, lc);
+    case WT_Q5_0: return gemv_store<WT_Q5_0>(nt, a, e, lc);
+    case WT_Q4_0: return gemv_store<WT_Q4_0>(nt, a, e, lc);
+  }
+  return cudaErrorInvalidValue;
+}
+cudaError_t gemv_resid_any(int wt, int nt, const GemvArgs& a, const EpiResid& e, const LaunchCfg& lc) {
+  switch (wt) {
+    case WT_BF16: return gemv_resid<WT_BF16>(nt, a, e, lc);
+    case WT_Q8_0: return gemv_resid<WT_Q8_0>(nt, a, e, lc);
+    case WT_Q5_0: return gemv_resid<WT_Q5_0>(nt, a, e, lc);
+    case WT_Q4_0: return gemv_resid<WT_Q4_0>(nt, a, e, lc);
+  }
+  return cudaErrorInvalidValue;
+}
+cudaError_t gemv_swiglu_any(int wt, int nt, const GemvArgs& a, void* h, int ldh, const LaunchCfg& lc) {
+  switch (wt) {
+    case WT_BF16: return gemv_swiglu<WT_BF16>(nt, a, h, ldh, lc);
+    case WT_Q8_0: return gemv_swiglu<WT_Q8_0>(nt, a, h, ldh, lc);
+    case WT_Q5_0: return gemv_swiglu<WT_Q5_0>(nt, a, h, ldh, lc);
+    case WT_Q4_0: return gemv_swiglu<WT_Q4_0>(nt, a, h, ldh, lc);
+  }
+  return cudaErrorInvalidValue;
+}
+cudaError_t gemv_heads_any(int wt, int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
+  switch (wt) {
+    case WT_BF16: return gemv_heads<WT_BF16>(nt, a, e, lc);
+    case WT_Q8_0: return gemv_heads<WT_Q8_0>(nt, a, e, lc);
+    case WT_Q5_0: return gemv_heads<WT_Q5_0>(nt, a, e, lc);
+    case WT_Q4_0: return gemv_heads<WT_Q4_0>(nt, a, e, lc);
+  }
+  return cudaErrorInvalidValue;
+}
+
+bool is_dev_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_status_string(int status) {
+  switch (status) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DFLASH_ERR_CAPACITY: return "request exceeds the state's capacity";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_NO_DEVICE: return "no usable sm_100+ GPU";
+    case DFLASH_ERR_OUT_OF_MEMORY: return "out of device memory";
+  }
+  return "unknown status";
+}
+
+const char* dflash_last_cuda_error(void) { return g_cuda_err; }
+
+int dflash_config_check(const dflash_config* c) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->n_layers > DFLASH_MAX_LAYERS) return DFLASH_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return DFLASH_ERR_UNSUPPORTED;
+  const int gq = c->n_q_heads / c->n_kv_heads;
+  if ((gq * 8) % 16 || gq * 8 > 224) return DFLASH_ERR_UNSUPPORTED;
+  if (c->hidden < 256 || c->hidden % 256) return DFLASH_ERR_UNSUPPORTED;
+  if ((c->n_q_heads * c->head_dim) % 256 || c->intermediate < 256 || c->intermediate % 256)
+    return DFLASH_ERR_UNSUPPORTED;
+  if ((c->n_kv_heads * c->head_dim) % 64) return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_taps < 1 || c->n_taps > 64) return DFLASH_ERR_UNSUPPORTED;
+  if (c->vocab < 2) return DFLASH_ERR_UNSUPPORTED;
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return DFLASH_ERR_INVALID_ARG;
+  if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta)) return DFLASH_ERR_INVALID_ARG;
+  if (!(c->norm_eps >= 0.f) || !std::isfinite(c->norm_eps)) return DFLASH_ERR_INVALID_ARG;
+  if (c->weight_type < DFLASH_WT_BF16 || c->weight_type > DFLASH_WT_Q4_0) return DFLASH_ERR_UNSUPPORTED;
+  // K/V arena rows and head rows must fit 32-bit tensor-map coordinates
+  if (static_cast<long long>(c->vocab) > 0x7fffffffLL) return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+
+size_t dflash_model_device_bytes(const dflash_model* m) { return m ? m->device_bytes : 0; }
+size_t dflash_state_device_bytes(const dflash_state* s) { return s ? s->device_bytes : 0; }
+
+int dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model** out) {
+  if (!cfg || !w || !out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  TRY(dflash_config_check(cfg));
+  const dflash_config& c = *cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate;
+  if (!w->fc || !w->hidden_norm || !w->final_norm || !w->embed || !w->head) return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    const void* ps[] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.q_norm, lw.k_norm, lw.wo, lw.mlp_norm,
+                        lw.w_gate, lw.w_up, lw.w_down};
+    for (const void* p : ps)
+      if (!p) return DFLASH_ERR_INVALID_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(w->head) % 16) return DFLASH_ERR_INVALID_ARG;
+  int dev = 0;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return DFLASH_ERR_NO_DEVICE;
+  }
+  CK(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major < 10) return DFLASH_ERR_NO_DEVICE;
+  if (!is_dev_ptr(w->fc) || !is_dev_ptr(w->head) || !is_dev_ptr(w->embed)) return DFLASH_ERR_INVALID_ARG;
+
+  dflash_model* m = new (std::nothrow) dflash_model();
+  if (!m) return DFLASH_ERR_OUT_OF_MEMORY;
+  m->cfg = c;
+  m->wtype = c.weight_type;
+  m->device = dev;
+  m->sm_count = prop.multiProcessorCount;
+  m->embed = static_cast<const uint16_t*>(w->embed);
+  m->head = static_cast<const uint16_t*>(w->head);
+  size_t total = 0;
+  const int wt = c.weight_type;
+  auto fail = [&](int rc) {
+    free_model(m);
+    delete m;
+    return rc;
+  };
+  int rc;
+#define MTRY(x)                      \
+  do {                               \
+    if ((rc = (x)) != DFLASH_OK) return fail(rc); \
+  } while (0)
+  const int nqkv = (nq + 2 * nkv) * d;
+  MTRY(alloc_packed(m->fc, wt, H, c.n_taps * H, &total));
+  MTRY(repack_into(m->fc, w->fc, H, 0, -1));
+  MTRY(alloc_packed(m->kv_all, wt, L * 2 * nkv * d, H, &total));
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    MTRY(alloc_packed(m->qkv[l], wt, nqkv, H, &total));
+    MTRY(repack_into(m->qkv[l], lw.wq, nq * d, 0, -1));
+    MTRY(repack_into(m->qkv[l], lw.wk, nkv * d, nq * d, -1));
+    MTRY(repack_into(m->qkv[l], lw.wv, nkv * d, (nq + nkv) * d, -1));
+    MTRY(repack_into(m->kv_all, lw.wk, nkv * d, l * 2 * nkv * d, -1));
+    MTRY(repack_into(m->kv_all, lw.wv, nkv * d, l * 2 * nkv * d + nkv * d, -1));
+    MTRY(alloc_packed(m->o[l], wt, H, nq * d, &total));
+    MTRY(repack_into(m->o[l], lw.wo, H, 0, -1));
+    MTRY(alloc_packed(m->gu[l], wt, 2 * I, H, &total));
+    MTRY(repack_into(m->gu[l], lw.w_gate, I, 0, 0));
+    MTRY(repack_into(m->gu[l], lw.w_up, I, 0, 1));
+    MTRY(alloc_packed(m->down[l], wt, H, I, &total));
+    MTRY(repack_into(m->down[l], lw.w_down, H, 0, -1));
+  }
+  MTRY(dev_alloc(&m->hidden_norm, H * 4, &total));
+  MTRY(dev_alloc(&m->attn_norm, size_t(L) * H * 4, &total));
+  MTRY(dev_alloc(&m->q_norm, size_t(L) * d * 4, &total));
+  MTRY(dev_alloc(&m->k_norm, size_t(L) * d * 4, &total));
+  MTRY(dev_alloc(&m->mlp_norm, size_t(L) * H * 4, &total));
+  MTRY(dev_alloc(&m->final_norm, H * 4, &total));
+  MTRY(convert_norm(w->hidden_norm, m->hidden_norm, H, 0));
+  MTRY(convert_norm(w->final_norm, m->final_norm, H, 0));
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    MTRY(convert_norm(lw.attn_norm, m->attn_norm + size_t(l) * H, H, 0));
+    MTRY(convert_norm(lw.q_norm, m->q_norm + size_t(l) * d, d, 0));
+    MTRY(convert_norm(lw.k_norm, m->k_norm + size_t(l) * d, d, 0));
+    MTRY(convert_norm(lw.mlp_norm, m->mlp_norm + size_t(l) * H, H, 0));
+  }
+  // RoPE frequencies as 0.64 fixed-point turns: inv_freq_i / (2 pi) * 2^64.
+  {
+    uint64_t turns[128];
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < d / 2; ++i) {
+      const double inv_freq = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / d);
+      const double t = std::ldexp(inv_freq / two_pi, 64);
+      turns[i] = t >= 18446744073709551615.0 ? ~0ull : static_cast<uint64_t>(t);
+    }
+    MTRY(dev_alloc(&m->rope_turns, sizeof(uint64_t) * (d / 2), &total));
+    if (cudaMemcpy(m->rope_turns, turns, sizeof(uint64_t) * (d / 2), cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(cuda_fail(cudaGetLastError(), "cudaMemcpy rope turns"));
+  }
+  MTRY(make_map_2d(&m->head_map, w->head, static_cast<uint64_t>(c.vocab), static_cast<uint64_t>(H),
+                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16));
+  {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(cuda_fail(e, "model create"));
+  }
+  m->device_bytes = total;
+#undef MTRY
+  *out = m;
+  return DFLASH_OK;
+}
+
+int dflash_model_destroy(dflash_model* m) {
+  if (!m) return DFLASH_ERR_INVALID_ARG;
+  free_model(m);
+  delete m;
+  return DFLASH_OK;
+}
+
+int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity, dflash_state** out) {
+  if (!m || !out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (n_slots < 1 || n_slots > DFLASH_MAX_SLOTS) return DFLASH_ERR_INVALID_ARG;
+  if (capacity < DFLASH_MAX_BLOCK) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = m->cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate;
+  const long long arena_rows = static_cast<long long>(L) * n_slots * nkv * capacity;
+  if (arena_rows > 0x7fffffffLL) return DFLASH_ERR_CAPACITY;
+  dflash_state* s = new (std::nothrow) dflash_state();
+  if (!s) return DFLASH_ERR_OUT_OF_MEMORY;
+  auto fail = [&](int rc) {
+    free_state(s);
+    delete s;
+    return rc;
+  };
+  int rc;
+#define STRY(x)                      \
+  do {                               \
+    if ((rc = (x)) != DFLASH_OK) return fail(rc); \
+  } while (0)
+  s->model = m;
+  s->n_slots = n_slots;
+  s->capacity = capacity;
+  s->nt = pow2ceil(n_slots);
+  s->rows = s->nt * 8;
+  const int R = s->rows;
+  const int gq = nq / nkv;
+  const int M = gq * 8;
+  {
+    long long want = (capacity + 255) / 256;
+    long long maxc = (2LL * m->sm_count) / (static_cast<long long>(n_slots) * nkv);
+    if (maxc < 1) maxc = 1;
+    if (want > maxc) want = maxc;
+    if (want < 1) want = 1;
+    s->attn_chunks = static_cast<int>(want);
+  }
+  size_t total = 0;
+  const size_t kv_elems = static_cast<size_t>(arena_rows) * d;
+  STRY(dev_alloc(&s->K, kv_elems * 2, &total));
+  STRY(dev_alloc(&s->V, kv_elems * 2, &total));
+  if (cudaMemset(s->K, 0, kv_elems * 2) != cudaSuccess || cudaMemset(s->V, 0, kv_elems * 2) != cudaSuccess)
+    return fail(cuda_fail(cudaGetLastError(), "cudaMemset K/V"));
+  const int nqkv = (nq + 2 * nkv) * d;
+  STRY(dev_alloc(&s->x, size_t(R) * H * 4, &total));
+  STRY(dev_alloc(&s->qkv_raw, size_t(R) * nqkv * 4, &total));
+  STRY(dev_alloc(&s->q_ready, size_t(R) * nq * d * 2, &total));
+  STRY(dev_alloc(&s->attn_out, size_t(R) * nq * d * 2, &total));
+  STRY(dev_alloc(&s->hbuf, size_t(R) * I * 2, &total));
+  STRY(dev_alloc(&s->xnorm, size_t(R) * H * 2, &total));
+  STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks * M * d * 4, &total));
+  STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks * M * 8, &total));
+  s->max_grid = 2 * m->sm_count;
+  const int rmax = 128;
+  STRY(dev_alloc(&s->partials, size_t(s->max_grid) * 2 * 64 * rmax * 4, &total));
+  {
+    int stride = c.vocab / 64 + 1;
+    const int cands[] = {nqkv / 64, H / 64, 2 * I / 64, L * 2 * nkv * d / 64, nq + 2 * nkv, L * 2 * nkv, 16};
+    for (int v : cands) stride = stride > v ? stride : v + 1;
+    s->counter_stride = stride;
+  }
+  STRY(dev_alloc(&s->counters, size_t(CNT_REGIONS) * s->counter_stride * 4, &total));
+  if (cudaMemset(s->counters, 0, size_t(CNT_REGIONS) * s->counter_stride * 4) != cudaSuccess)
+    return fail(cuda_fail(cudaGetLastError(), "cudaMemset counters"));
+  STRY(dev_alloc(&s->argmax_slots, size_t(s->max_grid) * rmax * 8, &total));
+  STRY(dev_alloc(&s->nonfinite, 16, &total));
+  s->fuse_rows = 128;
+  STRY(dev_alloc(&s->h_raw, size_t(s->fuse_rows) * H * 4, &total));
+  STRY(dev_alloc(&s->kv_raw, size_t(s->fuse_rows) * L * 2 * nkv * d * 4, &total));
+  STRY(dev_alloc(&s->fuse_xnorm, size_t(s->fuse_rows) * H * 2, &total));
+  STRY(dev_alloc(&s->status, 16, &total));
+  if (cudaMemset(s->status, 0, 16) != cudaSuccess) return fail(cuda_fail(cudaGetLastError(), "cudaMemset"));
+  STRY(make_map_2d(&s->k_map, s->K, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+  STRY(make_map_2d(&s->v_map, s->V, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+  {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(cuda_fail(e, "state create"));
+  }
+  s->device_bytes = total;
+#undef STRY
+  *out = s;
+  return DFLASH_OK;
+}
+
+int dflash_state_destroy(dflash_state* s) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  free_state(s);
+  delete s;
+  return DFLASH_OK;
+}
+
+int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, const uint16_t* taps,
+                        const int32_t* positions, int32_t n, int32_t* dev_status, dflash_stream_t stream_) {
+  if (!m || !s || s->model != m) return DFLASH_ERR_INVALID_ARG;
+  if (slot < 0 || slot >= s->n_slots || n < 0) return DFLASH_ERR_INVALID_ARG;
+  if (n == 0) return DFLASH_OK;
+  if (!taps || !positions) return DFLASH_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(taps) % 16) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const dflash_config& c = m->cfg;
+  const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers;
+  const int wt = m->wtype;
+  int32_t* status = dev_status ? dev_status : s->status;
+  const int tw = c.n_taps * H;
+  for (int base = 0; base < n; base += s->fuse_rows) {
+    const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
+    const int nt = rows <= 8 ? 1 : 16;
+    // fc: h_raw = taps . W_fc^T
+    {
+      GemvArgs a = base_args(m->fc, *s, CNT_FC, status);
+      a.n_valid_rows = rows;
+      a.X = taps + static_cast<size_t>(base) * tw;
+      a.ldx = tw;
+      EpiStore e{s->h_raw, H};
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
+    }
+    // K/V of every layer from rmsnorm(h_raw) * hidden_norm
+    {
+      GemvArgs a = base_args(m->kv_all, *s, CNT_KV, status);
+      a.n_valid_rows = rows;
+      a.eps = c.norm_eps;
+      if (nt == 1) {
+        a.X = s->h_raw;
+        a.ldx = H;
+        a.norm_w = m->hidden_norm;
+      } else {
+        NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0};
+        TRY(check_gemv(launch_rmsnorm_rows(na, nt * 8, stream), "fuse norm"));
+        a.X = s->fuse_xnorm;
+        a.ldx = H;
+      }
+      EpiHeads e;
+      std::memset(&e, 0, sizeof(e));
+      e.mode = 1;
+      e.raw = s->kv_raw;
+      e.ldr = L * 2 * nkv * d;
+      e.d = d;
+      e.n_q = c.n_q_heads;
+      e.n_kv = nkv;
+      e.gph = d / 64;
+      e.head_cnt = s->counters + static_cast<size_t>(CNT_KV_HEADS) * s->counter_stride;
+      e.k_norm = m->k_norm;
+      e.turns = m->rope_turns;
+      e.eps = c.norm_eps;
+      e.q_scale = 1.f;
+      e.Kst = s->K;
+      e.Vst = s->V;
+      e.n_slots = s->n_slots;
+      e.cap = s->capacity;
+      e.slot = slot;
+      e.positions = positions + base;
+      e.n_valid = rows;
+      e.status = status;
+      e.rows_ = nt * 8;
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "fuse kv"));
+    }
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, const int32_t* anchor_tok,
+                       const int32_t* anchor_pos, const int32_t* block_len, int32_t* drafts, float* final_hidden,
+                       int32_t* dev_status, dflash_stream_t stream_) {
+  if (!m || !s || s->model != m) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > s->n_slots) return DFLASH_ERR_INVALID_ARG;
+  if (!anchor_tok || !anchor_pos || !block_len || !drafts) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const dflash_config& c = m->cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate;
+  const int wt = m->wtype;
+  const int nt = pow2ceil(n_seq);
+  const int R = nt * 8;
+  int32_t* status = dev_status ? dev_status : s->status;
+  const bool f16 = wt != WT_BF16;
+
+  {
+    EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
+                 s->capacity, status};
+    TRY(check_gemv(launch_embed(ea, nt, stream), "embed"));
+  }
+  for (int l = 0; l < L; ++l) {
+    // q, k, v projections with per-head norm, RoPE and block K/V cells
+    {
+      GemvArgs a = base_args(m->qkv[l], *s, CNT_QKV, status);
+      a.n_valid_rows = R;
+      a.eps = c.norm_eps;
+      if (nt == 1) {
+        a.X = s->x;
+        a.ldx = H;
+        a.norm_w = m->attn_norm + size_t(l) * H;
+      } else {
+        NormArgs na{s->x, m->attn_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0};
+        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "attn norm"));
+        a.X = s->xnorm;
+        a.ldx = H;
+      }
+      EpiHeads e;
+      std::memset(&e, 0, sizeof(e));
+      e.mode = 0;
+      e.raw = s->qkv_raw;
+      e.ldr = (nq + 2 * nkv) * d;
+      e.d = d;
+      e.n_q = nq;
+      e.n_kv = nkv;
+      e.gph = d / 64;
+      e.head_cnt = s->counters + static_cast<size_t>(CNT_QKV_HEADS) * s->counter_stride;
+      e.q_norm = m->q_norm + size_t(l) * d;
+      e.k_norm = m->k_norm + size_t(l) * d;
+      e.turns = m->rope_turns;
+      e.eps = c.norm_eps;
+      e.q_scale = 1.f / std::sqrt(static_cast<float>(d));
+      e.q_ready = s->q_ready;
+      e.Kst = s->K;
+      e.Vst = s->V;
+      e.layer = l;
+      e.n_slots = s->n_slots;
+      e.cap = s->capacity;
+      e.n_seq = n_seq;
+      e.anchor_pos = anchor_pos;
+      e.block_len = block_len;
+      e.status = status;
+      e.rows_ = R;
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "qkv"));
+    }
+    TRY(check_gemv(launch_attention(*m, *s, l, n_seq, anchor_pos, block_len, status, stream), "attention"));
+    {
+      GemvArgs a = base_args(m->o[l], *s, CNT_O, status);
+      a.n_valid_rows = R;
+      a.X = s->attn_out;
+      a.ldx = nq * d;
+      EpiResid e{s->x, H};
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
+    }
+    {
+      GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
+      a.n_valid_rows = R;
+      a.eps = c.norm_eps;
+      if (nt == 1) {
+        a.X = s->x;
+        a.ldx = H;
+        a.norm_w = m->mlp_norm + size_t(l) * H;
+      } else {
+        NormArgs na{s->x, m->mlp_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0};
+        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "mlp norm"));
+        a.X = s->xnorm;
+        a.ldx = H;
+      }
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_swiglu_any(wt, nt, a, s->hbuf, I, lc), "gate/up"));
+    }
+    {
+      GemvArgs a = base_args(m->down[l], *s, CNT_DOWN, status);
+      a.n_valid_rows = R;
+      a.X = s->hbuf;
+      a.ldx = I;
+      EpiResid e{s->x, H};
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
+    }
+  }
+  // final norm + LM head + argmax
+  {
+    GemvArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.wmap = m->head_map;
+    a.N = ((c.vocab + 63) / 64) * 64;
+    a.K = H;
+    a.UPG = H / 128;
+    a.U = (a.N / 64) * a.UPG;
+    a.n_valid_rows = R;
+    a.eps = c.norm_eps;
+    a.partials = s->partials;
+    a.counters = s->counters + static_cast<size_t>(CNT_HEAD) * s->counter_stride;
+    a.status = status;
+    ArgmaxParams p;
+    p.vocab = c.vocab;
+    p.n_seq = n_seq;
+    p.H = H;
+    p.block_len = block_len;
+    p.drafts = drafts;
+    p.slots = s->argmax_slots;
+    p.grid_cnt = s->counters + static_cast<size_t>(CNT_ARGMAX) * s->counter_stride;
+    p.final_hidden = final_hidden;
+    p.x = s->x;
+    p.norm_w = m->final_norm;
+    p.status = status;
+    if (nt == 1) {
+      a.X = s->x;
+      a.ldx = H;
+      a.norm_w = m->final_norm;
+    } else {
+      NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8};
+      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "final norm"));
+      a.X = s->xnorm;
+      a.ldx = H;
+      p.final_hidden = nullptr;
+    }
+    LaunchCfg lc{stream, grid_for(*m, a), true};
+    if (s->head_ev_begin) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_begin), stream));
+    TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
+    if (s->head_ev_end) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_end), stream));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_accept(const int32_t* drafts, const int32_t* target_ids, const int32_t* block_len, int32_t n_seq,
+                  int32_t max_block_len, int32_t* accept_len, int32_t* next_anchor, int32_t* anchor_pos_inout,
+                  dflash_stream_t stream) {
+  if (!drafts || !target_ids || !block_len || !accept_len || !next_anchor) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || max_block_len < DFLASH_MIN_BLOCK || max_block_len > DFLASH_MAX_BLOCK)
+    return DFLASH_ERR_INVALID_ARG;
+  TRY(check_gemv(launch_accept(drafts, target_ids, block_len, n_seq, max_block_len, accept_len, next_anchor,
+                               anchor_pos_inout, reinterpret_cast<cudaStream_t>(stream)),
+                 "accept"));
+  return DFLASH_OK;
+}
+
+int dflash_state_read_kv(const dflash_state* s, int32_t slot, int32_t layer, int32_t pos0, int32_t n, float* k_out,
+                         float* v_out, dflash_stream_t stream) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = s->model->cfg;
+  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 ||
+      static_cast<long long>(pos0) + n > s->capacity)
+    return DFLASH_ERR_INVALID_ARG;
+  const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (k_out)
+    TRY(check_gemv(launch_kv_copy(false, s->K + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, k_out, nullptr, st),
+                   "read k"));
+  if (v_out)
+    TRY(check_gemv(launch_kv_copy(false, s->V + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, v_out, nullptr, st),
+                   "read v"));
+  return DFLASH_OK;
+}
+
+int dflash_state_write_kv(dflash_state* s, int32_t slot, int32_t layer, int32_t pos0, int32_t n, const uint16_t* k_in,
+                          const uint16_t* v_in, dflash_stream_t stream) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = s->model->cfg;
+  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 ||
+      static_cast<long long>(pos0) + n > s->capacity)
+    return DFLASH_ERR_INVALID_ARG;
+  const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (k_in)
+    TRY(check_gemv(launch_kv_copy(true, s->K + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, nullptr, k_in, st),
+                   "write k"));
+  if (v_in)
+    TRY(check_gemv(launch_kv_copy(true, s->V + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, nullptr, v_in, st),
+                   "write v"));
+  return DFLASH_OK;
+}
+
+int dflash_state_status(dflash_state* s, int32_t* status_out, dflash_stream_t stream) {
+  if (!s || !status_out) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(status_out, s->status, 4, cudaMemcpyDeviceToHost, st));
+  CK(cudaMemsetAsync(s->status, 0, 4, st));
+  CK(cudaStreamSynchronize(st));
+  return DFLASH_OK;
+}
+
+int dflash_model_dequantize(const dflash_model* m, int32_t which, float* out, dflash_stream_t stream) {
+  if (!m || !out) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = m->cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate;
+  if (which < 0 || which > 7 * L) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const PackedMatrix* pm;
+  int row_off = 0, rows = 0, inter = -1;
+  if (which == 0) {
+    pm = &m->fc;
+    rows = H;
+  } else {
+    const int l = (which - 1) / 7, k = (which - 1) % 7;
+    switch (k) {
+      case 0: pm = &m->qkv[l]; rows = nq * d; break;
+      case 1: pm = &m->qkv[l]; rows = nkv * d; row_off = nq * d; break;
+      case 2: pm = &m->qkv[l]; rows = nkv * d; row_off = (nq + nkv) * d; break;
+      case 3: pm = &m->o[l]; rows = H; break;
+      case 4: pm = &m->gu[l]; rows = I; inter = 0; break;
+      case 5: pm = &m->gu[l]; rows = I; inter = 1; break;
+      default: pm = &m->down[l]; rows = H; break;
+    }
+  }
+  TRY(check_gemv(launch_dequant(pm->wtype, pm->data, pm->n, pm->k, out, row_off, rows, inter, st), "dequant"));
+  return DFLASH_OK;
+}
+
+int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
+  if (!s || n_seq < 1 || n_seq > s->n_slots) return -1;
+  const int L = s->model->cfg.n_layers;
+  const bool streamed = pow2ceil(n_seq) > 1;  // separate RMSNorm kernels before qkv, gate/up and head
+  const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
+  return 1 + L * per_layer + 1 + (streamed ? 1 : 0);
+}
+
+int32_t dflash_fuse_launches(const dflash_state* s, int32_t n) {
+  if (!s || n < 0) return -1;
+  int k = 0;
+  for (int base = 0; base < n; base += s->fuse_rows) {
+    const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
+    k += rows <= 8 ? 2 : 3;
+  }
+  return k;
+}
+
+int dflash_state_set_head_events(dflash_state* s, void* ev_begin, void* ev_end) {
+  if (!s || (ev_begin == nullptr) != (ev_end == nullptr)) return DFLASH_ERR_INVALID_ARG;
+  s->head_ev_begin = ev_begin;
+  s->head_ev_end = ev_end;
+  return DFLASH_OK;
+}
+
+}  // extern "C"

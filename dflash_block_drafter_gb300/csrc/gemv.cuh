@@ -1,0 +1,357 @@
+// Weight-streaming skinny GEMM ("GEMV" over up to 128 activation rows):
+//     Y[R, N] = X[R, K] . W[N, K]^T,   R = 8 * NT
+// followed by a fused epilogue.  Each weight byte is read from HBM exactly
+// once per launch.
+//
+// Work split: the matrix is cut into units of 64 rows x (32 * CB) inputs;
+// units are ordered group-major and the grid is given equal contiguous
+// ranges of units (stream-K).  A CTA = 4 consumer warps (one 16-row m-tile
+// each) + 1 producer warp.  The producer streams the CTA's range through a
+// ring of shared-memory stages with bulk copies (one per unit, plus the
+// matching X chunk when X is streamed) completing on mbarriers; weight
+// copies for the first stages are issued before the programmatic-dependent-
+// launch wait, so they overlap the previous kernel's tail.  Consumers build
+// mma.sync m16n8k16 fragments straight from the stage (layout.cuh), apply
+// the per-32-block quantisation scales in fp32 between blocks, and
+// accumulate in registers.  A group whose units were split between CTAs is
+// finished by whichever contributor arrives last (deterministic summation
+// order over contributors, no waiting).
+#pragma once
+
+#include "layout.cuh"
+
+namespace dflash {
+
+struct GemvArgs {
+  CUtensorMap wmap;  // WT_HEAD only
+  const uint8_t* W;              // packed weights (fragment-native formats)
+  int N, K;                      // logical rows / inputs
+  int UPG;                       // units per 64-row group
+  int U;                         // total units
+  int n_valid_rows;              // activation rows that exist (others are zero)
+  // X_STREAM: activation rows [R, ldx] (bf16 or fp16 per weight type)
+  // X_RESIDENT: fp32 rows [R, ldx] normalised with norm_w in the prologue
+  const void* X;
+  int ldx;
+  const float* norm_w;
+  float eps;
+  float* partials;               // [gridDim.x, 2, 64, R]
+  int* counters;                 // [N / 64]
+  int32_t* status;
+};
+
+template <int WT, int NT, int XMODE>
+struct GemvGeom {
+  using F = Fmt<WT>;
+  static constexpr int R = NT * 8;
+  static constexpr int KU = F::CB * 32;                 // inputs per unit
+  static constexpr int XS_STRIDE = KU * 2 + 64;         // streamed X row stride (bytes, padded)
+  static constexpr bool kStream = XMODE == X_STREAM || XMODE == X_STREAM_BF16;
+  // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
+  static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16;
+  static constexpr int XS_BYTES = kStream ? R * XS_STRIDE : 0;
+  static constexpr int STAGE = ((F::UNIT + XS_BYTES + 1023) / 1024) * 1024;
+  // as many stages as the format asks for, within ~190 KB of ring
+  static constexpr int STAGES_FIT = 190000 / STAGE;
+  static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int THREADS = 160;
+  // smem: [ring][X resident][barriers][misc]
+  static __host__ __device__ constexpr int xres_stride(int K) { return K * 2 + 64; }
+  static __host__ __device__ constexpr int xres_bytes(int K) {
+    return (XMODE == X_RESIDENT) ? ((R * xres_stride(K) + 127) / 128) * 128 : 0;
+  }
+  static constexpr int MISC = 2 * 8 * STAGES + 64 + 4 * R * 8 + R * 4;
+  static __host__ __device__ constexpr int smem_bytes(int K) { return 1024 + RING + xres_bytes(K) + MISC; }
+};
+
+// Epilogue interface (see gemv_epilogues.cuh):
+//   struct Epi {
+//     static constexpr bool kAfterGroup;   // needs a CTA-wide step after a group
+//     static constexpr bool kFinish;       // needs a CTA-wide step at the end
+//     struct Local { ... };                // per-thread registers across groups
+//     __device__ void init(Local&) const;
+//     __device__ void prologue(const GemvArgs&, int tid) const;     // consumers, after X is ready
+//     __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const;
+//     __device__ void after_group(const GemvArgs&, int g, int tid, int* sflag) const;
+//     __device__ void finish(const GemvArgs&, Local&, int w, int lane, int tid, unsigned long long* stage,
+//                            int* sflag) const;
+//   };
+
+__device__ __forceinline__ int cta_of_unit(long long u, int G, int U) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+template <int WT, int NT, int XMODE, class Epi>
+__global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ Epi epi) {
+  using Geo = GemvGeom<WT, NT, XMODE>;
+  using F = Fmt<WT>;
+  constexpr int R = Geo::R;
+  constexpr int STAGES = Geo::STAGES;
+  constexpr bool kF16 = Geo::kF16;
+  constexpr bool kStream = Geo::kStream;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* xres = ring + Geo::RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(xres + Geo::xres_bytes(a.K));
+  uint64_t* empty = full + STAGES;
+  int* sflag = reinterpret_cast<int*>(empty + STAGES);               // 16 ints
+  float* srs = reinterpret_cast<float*>(sflag + 16);                 // [R] row scales
+  unsigned long long* sstage = reinterpret_cast<unsigned long long*>(srs + R);  // [4][R]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.U) / G);
+  const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
+  const int n_units = u_end - u_begin;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    fence_barrier_init();
+  }
+  if constexpr (kStream) {
+    // rows that are never copied (beyond n_valid_rows) must read as zeros
+    if (a.n_valid_rows < R) {
+      for (int s = 0; s < STAGES; ++s) {
+        uint8_t* xs = ring + s * Geo::STAGE + F::UNIT;
+        for (int i = tid; i < (R - a.n_valid_rows) * (Geo::XS_STRIDE / 16); i += Geo::THREADS) {
+          const int rr = a.n_valid_rows + i / (Geo::XS_STRIDE / 16);
+          reinterpret_cast<uint4*>(xs + rr * Geo::XS_STRIDE)[i % (Geo::XS_STRIDE / 16)] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      if constexpr (WT == WT_HEAD) prefetch_tensormap(&a.wmap);
+      const uint64_t pol = l2_policy_evict_first();
+      constexpr int XBYTES_ROW = Geo::KU * 2;
+      const uint32_t tx = F::UNIT + (kStream ? a.n_valid_rows * XBYTES_ROW : 0);
+      auto issue_w = [&](int it, int u) {
+        uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
+        if constexpr (WT == WT_HEAD) {
+          const int g = u / a.UPG, j = u - g * a.UPG;
+          tma_load_2d_hint(dst, &a.wmap, j * 128, g * 64, &full[it % STAGES], pol);
+          tma_load_2d_hint(dst + 8192, &a.wmap, j * 128 + 64, g * 64, &full[it % STAGES], pol);
+        } else {
+          bulk_g2s_hint(dst, a.W + static_cast<size_t>(u) * F::UNIT, F::UNIT, &full[it % STAGES], pol);
+        }
+      };
+      auto issue_x = [&](int it, int u) {
+        if constexpr (kStream) {
+          const int j = u % a.UPG;
+          uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
+          const uint8_t* src = static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XBYTES_ROW;
+          for (int r = 0; r < a.n_valid_rows; ++r)
+            bulk_g2s(dst + r * Geo::XS_STRIDE, src + static_cast<size_t>(r) * a.ldx * 2, XBYTES_ROW,
+                     &full[it % STAGES]);
+        }
+      };
+      const int n_pre = n_units < STAGES ? n_units : STAGES;
+      for (int it = 0; it < n_pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], tx);
+        issue_w(it, u_begin + it);
+      }
+      pdl_wait();  // activations below come from the previous kernel
+      for (int it = 0; it < n_pre; ++it) issue_x(it, u_begin + it);
+      int issued = n_pre;
+      for (int it = n_pre; it < n_units; ++it) {
+        const int s = it % STAGES;
+        if (!mbar_wait(&empty[s], ((it / STAGES) - 1) & 1)) {
+          set_status(a.status, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], tx);
+        issue_w(it, u_begin + it);
+        issue_x(it, u_begin + it);
+        issued = it + 1;
+      }
+      // Every issued copy must land before the CTA may exit.
+      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+        if (!mbar_wait(&full[it % STAGES], (it / STAGES) & 1)) {
+          set_status(a.status, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();
+  pdl_launch_dependents();
+  const int w = warp;
+
+  if constexpr (XMODE == X_RESIDENT) {
+    // X = RMSNorm(x) * w for all R rows and the full K, into shared memory.
+    const float* x = static_cast<const float*>(a.X);
+    for (int r = w; r < R; r += 4) {
+      float ss = 0.f;
+      if (r < a.n_valid_rows) {
+        const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * a.ldx);
+        for (int i = lane; i < a.K / 4; i += 32) {
+          const float4 v = __ldcg(xr + i);
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
+    }
+    named_bar_sync(1, 128);
+    const int xstride = Geo::xres_stride(a.K);
+    const int k8 = a.K / 8;
+    for (int i = tid; i < R * k8; i += 128) {
+      const int r = i / k8, kk = (i - r * k8) * 8;
+      const float s = srs[r];
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (r < a.n_valid_rows) {
+        const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * a.ldx + kk);
+        const float4* wr = reinterpret_cast<const float4*>(a.norm_w + kk);
+        const float4 x0 = __ldcg(xr), x1 = __ldcg(xr + 1);
+        const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
+        if constexpr (kF16) {
+          o.x = pack_f16x2(x0.x * s * w0.x, x0.y * s * w0.y);
+          o.y = pack_f16x2(x0.z * s * w0.z, x0.w * s * w0.w);
+          o.z = pack_f16x2(x1.x * s * w1.x, x1.y * s * w1.y);
+          o.w = pack_f16x2(x1.z * s * w1.z, x1.w * s * w1.w);
+        } else {
+          o.x = pack_bf16x2(x0.x * s * w0.x, x0.y * s * w0.y);
+          o.y = pack_bf16x2(x0.z * s * w0.z, x0.w * s * w0.w);
+          o.z = pack_bf16x2(x1.x * s * w1.x, x1.y * s * w1.y);
+          o.w = pack_bf16x2(x1.z * s * w1.z, x1.w * s * w1.w);
+        }
+      }
+      *reinterpret_cast<uint4*>(xres + r * xstride + kk * 2) = o;
+    }
+  }
+  epi.prologue(a, tid, XMODE == X_RESIDENT ? srs : nullptr);
+  named_bar_sync(1, 128);
+
+  typename Epi::Local loc;
+  epi.init(loc);
+  float acc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+
+  const int first_group = u_begin / a.UPG;
+  const int xstride = (XMODE == X_RESIDENT) ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
+  const uint32_t ring_s = smem_u32(ring);
+  const uint32_t xres_s = smem_u32(xres);
+  const int xrow = lane >> 2, xcol = (lane & 3) * 16;  // bytes within a 32-block row segment
+  bool ok = true;
+
+  for (int it = 0; it < n_units && ok; ++it) {
+    const int u = u_begin + it;
+    const int s = it % STAGES;
+    if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
+      set_status(a.status, DFLASH_DEV_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const int g = u / a.UPG, j = u - g * a.UPG;
+    const uint32_t ubase = ring_s + s * Geo::STAGE;
+    uint32_t xb;
+    if constexpr (XMODE == X_RESIDENT)
+      xb = xres_s + xrow * xstride + j * Geo::KU * 2 + xcol;
+    else
+      xb = ubase + F::UNIT + xrow * xstride + xcol;
+
+#pragma unroll
+    for (int bl = 0; bl < F::CB; ++bl) {
+      const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint4 xf = lds128(xb + t * 8 * xstride + bl * 64);
+        if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
+          mma_bf16_16816(acc[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
+          mma_bf16_16816(acc[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+        } else {
+          float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (kF16) {
+            mma_f16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
+            mma_f16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+          } else {
+            mma_bf16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
+            mma_bf16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+          }
+          acc[t][0] = fmaf(f.d_r, tmp[0], acc[t][0]);
+          acc[t][1] = fmaf(f.d_r, tmp[1], acc[t][1]);
+          acc[t][2] = fmaf(f.d_r8, tmp[2], acc[t][2]);
+          acc[t][3] = fmaf(f.d_r8, tmp[3], acc[t][3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    if (j == a.UPG - 1 || u == u_end - 1) {
+      const bool complete = (g * a.UPG >= u_begin) && (j == a.UPG - 1);
+      if (complete) {
+        epi.template group<WT, NT>(a, loc, g, w, lane, acc);
+        if constexpr (Epi::kAfterGroup) {
+          named_bar_sync(1, 128);
+          epi.after_group(a, g, tid, sflag);
+        }
+      } else {
+        // ---------------------------------------------- split-group fix-up
+        const int which = (g == first_group) ? 0 : 1;
+        float* slot = a.partials + (static_cast<size_t>(blockIdx.x) * 2 + which) * 64 * R;
+        const int r0 = w * 16 + (lane >> 2);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int c0 = t * 8 + (lane & 3) * 2;
+          __stcg(reinterpret_cast<float2*>(slot + r0 * R + c0), make_float2(acc[t][0], acc[t][1]));
+          __stcg(reinterpret_cast<float2*>(slot + (r0 + 8) * R + c0), make_float2(acc[t][2], acc[t][3]));
+        }
+        __threadfence();
+        named_bar_sync(1, 128);
+        const long long ufirst = static_cast<long long>(g) * a.UPG;
+        const int c_first = cta_of_unit(ufirst, G, a.U);
+        const int c_last = cta_of_unit(ufirst + a.UPG - 1, G, a.U);
+        if (tid == 0) {
+          const int old = atomicAdd(&a.counters[g], 1);
+          sflag[0] = (old == c_last - c_first);
+        }
+        named_bar_sync(1, 128);
+        if (sflag[0]) {
+          __threadfence();
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+          for (int c = c_first; c <= c_last; ++c) {
+            const int cfg = static_cast<int>((static_cast<long long>(c) * a.U) / G) / a.UPG;
+            const int wc = (g == cfg) ? 0 : 1;
+            const float* sl = a.partials + (static_cast<size_t>(c) * 2 + wc) * 64 * R;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const int c0 = t * 8 + (lane & 3) * 2;
+              const float2 p0 = __ldcg(reinterpret_cast<const float2*>(sl + r0 * R + c0));
+              const float2 p1 = __ldcg(reinterpret_cast<const float2*>(sl + (r0 + 8) * R + c0));
+              acc[t][0] += p0.x; acc[t][1] += p0.y; acc[t][2] += p1.x; acc[t][3] += p1.y;
+            }
+          }
+          if (tid == 0) a.counters[g] = 0;
+          epi.template group<WT, NT>(a, loc, g, w, lane, acc);
+          if constexpr (Epi::kAfterGroup) {
+            named_bar_sync(1, 128);
+            epi.after_group(a, g, tid, sflag);
+          }
+        }
+        named_bar_sync(1, 128);  // sflag reuse
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    }
+  }
+  if constexpr (Epi::kFinish) epi.template finish<NT>(a, loc, w, lane, tid, sstage, sflag);
+}
+
+}  // namespace dflash

@@ -1,0 +1,375 @@
+// Fused epilogues of the weight-streaming GEMV (gemv.cuh).  Each receives the
+// fp32 result of one 16-row m-tile for all activation rows, as the mma.sync
+// C fragment: lane (r = lane/4, c = lane%4) holds, for n-tile t,
+//   acc[t][0..1] = Y[row t*8 + 2c + {0,1}][weight row m = r]
+//   acc[t][2..3] = Y[row t*8 + 2c + {0,1}][weight row m = r + 8]
+// where the weight row of the 64-row group is frag_row<WT>(w, m).
+#pragma once
+
+#include "gemv.cuh"
+
+namespace dflash {
+
+struct NoLocal {};
+
+// Y stored as fp32 [R, ldo] (activation row major).  Feature fusion: fc.
+struct EpiStore {
+  static constexpr bool kAfterGroup = false, kFinish = false;
+  using Local = NoLocal;
+  float* out;
+  int ldo;
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      out[static_cast<size_t>(n) * ldo + m0] = acc[t][0];
+      out[static_cast<size_t>(n + 1) * ldo + m0] = acc[t][1];
+      out[static_cast<size_t>(n) * ldo + m1] = acc[t][2];
+      out[static_cast<size_t>(n + 1) * ldo + m1] = acc[t][3];
+    }
+  }
+  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
+  template <int NT>
+  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
+};
+
+// Residual update x[R, ldx] += Y: attention output projection and MLP down
+// projection.  Every element has exactly one owner thread.
+struct EpiResid {
+  static constexpr bool kAfterGroup = false, kFinish = false;
+  using Local = NoLocal;
+  float* x;
+  int ldx;
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      x[static_cast<size_t>(n) * ldx + m0] += acc[t][0];
+      x[static_cast<size_t>(n + 1) * ldx + m0] += acc[t][1];
+      x[static_cast<size_t>(n) * ldx + m1] += acc[t][2];
+      x[static_cast<size_t>(n + 1) * ldx + m1] += acc[t][3];
+    }
+  }
+  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
+  template <int NT>
+  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
+};
+
+// SwiGLU: the packed gate/up matrix holds, in every 16-row m-tile, 8 gate
+// rows then the 8 up rows of the same outputs, so a lane owns gate (m = r)
+// and up (m = r + 8) of output o = g*32 + w*8 + r:  h[n][o] = silu(g) * u.
+template <bool kF16>
+struct EpiSwiglu {
+  static constexpr bool kAfterGroup = false, kFinish = false;
+  using Local = NoLocal;
+  void* h;  // [R, ldh] bf16 / fp16
+  int ldh;
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  __device__ static float silu(float v) { return v / (1.f + __expf(-v)); }
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int o = g * 32 + w * 8 + (lane >> 2);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      const float h0 = silu(acc[t][0]) * acc[t][2];
+      const float h1 = silu(acc[t][1]) * acc[t][3];
+      if constexpr (kF16) {
+        __half* hp = static_cast<__half*>(h);
+        hp[static_cast<size_t>(n) * ldh + o] = __float2half_rn(h0);
+        hp[static_cast<size_t>(n + 1) * ldh + o] = __float2half_rn(h1);
+      } else {
+        __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(h);
+        hp[static_cast<size_t>(n) * ldh + o] = __float2bfloat16_rn(h0);
+        hp[static_cast<size_t>(n + 1) * ldh + o] = __float2bfloat16_rn(h1);
+      }
+    }
+  }
+  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
+  template <int NT>
+  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
+};
+
+// Per-attention-head epilogue.  Group results are stored raw; the CTA that
+// completes the last 64-row group of a head (atomic counter, no waiting)
+// applies the per-head RMSNorm, the NeoX rotation and the FP16 rounding and
+// writes the results: queries to q_ready, keys and values into the
+// position-addressed state cells.
+//   mode 0 (draft QKV): heads [0, n_q) are queries, then n_kv key heads, then
+//     n_kv value heads; activation row n is block row n % 8 of slot n / 8 at
+//     position anchor_pos[slot] + n % 8.
+//   mode 1 (fusion K/V): per layer l, n_kv key heads then n_kv value heads;
+//     activation row n is committed position positions[n].
+struct EpiHeads {
+  static constexpr bool kAfterGroup = true, kFinish = false;
+  using Local = NoLocal;
+  int mode;
+  float* raw;       // [R, ldr]
+  int ldr;
+  int d, n_q, n_kv, gph;
+  int* head_cnt;
+  const float* q_norm;   // mode 0: this layer's [d]
+  const float* k_norm;   // mode 0: this layer's [d]; mode 1: all layers [L, d]
+  const uint64_t* turns; // [d/2]
+  float eps, q_scale;
+  __half* q_ready;       // [R, n_q, d]
+  __half* Kst;
+  __half* Vst;
+  int layer, n_slots, cap;
+  int n_seq;             // mode 0: slots in this pass
+  const int32_t* anchor_pos;
+  const int32_t* block_len;
+  int slot;              // mode 1
+  const int32_t* positions;  // mode 1: [n_valid] of this tile
+  int n_valid;               // mode 1
+  int32_t* status;
+
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      __stcg(raw + static_cast<size_t>(n) * ldr + m0, acc[t][0]);
+      __stcg(raw + static_cast<size_t>(n + 1) * ldr + m0, acc[t][1]);
+      __stcg(raw + static_cast<size_t>(n) * ldr + m1, acc[t][2]);
+      __stcg(raw + static_cast<size_t>(n + 1) * ldr + m1, acc[t][3]);
+    }
+  }
+
+  __device__ void after_group(const GemvArgs& a, int g, int tid, int* sflag) const {
+    const int head = g / gph;
+    if (gph > 1) {
+      if (tid == 0) {
+        __threadfence();
+        const int old = atomicAdd(&head_cnt[head], 1);
+        sflag[1] = (old == gph - 1);
+      }
+      named_bar_sync(1, 128);
+      if (!sflag[1]) return;
+      __threadfence();
+      if (tid == 0) head_cnt[head] = 0;
+    }
+    process_head(head, tid);
+  }
+
+  __device__ void process_head(int hh, int tid) const {
+    const int w = tid >> 5, lane = tid & 31;
+    const int half = d / 2;
+    const int R = n_rows();
+    int kind, kvh, l;
+    const float* wn;
+    if (mode == 0) {
+      l = layer;
+      if (hh < n_q) { kind = 0; kvh = 0; wn = q_norm; }
+      else if (hh < n_q + n_kv) { kind = 1; kvh = hh - n_q; wn = k_norm; }
+      else { kind = 2; kvh = hh - n_q - n_kv; wn = nullptr; }
+    } else {
+      l = hh / (2 * n_kv);
+      const int rem = hh - l * 2 * n_kv;
+      kind = rem < n_kv ? 1 : 2;
+      kvh = rem < n_kv ? rem : rem - n_kv;
+      wn = kind == 1 ? k_norm + static_cast<size_t>(l) * d : nullptr;
+    }
+    for (int n = w; n < R; n += 4) {
+      int pos, s;
+      bool write_state;
+      if (mode == 0) {
+        s = n >> 3;
+        const int i = n & 7;
+        if (s < n_seq) {
+          int B = block_len[s];
+          B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+          pos = anchor_pos[s] + i;
+          write_state = (i < B) && pos >= 0 && pos < cap;
+        } else {
+          pos = 0;
+          write_state = false;
+        }
+      } else {
+        s = slot;
+        if (n >= n_valid) continue;
+        pos = positions[n];
+        write_state = pos >= 0 && pos < cap;
+        if (!write_state && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
+      }
+      const float* y = raw + static_cast<size_t>(n) * ldr + static_cast<size_t>(hh) * d;
+      if (kind == 2) {
+        if (!write_state) continue;
+        __half* dst = Vst + ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
+        for (int i = lane; i < d; i += 32) dst[i] = __float2half_rn(__ldcg(y + i));
+        continue;
+      }
+      if (kind == 1 && !write_state) continue;
+      float ss = 0.f;
+      for (int i = lane; i < d; i += 32) {
+        const float v = __ldcg(y + i);
+        ss += v * v;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rs = rsqrtf(ss / d + eps);
+      __half* dst;
+      float scale;
+      if (kind == 0) {
+        dst = q_ready + (static_cast<size_t>(n) * n_q + hh) * d;
+        scale = q_scale;
+      } else {
+        dst = Kst + ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
+        scale = 1.f;
+      }
+      for (int i = lane; i < half; i += 32) {
+        const float a = __ldcg(y + i) * rs * wn[i];
+        const float b = __ldcg(y + i + half) * rs * wn[i + half];
+        float sn, cs;
+        rope_sincos(turns[i], pos, sn, cs);
+        dst[i] = __float2half_rn((a * cs - b * sn) * scale);
+        dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+      }
+    }
+  }
+  __device__ int n_rows() const { return rows_; }
+  int rows_;
+  template <int NT>
+  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
+};
+
+// LM head + argmax.  Every thread keeps the best (value, vocab id) of its two
+// activation rows per n-tile across all groups of the CTA's range; at the
+// end the CTA reduces them, publishes one packed key per activation row, and
+// the CTA that arrives last reduces all CTAs' keys into the drafts.  Keys are
+// (order-preserving float bits << 32) | (0xffffffff - id), so the maximum is
+// the largest logit with ties going to the lowest id.
+template <int NT_>
+struct EpiArgmax {
+  static constexpr bool kAfterGroup = false, kFinish = true;
+  struct Local {
+    float v[NT_][2];
+    int id[NT_][2];
+    int bad;
+  };
+  int vocab;
+  int n_seq;
+  const int32_t* block_len;
+  int32_t* drafts;               // [n_seq, 7]
+  unsigned long long* slots;     // [gridDim.x, R]
+  int* grid_cnt;
+  float* final_hidden;           // optional [n_seq, 8, H] (X_RESIDENT prologue)
+  const float* x;                // residual rows for final_hidden
+  const float* norm_w;
+  int H;
+  int32_t* status;
+
+  __device__ void init(Local& L) const {
+#pragma unroll
+    for (int t = 0; t < NT_; ++t)
+      for (int h = 0; h < 2; ++h) {
+        L.v[t][h] = -INFINITY;
+        L.id[t][h] = 0x7fffffff;
+      }
+    L.bad = 0;
+  }
+  __device__ void prologue(const GemvArgs&, int tid, const float* srs) const {
+    if (final_hidden == nullptr || blockIdx.x != 0 || srs == nullptr) return;
+    for (int i = tid; i < n_seq * 8 * H; i += 128) {
+      const int n = i / H, k = i - n * H;
+      final_hidden[i] = __ldcg(x + static_cast<size_t>(n) * H + k) * srs[n] * norm_w[k];
+    }
+  }
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local& L, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = e < 2 ? m0 : m1;
+        const float v = acc[t][e];
+        if (m < vocab) {
+          if (!isfinite(v)) {
+            L.bad = 1;
+          } else if (v > L.v[t][e & 1] || (v == L.v[t][e & 1] && m < L.id[t][e & 1])) {
+            L.v[t][e & 1] = v;
+            L.id[t][e & 1] = m;
+          }
+        }
+      }
+  }
+  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
+
+  __device__ static unsigned long long pack(float v, int id) {
+    if (id == 0x7fffffff) return 0ull;
+    return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+           static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(id));
+  }
+
+  template <int NT>
+  __device__ void finish(const GemvArgs& a, Local& L, int w, int lane, int tid, unsigned long long* sstage,
+                         int* sflag) const {
+    constexpr int R = NT * 8;
+    const bool any_bad = __any_sync(0xffffffffu, L.bad);
+    if (any_bad && lane == 0) set_status(status, DFLASH_DEV_NONFINITE);
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        unsigned long long k = pack(L.v[t][h], L.id[t][h]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, k, o);
+          k = k2 > k ? k2 : k;
+        }
+        if (lane < 4) sstage[w * R + t * 8 + lane * 2 + h] = k;
+      }
+    named_bar_sync(1, 128);
+    if (tid < R) {
+      unsigned long long k = sstage[tid];
+      for (int ww = 1; ww < 4; ++ww) {
+        const unsigned long long k2 = sstage[ww * R + tid];
+        k = k2 > k ? k2 : k;
+      }
+      __stcg(slots + static_cast<size_t>(blockIdx.x) * R + tid, k);
+    }
+    __threadfence();
+    named_bar_sync(1, 128);
+    if (tid == 0) {
+      const int old = atomicAdd(grid_cnt, 1);
+      sflag[2] = (old == static_cast<int>(gridDim.x) - 1);
+    }
+    named_bar_sync(1, 128);
+    if (!sflag[2]) return;
+    __threadfence();
+    if (tid < R) {
+      unsigned long long k = 0ull;
+      for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
+        const unsigned long long k2 = __ldcg(slots + static_cast<size_t>(c) * R + tid);
+        k = k2 > k ? k2 : k;
+      }
+      const int s = tid >> 3, i = tid & 7;
+      if (s < n_seq && i >= 1) {
+        int B = block_len[s];
+        B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+        int out = -1;
+        if (i < B) {
+          if (k == 0ull) set_status(status, DFLASH_DEV_NONFINITE);
+          else out = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
+        }
+        drafts[s * (DFLASH_MAX_BLOCK - 1) + (i - 1)] = out;
+      }
+    }
+    if (tid == 0) *grid_cnt = 0;
+  }
+};
+
+}  // namespace dflash

@@ -1,0 +1,139 @@
+// Host-side launchers of the GEMV kernel family.  The templates are defined
+// here and explicitly instantiated once per weight type in gemv_<type>.cu, so
+// the heavy kernel instantiations compile in parallel translation units.
+#pragma once
+
+#include "gemv_epilogues.cuh"
+
+namespace dflash {
+
+struct LaunchCfg {
+  cudaStream_t stream;
+  int grid;
+  bool pdl;
+};
+
+struct ArgmaxParams {
+  int vocab, n_seq, H;
+  const int32_t* block_len;
+  int32_t* drafts;
+  unsigned long long* slots;
+  int* grid_cnt;
+  float* final_hidden;
+  const float* x;
+  const float* norm_w;
+  int32_t* status;
+};
+
+constexpr int kMaxDynSmem = 232448;  // 227 KB, the sm_100 per-CTA limit
+
+template <int WT, int NT, int XMODE>
+inline int gemv_smem(int K) {
+  return GemvGeom<WT, NT, XMODE>::smem_bytes(K);
+}
+
+// Raise the dynamic shared-memory cap once per (kernel instantiation, device).
+template <int WT, int NT, int XMODE, class Epi>
+inline cudaError_t ensure_smem_attr() {
+  static unsigned set_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (__atomic_load_n(&set_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemv_kernel<WT, NT, XMODE, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  if (e == cudaSuccess) __atomic_fetch_or(&set_mask, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
+template <int WT, int NT, int XMODE, class Epi>
+inline cudaError_t launch_gemv(const GemvArgs& a, const Epi& epi, const LaunchCfg& lc) {
+  auto kern = gemv_kernel<WT, NT, XMODE, Epi>;
+  cudaError_t e = ensure_smem_attr<WT, NT, XMODE, Epi>();
+  if (e != cudaSuccess) return e;
+  const int smem = GemvGeom<WT, NT, XMODE>::smem_bytes(a.K);
+  if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(lc.grid);
+  cfg.blockDim = dim3(GemvGeom<WT, NT, XMODE>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, epi);
+}
+
+#define DFLASH_NT_SWITCH(nt, ...)                 \
+  switch (nt) {                                   \
+    case 1: { constexpr int NT = 1; __VA_ARGS__ } \
+    case 2: { constexpr int NT = 2; __VA_ARGS__ } \
+    case 4: { constexpr int NT = 4; __VA_ARGS__ } \
+    case 8: { constexpr int NT = 8; __VA_ARGS__ } \
+    case 16: { constexpr int NT = 16; __VA_ARGS__ } \
+    default: return cudaErrorInvalidValue;        \
+  }
+
+// X (the caller's BF16 taps) streamed, raw fp32 result stored (fusion fc).
+template <int WT>
+cudaError_t gemv_store(int nt, const GemvArgs& a, const EpiStore& e, const LaunchCfg& lc) {
+  switch (nt) {
+    case 1: return launch_gemv<WT, 1, X_STREAM_BF16>(a, e, lc);
+    case 16: return launch_gemv<WT, 16, X_STREAM_BF16>(a, e, lc);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// X streamed, residual add (attention output projection, MLP down).
+template <int WT>
+cudaError_t gemv_resid(int nt, const GemvArgs& a, const EpiResid& e, const LaunchCfg& lc) {
+  DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
+}
+
+// SwiGLU gate/up; X resident (RMSNorm prologue) for one n-tile, else streamed.
+template <int WT>
+cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, int ldh, const LaunchCfg& lc) {
+  const EpiSwiglu<Fmt<WT>::kF16> e{h, ldh};
+  DFLASH_NT_SWITCH(nt, if constexpr (NT == 1) return launch_gemv<WT, NT, X_RESIDENT>(a, e, lc);
+                   else return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
+}
+
+// Per-head epilogue (draft QKV / fusion K/V).
+template <int WT>
+cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
+  if (e.mode == 1) {
+    switch (nt) {
+      case 1: return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+      case 16: return launch_gemv<WT, 16, X_STREAM>(a, e, lc);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  DFLASH_NT_SWITCH(nt, if constexpr (NT == 1) return launch_gemv<WT, NT, X_RESIDENT>(a, e, lc);
+                   else return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
+}
+
+// LM head + argmax over the borrowed row-major BF16 head.
+inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc) {
+  DFLASH_NT_SWITCH(
+      nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.grid_cnt, p.final_hidden, p.x,
+                          p.norm_w, p.H, p.status};
+      if constexpr (NT == 1) return launch_gemv<WT_HEAD, NT, X_RESIDENT>(a, e, lc);
+      else return launch_gemv<WT_HEAD, NT, X_STREAM>(a, e, lc);)
+}
+
+// Shared-memory bytes of the configuration a launcher will pick.
+template <int WT>
+int gemv_smem_for(int nt, int xmode, int K) {
+  switch (nt) {
+    case 1: return xmode == X_RESIDENT ? gemv_smem<WT, 1, X_RESIDENT>(K) : gemv_smem<WT, 1, X_STREAM>(K);
+    case 2: return gemv_smem<WT, 2, X_STREAM>(K);
+    case 4: return gemv_smem<WT, 4, X_STREAM>(K);
+    case 8: return gemv_smem<WT, 8, X_STREAM>(K);
+    case 16: return gemv_smem<WT, 16, X_STREAM>(K);
+  }
+  return 0;
+}
+
+}  // namespace dflash

@@ -1,0 +1,48 @@
+// Argument structs and host launchers of the small kernels (misc.cu,
+// attention.cu), shared with the C-ABI implementation.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace dflash {
+
+struct EmbedArgs {
+  const uint16_t* embed;
+  const int32_t* anchor_tok;
+  const int32_t* anchor_pos;
+  const int32_t* block_len;
+  float* x;
+  int H, vocab, mask_id, n_seq, cap;
+  int32_t* status;
+};
+
+struct NormArgs {
+  const float* x;
+  const float* w;
+  void* out;
+  int out_f16;
+  int H, rows_valid;
+  float eps;
+  float* f32_out;  // optional fp32 copy of rows [0, rows_f32)
+  int rows_f32;
+};
+
+cudaError_t launch_repack(int wtype, const void* src, int rows, int K, uint8_t* dst, int row_off, int interleave,
+                          cudaStream_t st);
+cudaError_t launch_dequant(int wtype, const uint8_t* packed, int N, int K, float* out, int row_off, int rows_out,
+                           int interleave, cudaStream_t st);
+cudaError_t launch_embed(const EmbedArgs& a, int nt, cudaStream_t st);
+cudaError_t launch_rmsnorm_rows(const NormArgs& a, int rows, cudaStream_t st);
+cudaError_t launch_accept(const int32_t* drafts, const int32_t* tgt, const int32_t* block_len, int n_seq, int maxB,
+                          int32_t* accept_len, int32_t* next_anchor, int32_t* anchor_pos, cudaStream_t st);
+cudaError_t launch_kv_copy(bool write, __half* cells, int cap, int d, int n_kv, int pos0, int n, float* out,
+                           const uint16_t* in, cudaStream_t st);
+cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, const int32_t* anchor_pos,
+                             const int32_t* block_len, int32_t* status, cudaStream_t stream);
+int attn_smem_bytes(int D, int gq);
+
+}  // namespace dflash
