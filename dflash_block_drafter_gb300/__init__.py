@@ -105,6 +105,7 @@ _SIGS = {
     "dflash_draft_launches": (ctypes.c_int32, [_P, _I]),
     "dflash_fuse_launches": (ctypes.c_int32, [_P, _I]),
     "dflash_state_set_head_events": (ctypes.c_int, [_P, _P, _P]),
+    "dflash_head_argmax_static": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
 }
 
 
@@ -262,3 +263,11 @@ def dflash_fuse_launches(state: int, n: int) -> int:
 def dflash_state_set_head_events(state: int, ev_begin: int, ev_end: int) -> None:
     _check(load_library().dflash_state_set_head_events(state, ev_begin or None, ev_end or None),
            "dflash_state_set_head_events")
+
+
+def dflash_head_argmax_static(model: int, hidden: int, n_rows: int, ids: int, dev_status: int = 0,
+                              stream: int = 0) -> None:
+    """LM-head argmax of up to 8 final-hidden rows using only the library's
+    fixed scratch array (no device allocation); see include/dflash.h."""
+    _check(load_library().dflash_head_argmax_static(model, hidden, n_rows, ids, dev_status or None,
+                                                    stream or None), "dflash_head_argmax_static")

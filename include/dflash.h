@@ -274,6 +274,25 @@ int32_t dflash_fuse_launches(const dflash_state* state, int32_t n);
  * pass.  NULL, NULL switches it off. */
 int dflash_state_set_head_events(dflash_state* state, void* ev_begin, void* ev_end);
 
+/* Greedy ids over the target's LM head for n_rows (1..8) rows of final
+ * hidden states, for callers that cannot allocate device memory: code that
+ * runs while a CUDA graph is being captured, engines that own all device
+ * memory as one arena reserved up front, or loops that must never enter the
+ * allocator.  It needs no dflash_state: its scratch is a fixed array of about
+ * 1.2 MB inside the library (held by every GPU that loads it until exit), and
+ * it allocates nothing.  The pages have no counterpart of this entry point.
+ *   hidden: [n_rows, H] float, rows already through the final RMSNorm (the
+ *           final_hidden output of dflash_draft_block is such a row set).
+ *   ids:    [n_rows] int32 out: argmax over the vocabulary of head . row
+ *           (ties to the lowest id), computed exactly as the draft pass does.
+ * Returns DFLASH_ERR_CAPACITY when n_rows > 8, hidden > 8192 or vocab >
+ * 262144 (the fixed scratch's limits).  The first call on each device looks
+ * up the scratch array's device address; make it before any stream capture.
+ * All calls share the one scratch array: calls that overlap on the GPU race
+ * (order them on one stream).  Each call clears the counters it relies on. */
+int dflash_head_argmax_static(const dflash_model* model, const float* hidden, int32_t n_rows, int32_t* ids,
+                              int32_t* dev_status, dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
