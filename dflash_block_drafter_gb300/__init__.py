@@ -105,6 +105,8 @@ _SIGS = {
     "dflash_draft_launches": (ctypes.c_int32, [_P, _I]),
     "dflash_fuse_launches": (ctypes.c_int32, [_P, _I]),
     "dflash_state_set_head_events": (ctypes.c_int, [_P, _P, _P]),
+    "dflash_state_set_profile_events": (ctypes.c_int, [_P, ctypes.POINTER(_P), _I]),
+    "dflash_state_set_attn_chunks": (ctypes.c_int, [_P, _I, ctypes.POINTER(_I)]),
     "dflash_head_argmax_static": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
 }
 
@@ -271,3 +273,19 @@ def dflash_head_argmax_static(model: int, hidden: int, n_rows: int, ids: int, de
     fixed scratch array (no device allocation); see include/dflash.h."""
     _check(load_library().dflash_head_argmax_static(model, hidden, n_rows, ids, dev_status or None,
                                                     stream or None), "dflash_head_argmax_static")
+
+
+def dflash_state_set_profile_events(state: int, events) -> None:
+    """events: list of cudaEvent_t integers (empty list switches profiling off)."""
+    arr = (_P * max(1, len(events)))(*events) if events else None
+    _check(load_library().dflash_state_set_profile_events(state, arr, len(events)),
+           "dflash_state_set_profile_events")
+
+
+def dflash_state_set_attn_chunks(state: int, chunks: int = 0) -> int:
+    """Set the attention's context chunks per (sequence, kv head) (0: query
+    only); returns the maximum the state supports."""
+    mx = _I()
+    _check(load_library().dflash_state_set_attn_chunks(state, chunks, ctypes.byref(mx)),
+           "dflash_state_set_attn_chunks")
+    return mx.value

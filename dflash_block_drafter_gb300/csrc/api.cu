@@ -17,7 +17,7 @@ namespace dflash {
 #define DFLASH_DECLARE_GEMV(WT)                                                                           \
   extern template cudaError_t gemv_store<WT>(int, const GemvArgs&, const EpiStore&, const LaunchCfg&);  \
   extern template cudaError_t gemv_resid<WT>(int, const GemvArgs&, const EpiResid&, const LaunchCfg&);  \
-  extern template cudaError_t gemv_swiglu<WT>(int, const GemvArgs&, void*, int, const LaunchCfg&);      \
+  extern template cudaError_t gemv_swiglu<WT>(int, const GemvArgs&, void*, const LaunchCfg&);             \
   extern template cudaError_t gemv_heads<WT>(int, const GemvArgs&, const EpiHeads&, const LaunchCfg&);
 DFLASH_DECLARE_GEMV(WT_BF16)
 DFLASH_DECLARE_GEMV(WT_Q8_0)
@@ -49,6 +49,8 @@ int cuda_fail(cudaError_t e, const char* what) {
   } while (0)
 
 int cb_of(int wt) { return wt == WT_BF16 ? Fmt<WT_BF16>::CB : Fmt<WT_Q8_0>::CB; }
+// inputs per streaming unit of a weight type (the chunked X layout's KU)
+int ku_of(int wt) { return 32 * cb_of(wt); }
 
 __global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ in, float* __restrict__ out, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -75,8 +77,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D row-major 16-bit tensor [rows, cols] with 64 x 64 boxes, 128-byte swizzle.
-int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, CUtensorMapDataType dt) {
+// 2-D row-major 16-bit tensor [rows, cols] with 64-column x box_rows boxes, 128-byte swizzle.
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, CUtensorMapDataType dt,
+                uint32_t box_rows = 64) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) {
     std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled unavailable");
@@ -84,7 +87,7 @@ int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols
   }
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -166,9 +169,20 @@ int pow2ceil(int v) {
   return p;
 }
 
+// Diagnostic builds: the next per-CTA timestamp slot of a GEMV launch.
+unsigned long long* trace_slot(State& st) {
+#ifdef DFLASH_TRACE
+  if (st.trace && st.trace_k < st.trace_launches)
+    return st.trace + static_cast<size_t>(st.trace_k++) * st.max_grid * 8;
+#endif
+  (void)st;
+  return nullptr;
+}
+
 GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* status) {
   GemvArgs a;
   std::memset(&a, 0, sizeof(a));
+  a.trace = trace_slot(st);
   a.W = pm.data;
   a.N = pm.n;
   a.K = pm.k;
@@ -209,12 +223,12 @@ cudaError_t gemv_resid_any(int wt, int nt, const GemvArgs& a, const EpiResid& e,
   }
   return cudaErrorInvalidValue;
 }
-cudaError_t gemv_swiglu_any(int wt, int nt, const GemvArgs& a, void* h, int ldh, const LaunchCfg& lc) {
+cudaError_t gemv_swiglu_any(int wt, int nt, const GemvArgs& a, void* h, const LaunchCfg& lc) {
   switch (wt) {
-    case WT_BF16: return gemv_swiglu<WT_BF16>(nt, a, h, ldh, lc);
-    case WT_Q8_0: return gemv_swiglu<WT_Q8_0>(nt, a, h, ldh, lc);
-    case WT_Q5_0: return gemv_swiglu<WT_Q5_0>(nt, a, h, ldh, lc);
-    case WT_Q4_0: return gemv_swiglu<WT_Q4_0>(nt, a, h, ldh, lc);
+    case WT_BF16: return gemv_swiglu<WT_BF16>(nt, a, h, lc);
+    case WT_Q8_0: return gemv_swiglu<WT_Q8_0>(nt, a, h, lc);
+    case WT_Q5_0: return gemv_swiglu<WT_Q5_0>(nt, a, h, lc);
+    case WT_Q4_0: return gemv_swiglu<WT_Q4_0>(nt, a, h, lc);
   }
   return cudaErrorInvalidValue;
 }
@@ -226,6 +240,11 @@ cudaError_t gemv_heads_any(int wt, int nt, const GemvArgs& a, const EpiHeads& e,
     case WT_Q4_0: return gemv_heads<WT_Q4_0>(nt, a, e, lc);
   }
   return cudaErrorInvalidValue;
+}
+
+// Record the next profiling event on `stream` (no-op unless profiling is on).
+void prof_mark(State* s, cudaStream_t stream) {
+  if (s->prof_n > 0 && s->prof_k < s->prof_n) cudaEventRecord(static_cast<cudaEvent_t>(s->prof_events[s->prof_k++]), stream);
 }
 
 bool is_dev_ptr(const void* p) {
@@ -426,12 +445,20 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   const int gq = nq / nkv;
   const int M = gq * 8;
   {
-    long long want = (capacity + 255) / 256;
-    long long maxc = (2LL * m->sm_count) / (static_cast<long long>(n_slots) * nkv);
-    if (maxc < 1) maxc = 1;
-    if (want > maxc) want = maxc;
-    if (want < 1) want = 1;
-    s->attn_chunks = static_cast<int>(want);
+    // default: ~2 key tiles per CTA, at most 2 CTAs per SM; buffers sized for
+    // up to 4 CTAs per SM (and at most 512 chunks, the merge kernel's limit)
+    const long long tiles = (capacity + 63) / 64;
+    const long long per = static_cast<long long>(n_slots) * nkv;
+    long long cmax = (4LL * m->sm_count) / per;
+    cmax = cmax < 1 ? 1 : (cmax > 512 ? 512 : cmax);
+    if (cmax > tiles) cmax = tiles;
+    long long cdef = (tiles + 1) / 2;
+    const long long cap2 = (2LL * m->sm_count) / per;
+    if (cdef > cap2) cdef = cap2;
+    if (cdef > cmax) cdef = cmax;
+    if (cdef < 1) cdef = 1;
+    s->attn_chunks = static_cast<int>(cdef);
+    s->attn_chunks_max = static_cast<int>(cmax);
   }
   size_t total = 0;
   const size_t kv_elems = static_cast<size_t>(arena_rows) * d;
@@ -443,11 +470,12 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->x, size_t(R) * H * 4, &total));
   STRY(dev_alloc(&s->qkv_raw, size_t(R) * nqkv * 4, &total));
   STRY(dev_alloc(&s->q_ready, size_t(R) * nq * d * 2, &total));
-  STRY(dev_alloc(&s->attn_out, size_t(R) * nq * d * 2, &total));
-  STRY(dev_alloc(&s->hbuf, size_t(R) * I * 2, &total));
-  STRY(dev_alloc(&s->xnorm, size_t(R) * H * 2, &total));
-  STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks * M * d * 4, &total));
-  STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks * M * 8, &total));
+  // activations for streamed-X GEMVs: two 16-bit planes (BF16 hi and lo, or FP16 in the first)
+  STRY(dev_alloc(&s->attn_out, xchunk_elems(nq * d, R, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->hbuf, xchunk_elems(I, R, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->xnorm, xchunk_elems(H, R, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 4, &total));
+  STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks_max * M * 8, &total));
   s->max_grid = 2 * m->sm_count;
   const int rmax = 128;
   STRY(dev_alloc(&s->partials, size_t(s->max_grid) * 2 * 64 * rmax * 4, &total));
@@ -465,9 +493,11 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   s->fuse_rows = 128;
   STRY(dev_alloc(&s->h_raw, size_t(s->fuse_rows) * H * 4, &total));
   STRY(dev_alloc(&s->kv_raw, size_t(s->fuse_rows) * L * 2 * nkv * d * 4, &total));
-  STRY(dev_alloc(&s->fuse_xnorm, size_t(s->fuse_rows) * H * 2, &total));
+  STRY(dev_alloc(&s->fuse_xnorm, xchunk_elems(H, 128, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->status, 16, &total));
   if (cudaMemset(s->status, 0, 16) != cudaSuccess) return fail(cuda_fail(cudaGetLastError(), "cudaMemset"));
+  STRY(make_map_2d(&s->q_map, s->q_ready, static_cast<uint64_t>(s->nt) * nkv * M, d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   static_cast<uint32_t>(M)));
   STRY(make_map_2d(&s->k_map, s->K, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   STRY(make_map_2d(&s->v_map, s->V, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   {
@@ -500,6 +530,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
   const int wt = m->wtype;
   int32_t* status = dev_status ? dev_status : s->status;
   const int tw = c.n_taps * H;
+  s->prof_k = 0;
   for (int base = 0; base < n; base += s->fuse_rows) {
     const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
     const int nt = rows <= 8 ? 1 : 16;
@@ -511,6 +542,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       a.ldx = tw;
       EpiStore e{s->h_raw, H};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      prof_mark(s, stream);
       TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
     }
     // K/V of every layer from rmsnorm(h_raw) * hidden_norm
@@ -518,12 +550,14 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       GemvArgs a = base_args(m->kv_all, *s, CNT_KV, status);
       a.n_valid_rows = rows;
       a.eps = c.norm_eps;
-      if (nt == 1) {
+      if (resident_ok(nt, H)) {
         a.X = s->h_raw;
         a.ldx = H;
         a.norm_w = m->hidden_norm;
       } else {
-        NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0};
+        NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0,
+                    ku_of(wt)};
+        prof_mark(s, stream);
         TRY(check_gemv(launch_rmsnorm_rows(na, nt * 8, stream), "fuse norm"));
         a.X = s->fuse_xnorm;
         a.ldx = H;
@@ -552,9 +586,11 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       e.status = status;
       e.rows_ = nt * 8;
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      prof_mark(s, stream);
       TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "fuse kv"));
     }
   }
+  prof_mark(s, stream);
   return DFLASH_OK;
 }
 
@@ -573,9 +609,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   int32_t* status = dev_status ? dev_status : s->status;
   const bool f16 = wt != WT_BF16;
 
+  s->prof_k = 0;
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
                  s->capacity, status};
+    prof_mark(s, stream);
     TRY(check_gemv(launch_embed(ea, nt, stream), "embed"));
   }
   for (int l = 0; l < L; ++l) {
@@ -584,13 +622,16 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       GemvArgs a = base_args(m->qkv[l], *s, CNT_QKV, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
-      if (nt == 1) {
+      if (resident_ok(nt, H)) {
         a.X = s->x;
         a.ldx = H;
         a.norm_w = m->attn_norm + size_t(l) * H;
       } else {
-        NormArgs na{s->x, m->attn_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0};
-        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "attn norm"));
+        NormArgs na{s->x, m->attn_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
+                    ku_of(wt)};
+        prof_mark(s, stream);
+        prof_mark(s, stream);
+      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "attn norm"));
         a.X = s->xnorm;
         a.ldx = H;
       }
@@ -621,9 +662,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       e.status = status;
       e.rows_ = R;
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      prof_mark(s, stream);
       TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "qkv"));
     }
-    TRY(check_gemv(launch_attention(*m, *s, l, n_seq, anchor_pos, block_len, status, stream), "attention"));
+    prof_mark(s, stream);
+    TRY(check_gemv(launch_attention(*m, *s, l, n_seq, nt, anchor_pos, block_len, status, stream), "attention"));
     {
       GemvArgs a = base_args(m->o[l], *s, CNT_O, status);
       a.n_valid_rows = R;
@@ -631,24 +674,29 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.ldx = nq * d;
       EpiResid e{s->x, H};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
     }
     {
       GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
-      if (nt == 1) {
+      if (resident_ok(nt, H)) {
         a.X = s->x;
         a.ldx = H;
         a.norm_w = m->mlp_norm + size_t(l) * H;
       } else {
-        NormArgs na{s->x, m->mlp_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0};
-        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "mlp norm"));
+        NormArgs na{s->x, m->mlp_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
+                    ku_of(wt)};
+        prof_mark(s, stream);
+        prof_mark(s, stream);
+      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "mlp norm"));
         a.X = s->xnorm;
         a.ldx = H;
       }
       LaunchCfg lc{stream, grid_for(*m, a), true};
-      TRY(check_gemv(gemv_swiglu_any(wt, nt, a, s->hbuf, I, lc), "gate/up"));
+      prof_mark(s, stream);
+      TRY(check_gemv(gemv_swiglu_any(wt, nt, a, s->hbuf, lc), "gate/up"));
     }
     {
       GemvArgs a = base_args(m->down[l], *s, CNT_DOWN, status);
@@ -657,6 +705,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.ldx = I;
       EpiResid e{s->x, H};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
     }
   }
@@ -674,6 +723,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     a.partials = s->partials;
     a.counters = s->counters + static_cast<size_t>(CNT_HEAD) * s->counter_stride;
     a.status = status;
+    a.trace = trace_slot(*s);
     ArgmaxParams p;
     p.vocab = c.vocab;
     p.n_seq = n_seq;
@@ -686,12 +736,14 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.x = s->x;
     p.norm_w = m->final_norm;
     p.status = status;
-    if (nt == 1) {
+    if (resident_ok(nt, H)) {
       a.X = s->x;
       a.ldx = H;
       a.norm_w = m->final_norm;
     } else {
-      NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8};
+      NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8,
+                  32 * Fmt<WT_HEAD>::CB};
+      prof_mark(s, stream);
       TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "final norm"));
       a.X = s->xnorm;
       a.ldx = H;
@@ -699,9 +751,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     }
     LaunchCfg lc{stream, grid_for(*m, a), true};
     if (s->head_ev_begin) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_begin), stream));
+    prof_mark(s, stream);
     TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
     if (s->head_ev_end) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_end), stream));
   }
+  prof_mark(s, stream);
   return DFLASH_OK;
 }
 
@@ -792,7 +846,7 @@ int dflash_model_dequantize(const dflash_model* m, int32_t which, float* out, df
 int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   if (!s || n_seq < 1 || n_seq > s->n_slots) return -1;
   const int L = s->model->cfg.n_layers;
-  const bool streamed = pow2ceil(n_seq) > 1;  // separate RMSNorm kernels before qkv, gate/up and head
+  const bool streamed = !resident_ok(pow2ceil(n_seq), s->model->cfg.hidden);  // separate RMSNorm kernels
   const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
   return 1 + L * per_layer + 1 + (streamed ? 1 : 0);
 }
@@ -802,9 +856,26 @@ int32_t dflash_fuse_launches(const dflash_state* s, int32_t n) {
   int k = 0;
   for (int base = 0; base < n; base += s->fuse_rows) {
     const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
-    k += rows <= 8 ? 2 : 3;
+    k += resident_ok(rows <= 8 ? 1 : 16, s->model->cfg.hidden) ? 2 : 3;
   }
   return k;
+}
+
+int dflash_state_set_attn_chunks(dflash_state* s, int32_t chunks, int32_t* max_chunks) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  if (max_chunks) *max_chunks = s->attn_chunks_max;
+  if (chunks == 0) return DFLASH_OK;
+  if (chunks < 1 || chunks > s->attn_chunks_max) return DFLASH_ERR_INVALID_ARG;
+  s->attn_chunks = chunks;
+  return DFLASH_OK;
+}
+
+int dflash_state_set_profile_events(dflash_state* s, void* const* events, int32_t n_events) {
+  if (!s || n_events < 0 || n_events > 256 || (n_events > 0 && !events)) return DFLASH_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i) s->prof_events[i] = events[i];
+  s->prof_n = n_events;
+  s->prof_k = 0;
+  return DFLASH_OK;
 }
 
 int dflash_state_set_head_events(dflash_state* s, void* ev_begin, void* ev_end) {
@@ -813,5 +884,16 @@ int dflash_state_set_head_events(dflash_state* s, void* ev_begin, void* ev_end) 
   s->head_ev_end = ev_end;
   return DFLASH_OK;
 }
+
+#ifdef DFLASH_TRACE
+// Diagnostic builds only: per-CTA timestamps of the next GEMV launches.
+int dflash_state_set_trace(dflash_state* s, unsigned long long* buf, int32_t max_launches) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  s->trace = buf;
+  s->trace_launches = buf ? max_launches : 0;
+  s->trace_k = 0;
+  return DFLASH_OK;
+}
+#endif
 
 }  // extern "C"

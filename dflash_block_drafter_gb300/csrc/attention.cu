@@ -16,21 +16,22 @@
 // With C > 1 every chunk writes (O unnormalised, running max, sum) and
 // attn_combine_kernel merges them with the log-sum-exp rule; with C == 1 the
 // CTA normalises and writes the output directly.
-#include "common.cuh"
 #include "kernels.h"
+#include "layout.cuh"
 
 namespace dflash {
 
 struct AttnArgs {
+  CUtensorMap qmap;  // queries [slots * n_kv * M, d] fp16, 64 x M boxes (normed, rotated, scaled by 1/sqrt(d))
   CUtensorMap kmap;  // K arena as [rows, d] fp16
   CUtensorMap vmap;
-  const __half* q_ready;  // [R, n_q, d], already normed, rotated and scaled by 1/sqrt(d)
   const int32_t* anchor_pos;
   const int32_t* block_len;
   float* part;            // [slots, n_kv, C, M, d]
   float2* ml;             // [slots, n_kv, C, M]
-  void* out;              // [R, n_q * d] activation type (C == 1)
-  int out_f16;            // activation type of out: 1 fp16, 0 bf16
+  void* out;              // attention output in the o-projection's chunked X layout (C == 1)
+  int out_f16;            // 1: one FP16 plane; 0: BF16 hi and lo planes
+  int out_rows, out_ku;   // chunked layout: rows R of the pass and inputs per unit
   int layer, n_slots, n_kv, n_q, gq, cap, C, n_seq;
   int32_t* status;
 };
@@ -44,7 +45,7 @@ struct AttnGeom {
   static constexpr int TILE_BYTES = kAttnKT * D * 2;  // one K (or V) tile
   static __host__ __device__ constexpr int q_bytes(int M) { return M * D * 2; }
   static __host__ __device__ constexpr int smem(int M) {
-    return 1024 + q_bytes(M) + 2 * kAttnStages * TILE_BYTES + 4 * kAttnStages * 8 + 64;
+    return 1024 + q_bytes(M) + 2 * kAttnStages * TILE_BYTES + 4 * kAttnStages * 8 + 64 + 8;
   }
 };
 
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
   uint64_t* kfull = reinterpret_cast<uint64_t*>(sv + kAttnStages * Geo::TILE_BYTES);
   uint64_t* vfull = kfull + kAttnStages;
   uint64_t* empty = vfull + kAttnStages;
+  uint64_t* qbar = empty + kAttnStages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -91,13 +93,15 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
       mbar_init(&vfull[i], 1);
       mbar_init(&empty[i], NW);
     }
+    mbar_init(qbar, 1);
     fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == NW) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nt > 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&a.qmap);
       prefetch_tensormap(&a.kmap);
       prefetch_tensormap(&a.vmap);
       auto issue = [&](int it) {
@@ -116,6 +120,10 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
       const int n_pre = nt < kAttnStages ? nt : kAttnStages;
       for (; it < n_pre && (t0 + it + 1) * kAttnKT <= p; ++it) issue(it);
       pdl_wait();
+      // the queries (written by the previous kernel): one 64-column box each
+      mbar_arrive_expect_tx(qbar, Geo::q_bytes(M));
+      for (int b = 0; b < Geo::BOXES; ++b)
+        tma_load_2d(sq + b * M * 128, &a.qmap, b * 64, (s * a.n_kv + g) * M, qbar);
       int issued = it;
       for (; it < nt; ++it) {
         if (it >= kAttnStages && !mbar_wait(&empty[it % kAttnStages], ((it / kAttnStages) - 1) & 1)) {
@@ -140,20 +148,7 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
   // -------------------------------------------------------------- consumers
   pdl_wait();
   pdl_launch_dependents();
-  const int nthr = NW * 32;
-  // Q rows: m = hl * 8 + i  (local q head hl, block row i)
-  {
-    const uint32_t qb = smem_u32(sq);
-    for (int idx = tid; idx < M * (D / 8); idx += nthr) {
-      const int m = idx / (D / 8), col8 = idx - m * (D / 8);
-      const int hl = m >> 3, i = m & 7;
-      const uint4 v = *reinterpret_cast<const uint4*>(
-          a.q_ready + ((static_cast<size_t>(s * 8 + i) * a.n_q + g * a.gq + hl) * D) + col8 * 8);
-      const uint32_t dst = swz(qb, M, m, col8);
-      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-    }
-  }
-  named_bar_sync(1, nthr);
+  if (!mbar_wait(qbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
 
   constexpr float LOG2E = 1.4426950408889634f;
   constexpr int NDT = D / 8;  // output n-tiles
@@ -269,18 +264,27 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
   if (a.C == 1) {
     const float inv = l_r > 0.f ? 1.f / l_r : 0.f, inv8 = l_r8 > 0.f ? 1.f / l_r8 : 0.f;
     if (!(l_r > 0.f) || !(l_r8 > 0.f)) set_status(a.status, DFLASH_DEV_NONFINITE);
-    const int ldo = a.n_q * D;
-    const size_t r0 = static_cast<size_t>(s * 8 + (m0 & 7)) * ldo + static_cast<size_t>(g * a.gq + (m0 >> 3)) * D;
-    const size_t r1 = static_cast<size_t>(s * 8 + (m1 & 7)) * ldo + static_cast<size_t>(g * a.gq + (m1 >> 3)) * D;
+    const int P = a.out_f16 ? 1 : 2;
+    const int row0 = s * 8 + (m0 & 7), row1 = s * 8 + (m1 & 7);
+    const int c0 = (g * a.gq + (m0 >> 3)) * D, c1 = (g * a.gq + (m1 >> 3)) * D;
 #pragma unroll
     for (int i = 0; i < NDT; ++i) {
       const int col = i * 8 + (lane & 3) * 2;
+      const size_t o0 = xchunk_index(c0 + col, row0, 0, a.out_rows, a.out_ku, P);
+      const size_t o1 = xchunk_index(c1 + col, row1, 0, a.out_rows, a.out_ku, P);
       if (a.out_f16) {
-        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + r0 + col) = pack_f16x2(o[i][0] * inv, o[i][1] * inv);
-        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + r1 + col) = pack_f16x2(o[i][2] * inv8, o[i][3] * inv8);
+        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + o0) = pack_f16x2(o[i][0] * inv, o[i][1] * inv);
+        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + o1) = pack_f16x2(o[i][2] * inv8, o[i][3] * inv8);
       } else {
-        *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + r0 + col) = pack_bf16x2(o[i][0] * inv, o[i][1] * inv);
-        *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + r1 + col) = pack_bf16x2(o[i][2] * inv8, o[i][3] * inv8);
+        uint32_t h0, l0, h1, l1;
+        split_bf16x2(o[i][0] * inv, o[i][1] * inv, h0, l0);
+        split_bf16x2(o[i][2] * inv8, o[i][3] * inv8, h1, l1);
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out);
+        const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);  // next plane of the chunk
+        *reinterpret_cast<uint32_t*>(ob + o0) = h0;
+        *reinterpret_cast<uint32_t*>(ob + o1) = h1;
+        *reinterpret_cast<uint32_t*>(ob + o0 + lo_off) = l0;
+        *reinterpret_cast<uint32_t*>(ob + o1 + lo_off) = l1;
       }
     }
   } else {
@@ -298,46 +302,102 @@ __global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ At
   }
 }
 
-// Log-sum-exp merge of the C chunk partials of one (slot, q head, block row).
+// Log-sum-exp merge of the C chunk partials of one (slot, q head): all 8 block
+// rows, a 64-column slice of the head (blockIdx.y).  The per-row merge weights
+// 2^(m_c - M) / L are computed once into shared memory; then 8 groups of 32
+// threads each sum every 8th chunk for 2 columns x 8 rows with independent
+// loads, and the groups are reduced through shared memory.
 struct CombineArgs {
   const float* part;
   const float2* ml;
   void* out;
   int out_f16;
+  int out_rows, out_ku;
   int d, n_q, n_kv, gq, C;
   int32_t* status;
 };
 
+constexpr int kCombineMaxC = 512;
+
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineArgs a) {
-  const int hq = blockIdx.x, i = blockIdx.y, s = blockIdx.z;
+  __shared__ float sw[8][kCombineMaxC];
+  __shared__ float2 sacc[8][8][32];  // [chunk group][row][lane] partial sums of 2 columns
+  const int hq = blockIdx.x, cb = blockIdx.y, s = blockIdx.z;
   const int g = hq / a.gq, hl = hq - g * a.gq;
   const int M = a.gq * 8;
-  const int m = hl * 8 + i;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   pdl_launch_dependents();
   const size_t base = (static_cast<size_t>(s) * a.n_kv + g) * a.C * M;
-  float mx = -INFINITY;
-  for (int c = 0; c < a.C; ++c) {
-    const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
-    if (v.y > 0.f) mx = fmaxf(mx, v.x);
-  }
-  float L = 0.f;
-  for (int c = 0; c < a.C; ++c) {
-    const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
-    if (v.y > 0.f) L += v.y * exp2f(v.x - mx);
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  if (threadIdx.x == 0 && !(L > 0.f)) set_status(a.status, DFLASH_DEV_NONFINITE);
-  const size_t ob = static_cast<size_t>(s * 8 + i) * a.n_q * a.d + static_cast<size_t>(hq) * a.d;
-  for (int col = threadIdx.x; col < a.d; col += blockDim.x) {
-    float acc = 0.f;
-    for (int c = 0; c < a.C; ++c) {
+  {
+    // warp i: merge weights of block row i
+    const int m = hl * 8 + warp;
+    float mx = -INFINITY;
+    for (int c = lane; c < a.C; c += 32) {
       const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
-      if (v.y > 0.f) acc += __ldcg(a.part + (base + static_cast<size_t>(c) * M + m) * a.d + col) * exp2f(v.x - mx);
+      if (v.y > 0.f) mx = fmaxf(mx, v.x);
     }
-    const float r = acc * inv;
-    if (a.out_f16) static_cast<__half*>(a.out)[ob + col] = __float2half_rn(r);
-    else static_cast<__nv_bfloat16*>(a.out)[ob + col] = __float2bfloat16_rn(r);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float L = 0.f;
+    for (int c = lane; c < a.C; c += 32) {
+      const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
+      const float e = v.y > 0.f ? exp2f(v.x - mx) : 0.f;
+      sw[warp][c] = e;
+      L += v.y * e;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (!(L > 0.f)) {
+      if (lane == 0) set_status(a.status, DFLASH_DEV_NONFINITE);
+      L = 1.f;
+    }
+    const float inv = 1.f / L;
+    __syncwarp();
+    for (int c = lane; c < a.C; c += 32) sw[warp][c] *= inv;
+  }
+  __syncthreads();
+  // chunk group = warp; columns cb*64 + 2*lane, +1
+  const int col = cb * 64 + lane * 2;
+  float2 acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll 4
+  for (int c = warp; c < a.C; c += 8) {
+    const float* pc = a.part + (base + static_cast<size_t>(c) * M + hl * 8) * a.d + col;
+    float2 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldcg(reinterpret_cast<const float2*>(pc + static_cast<size_t>(i) * a.d));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float wgt = sw[i][c];
+      acc[i].x = fmaf(v[i].x, wgt, acc[i].x);
+      acc[i].y = fmaf(v[i].y, wgt, acc[i].y);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sacc[warp][i][lane] = acc[i];
+  __syncthreads();
+  // warp i writes row i
+  {
+    const int i = warp;
+    float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      r.x += sacc[k][i][lane].x;
+      r.y += sacc[k][i][lane].y;
+    }
+    const int P = a.out_f16 ? 1 : 2;
+    const size_t ob = xchunk_index(hq * a.d + col, s * 8 + i, 0, a.out_rows, a.out_ku, P);
+    if (a.out_f16) {
+      *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + ob) = pack_f16x2(r.x, r.y);
+    } else {
+      uint32_t hi, lo;
+      split_bf16x2(r.x, r.y, hi, lo);
+      const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);
+      *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + ob) = hi;
+      *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + ob + lo_off) = lo;
+    }
   }
 }
 
@@ -387,19 +447,20 @@ int attn_smem_bytes(int D, int gq) {
 
 // One layer's attention for slots [0, n_seq): chunked kernel plus, when the
 // context is split, the merge.
-cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, const int32_t* anchor_pos,
+cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,
                              const int32_t* block_len, int32_t* status, cudaStream_t stream) {
   const dflash_config& c = m.cfg;
   AttnArgs a;
   a.kmap = st.k_map;
   a.vmap = st.v_map;
-  a.q_ready = st.q_ready;
   a.anchor_pos = anchor_pos;
   a.block_len = block_len;
   a.part = st.attn_part;
   a.ml = st.attn_ml;
   a.out = st.attn_out;
   a.out_f16 = m.wtype != DFLASH_WT_BF16;
+  a.out_rows = 8 * pass_nt;
+  a.out_ku = m.wtype == DFLASH_WT_BF16 ? 128 : 256;
   a.layer = layer;
   a.n_slots = st.n_slots;
   a.n_kv = c.n_kv_heads;
@@ -409,13 +470,18 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, co
   a.C = st.attn_chunks;
   a.n_seq = n_seq;
   a.status = status;
+  a.qmap = st.q_map;
   cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.C, a.n_kv, n_seq), stream, true);
   if (e != cudaSuccess || a.C == 1) return e;
+  if (st.prof_n > 0 && st.prof_k < st.prof_n)
+    cudaEventRecord(static_cast<cudaEvent_t>(st.prof_events[st.prof_k++]), stream);
   CombineArgs cb;
   cb.part = st.attn_part;
   cb.ml = st.attn_ml;
   cb.out = st.attn_out;
   cb.out_f16 = a.out_f16;
+  cb.out_rows = a.out_rows;
+  cb.out_ku = a.out_ku;
   cb.d = c.head_dim;
   cb.n_q = c.n_q_heads;
   cb.n_kv = c.n_kv_heads;
@@ -423,7 +489,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, co
   cb.C = a.C;
   cb.status = status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(c.n_q_heads, 8, n_seq);
+  cfg.gridDim = dim3(c.n_q_heads, c.head_dim / 64, n_seq);
   cfg.blockDim = dim3(256);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -23,14 +23,16 @@
 namespace dflash {
 
 struct GemvArgs {
-  CUtensorMap wmap;  // WT_HEAD only
+  CUtensorMap wmap;              // WT_HEAD only
   const uint8_t* W;              // packed weights (fragment-native formats)
   int N, K;                      // logical rows / inputs
   int UPG;                       // units per 64-row group
   int U;                         // total units
-  int n_valid_rows;              // activation rows that exist (others are zero)
-  // X_STREAM: activation rows [R, ldx] (bf16 or fp16 per weight type)
-  // X_RESIDENT: fp32 rows [R, ldx] normalised with norm_w in the prologue
+  int n_valid_rows;              // activation rows that exist (others read as zero)
+  // X_RESIDENT: fp32 rows X[r * ldx + k] and the RMSNorm weight norm_w[K]
+  //             (fp32); staged by bulk copies, normalised in the consumer
+  // X_STREAM: activations in the chunked layout (layout.cuh), R = 8 * NT rows
+  // X_STREAM_BF16: BF16 rows X[r * ldx + k] (the caller's taps)
   const void* X;
   int ldx;
   const float* norm_w;
@@ -38,30 +40,50 @@ struct GemvArgs {
   float* partials;               // [gridDim.x, 2, 64, R]
   int* counters;                 // [N / 64]
   int32_t* status;
+  unsigned long long* trace;     // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
+
+#ifdef DFLASH_TRACE
+#define DFLASH_STAMP(k)                                                                   \
+  do {                                                                                    \
+    if (a.trace) a.trace[static_cast<size_t>(blockIdx.x) * 8 + (k)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define DFLASH_STAMP(k) \
+  do {                  \
+  } while (0)
+#endif
 
 template <int WT, int NT, int XMODE>
 struct GemvGeom {
   using F = Fmt<WT>;
   static constexpr int R = NT * 8;
   static constexpr int KU = F::CB * 32;                 // inputs per unit
-  static constexpr int XS_STRIDE = KU * 2 + 64;         // streamed X row stride (bytes, padded)
+  static constexpr int XSE = KU + 32;                   // streamed X row stride (elements, padded)
+  static constexpr int XS_STRIDE = XSE * 2;             // ... in bytes
   static constexpr bool kStream = XMODE == X_STREAM || XMODE == X_STREAM_BF16;
   // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
   static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16;
-  static constexpr int XS_BYTES = kStream ? R * XS_STRIDE : 0;
+  // BF16 activations computed in fp32 are carried as two BF16 planes, hi and
+  // lo = x - hi (about 16 significant bits), each multiplied on the tensor
+  // cores; the caller's BF16 taps (X_STREAM_BF16) are exact and need no lo.
+  static constexpr bool kSplit = !kF16 && XMODE != X_STREAM_BF16;
+  static constexpr int XPLANES = kSplit ? 2 : 1;
+  static constexpr int XS_BYTES = kStream ? XPLANES * R * XS_STRIDE : 0;
   static constexpr int STAGE = ((F::UNIT + XS_BYTES + 1023) / 1024) * 1024;
-  // as many stages as the format asks for, within ~190 KB of ring
-  static constexpr int STAGES_FIT = 190000 / STAGE;
+  // Resident X holds fp32 rows plus the norm weight; sized for K up to kResK.
+  static constexpr int kResK = 2560;
+  static __host__ __device__ constexpr int xres_stride(int K) { return K * 4 + 16; }
+  static __host__ __device__ constexpr int xres_bytes(int K) {
+    return (XMODE == X_RESIDENT) ? ((R * xres_stride(K) + K * 4 + 127) / 128) * 128 : 0;
+  }
+  static constexpr int RING_BUDGET = (XMODE == X_RESIDENT) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
+  static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
   static constexpr int THREADS = 160;
-  // smem: [ring][X resident][barriers][misc]
-  static __host__ __device__ constexpr int xres_stride(int K) { return K * 2 + 64; }
-  static __host__ __device__ constexpr int xres_bytes(int K) {
-    return (XMODE == X_RESIDENT) ? ((R * xres_stride(K) + 127) / 128) * 128 : 0;
-  }
-  static constexpr int MISC = 2 * 8 * STAGES + 64 + 4 * R * 8 + R * 4;
+  static constexpr int MISC = 8 * (2 * STAGES + 1) + 64 + 4 * R * 8 + R * 4;
+  // smem: [ring][resident X][barriers][misc]
   static __host__ __device__ constexpr int smem_bytes(int K) { return 1024 + RING + xres_bytes(K) + MISC; }
 };
 
@@ -90,32 +112,38 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   constexpr int STAGES = Geo::STAGES;
   constexpr bool kF16 = Geo::kF16;
   constexpr bool kStream = Geo::kStream;
+  constexpr bool kSplit = Geo::kSplit;
+  constexpr int XPLANES = Geo::XPLANES;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* xres = ring + Geo::RING;
+  uint8_t* xres = ring + Geo::RING;                                   // fp32 rows, then the norm weight
   uint64_t* full = reinterpret_cast<uint64_t*>(xres + Geo::xres_bytes(a.K));
   uint64_t* empty = full + STAGES;
-  int* sflag = reinterpret_cast<int*>(empty + STAGES);               // 16 ints
-  float* srs = reinterpret_cast<float*>(sflag + 16);                 // [R] row scales
+  uint64_t* xbar = empty + STAGES;
+  int* sflag = reinterpret_cast<int*>(xbar + 1);                      // 16 ints
+  float* srs = reinterpret_cast<float*>(sflag + 16);                  // [R] row scales
   unsigned long long* sstage = reinterpret_cast<unsigned long long*>(srs + R);  // [4][R]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
+  if (tid == 0) DFLASH_STAMP(0);
   const int u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.U) / G);
   const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
   const int n_units = u_end - u_begin;
+  const int xstride = (XMODE == X_RESIDENT) ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
+    mbar_init(xbar, 1);
     fence_barrier_init();
   }
-  if constexpr (kStream) {
+  if constexpr (XMODE == X_STREAM_BF16) {
     // rows that are never copied (beyond n_valid_rows) must read as zeros
     if (a.n_valid_rows < R) {
       for (int s = 0; s < STAGES; ++s) {
@@ -127,6 +155,12 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       }
     }
   }
+  if constexpr (XMODE == X_RESIDENT) {
+    for (int i = tid; i < (R - a.n_valid_rows) * (a.K / 4); i += Geo::THREADS) {
+      const int rr = a.n_valid_rows + i / (a.K / 4);
+      reinterpret_cast<float4*>(xres + rr * xstride)[i % (a.K / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   __syncthreads();
 
   if (warp == 4) {
@@ -135,7 +169,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       if constexpr (WT == WT_HEAD) prefetch_tensormap(&a.wmap);
       const uint64_t pol = l2_policy_evict_first();
       constexpr int XBYTES_ROW = Geo::KU * 2;
-      const uint32_t tx = F::UNIT + (kStream ? a.n_valid_rows * XBYTES_ROW : 0);
+      uint32_t tx = F::UNIT;
+      if constexpr (XMODE == X_STREAM) tx += XPLANES * R * Geo::XS_STRIDE;
+      if constexpr (XMODE == X_STREAM_BF16) tx += a.n_valid_rows * XBYTES_ROW;
       auto issue_w = [&](int it, int u) {
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
         if constexpr (WT == WT_HEAD) {
@@ -147,9 +183,14 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         }
       };
       auto issue_x = [&](int it, int u) {
-        if constexpr (kStream) {
-          const int j = u % a.UPG;
-          uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
+        const int j = u % a.UPG;
+        uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
+        if constexpr (XMODE == X_STREAM) {
+          // one contiguous chunk per plane
+          const uint8_t* src =
+              static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XPLANES * R * Geo::XS_STRIDE;
+          bulk_g2s(dst, src, XPLANES * R * Geo::XS_STRIDE, &full[it % STAGES]);
+        } else if constexpr (XMODE == X_STREAM_BF16) {
           const uint8_t* src = static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XBYTES_ROW;
           for (int r = 0; r < a.n_valid_rows; ++r)
             bulk_g2s(dst + r * Geo::XS_STRIDE, src + static_cast<size_t>(r) * a.ldx * 2, XBYTES_ROW,
@@ -162,7 +203,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         issue_w(it, u_begin + it);
       }
       pdl_wait();  // activations below come from the previous kernel
-      for (int it = 0; it < n_pre; ++it) issue_x(it, u_begin + it);
+      DFLASH_STAMP(1);
+      if constexpr (kStream)
+        for (int it = 0; it < n_pre; ++it) issue_x(it, u_begin + it);
       int issued = n_pre;
       for (int it = n_pre; it < n_units; ++it) {
         const int s = it % STAGES;
@@ -172,9 +215,10 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         }
         mbar_arrive_expect_tx(&full[s], tx);
         issue_w(it, u_begin + it);
-        issue_x(it, u_begin + it);
+        if constexpr (kStream) issue_x(it, u_begin + it);
         issued = it + 1;
       }
+      DFLASH_STAMP(2);
       // Every issued copy must land before the CTA may exit.
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         if (!mbar_wait(&full[it % STAGES], (it / STAGES) & 1)) {
@@ -189,64 +233,75 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   pdl_wait();
   pdl_launch_dependents();
   const int w = warp;
+  if (tid == 0) DFLASH_STAMP(3);
 
   if constexpr (XMODE == X_RESIDENT) {
-    // X = RMSNorm(x) * w for all R rows and the full K, into shared memory.
-    const float* x = static_cast<const float*>(a.X);
+    // Stage the fp32 rows and the norm weight with bulk copies, compute
+    // 1 / RMS per row, then overwrite every fp32 value v = x * (1/RMS) * w in
+    // place with the 16-bit operand(s) the MMA needs: BF16 hi | lo << 16, or
+    // FP16 in the low half.  The consumer pairs neighbouring values with PRMT.
+    float* wsm = reinterpret_cast<float*>(xres + R * xstride);
+    if (tid == 0) {
+      const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 4;
+      mbar_arrive_expect_tx(xbar, (a.n_valid_rows + 1) * row_bytes);
+      const float* x = static_cast<const float*>(a.X);
+      for (int r = 0; r < a.n_valid_rows; ++r)
+        bulk_g2s(xres + r * xstride, x + static_cast<size_t>(r) * a.ldx, row_bytes, xbar);
+      bulk_g2s(wsm, a.norm_w, row_bytes, xbar);
+    }
+    if (!mbar_wait(xbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
     for (int r = w; r < R; r += 4) {
+      const float4* xr = reinterpret_cast<const float4*>(xres + r * xstride);
       float ss = 0.f;
-      if (r < a.n_valid_rows) {
-        const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * a.ldx);
-        for (int i = lane; i < a.K / 4; i += 32) {
-          const float4 v = __ldcg(xr + i);
-          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
+#pragma unroll 4
+      for (int i = lane; i < a.K / 4; i += 32) {
+        const float4 v = xr[i];
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
     }
     named_bar_sync(1, 128);
-    const int xstride = Geo::xres_stride(a.K);
-    const int k8 = a.K / 8;
-    for (int i = tid; i < R * k8; i += 128) {
-      const int r = i / k8, kk = (i - r * k8) * 8;
-      const float s = srs[r];
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (r < a.n_valid_rows) {
-        const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * a.ldx + kk);
-        const float4* wr = reinterpret_cast<const float4*>(a.norm_w + kk);
-        const float4 x0 = __ldcg(xr), x1 = __ldcg(xr + 1);
-        const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
+    const int k4 = a.K / 4;
+#pragma unroll 4
+    for (int i = tid; i < R * k4; i += 128) {
+      const int r = i / k4, kq = i - r * k4;
+      float4* xp = reinterpret_cast<float4*>(xres + r * xstride) + kq;
+      const float4 v = *xp;
+      const float4 wv = reinterpret_cast<const float4*>(wsm)[kq];
+      const float sc = srs[r];
+      const float y[4] = {v.x * sc * wv.x, v.y * sc * wv.y, v.z * sc * wv.z, v.w * sc * wv.w};
+      uint4 o;
+      uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         if constexpr (kF16) {
-          o.x = pack_f16x2(x0.x * s * w0.x, x0.y * s * w0.y);
-          o.y = pack_f16x2(x0.z * s * w0.z, x0.w * s * w0.w);
-          o.z = pack_f16x2(x1.x * s * w1.x, x1.y * s * w1.y);
-          o.w = pack_f16x2(x1.z * s * w1.z, x1.w * s * w1.w);
+          op[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(y[e])));
         } else {
-          o.x = pack_bf16x2(x0.x * s * w0.x, x0.y * s * w0.y);
-          o.y = pack_bf16x2(x0.z * s * w0.z, x0.w * s * w0.w);
-          o.z = pack_bf16x2(x1.x * s * w1.x, x1.y * s * w1.y);
-          o.w = pack_bf16x2(x1.z * s * w1.z, x1.w * s * w1.w);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(y[e]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(y[e] - __bfloat162float(hi));
+          op[e] = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                  (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
         }
       }
-      *reinterpret_cast<uint4*>(xres + r * xstride + kk * 2) = o;
+      *reinterpret_cast<uint4*>(xp) = o;
     }
   }
   epi.prologue(a, tid, XMODE == X_RESIDENT ? srs : nullptr);
   named_bar_sync(1, 128);
+  if (tid == 0) DFLASH_STAMP(4);
 
   typename Epi::Local loc;
   epi.init(loc);
-  float acc[NT][4];
+  float acc[NT][4], acc2[NT][4];  // acc2: lo-plane products (a second, independent chain)
 #pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  for (int t = 0; t < NT; ++t)
+    for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = 0.f;
 
   const int first_group = u_begin / a.UPG;
-  const int xstride = (XMODE == X_RESIDENT) ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
   const uint32_t ring_s = smem_u32(ring);
-  const uint32_t xres_s = smem_u32(xres);
-  const int xrow = lane >> 2, xcol = (lane & 3) * 16;  // bytes within a 32-block row segment
+  const int xrow = lane >> 2;
   bool ok = true;
 
   for (int it = 0; it < n_units && ok; ++it) {
@@ -257,23 +312,41 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       ok = false;
       break;
     }
+    if (tid == 0 && it == 0) DFLASH_STAMP(5);
     const int g = u / a.UPG, j = u - g * a.UPG;
     const uint32_t ubase = ring_s + s * Geo::STAGE;
-    uint32_t xb;
-    if constexpr (XMODE == X_RESIDENT)
-      xb = xres_s + xrow * xstride + j * Geo::KU * 2 + xcol;
-    else
-      xb = ubase + F::UNIT + xrow * xstride + xcol;
 
 #pragma unroll
     for (int bl = 0; bl < F::CB; ++bl) {
       const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
+      uint32_t xofs = 0;
+      if constexpr (XMODE == X_RESIDENT) xofs = ((j * F::CB + bl) * 32 + (lane & 3) * 8) * 4;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const uint4 xf = lds128(xb + t * 8 * xstride + bl * 64);
+        uint4 xf, xl;
+        if constexpr (XMODE == X_RESIDENT) {
+          // 8 packed values of this lane's row: (hi | lo << 16) or FP16 in the low half
+          const uint8_t* xp = xres + (t * 8 + xrow) * xstride + xofs;
+          const uint4 p0 = *reinterpret_cast<const uint4*>(xp);
+          const uint4 p1 = *reinterpret_cast<const uint4*>(xp + 16);
+          xf.x = prmt(p0.x, p0.y, 0x5410); xf.y = prmt(p0.z, p0.w, 0x5410);
+          xf.z = prmt(p1.x, p1.y, 0x5410); xf.w = prmt(p1.z, p1.w, 0x5410);
+          if constexpr (kSplit) {
+            xl.x = prmt(p0.x, p0.y, 0x7632); xl.y = prmt(p0.z, p0.w, 0x7632);
+            xl.z = prmt(p1.x, p1.y, 0x7632); xl.w = prmt(p1.z, p1.w, 0x7632);
+          }
+        } else {
+          const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
+          xf = lds128(xb);
+          if constexpr (kSplit) xl = lds128(xb + R * Geo::XS_STRIDE);
+        }
         if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
           mma_bf16_16816(acc[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
           mma_bf16_16816(acc[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+          if constexpr (kSplit) {
+            mma_bf16_16816(acc2[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xl.x, xl.y);
+            mma_bf16_16816(acc2[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xl.z, xl.w);
+          }
         } else {
           float tmp[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (kF16) {
@@ -282,6 +355,10 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
           } else {
             mma_bf16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
             mma_bf16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+            if constexpr (kSplit) {
+              mma_bf16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xl.x, xl.y);
+              mma_bf16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xl.z, xl.w);
+            }
           }
           acc[t][0] = fmaf(f.d_r, tmp[0], acc[t][0]);
           acc[t][1] = fmaf(f.d_r, tmp[1], acc[t][1]);
@@ -292,8 +369,17 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
 
     if (j == a.UPG - 1 || u == u_end - 1) {
+      if constexpr (kSplit && (WT == WT_BF16 || WT == WT_HEAD)) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          for (int e = 0; e < 4; ++e) {
+            acc[t][e] += acc2[t][e];
+            acc2[t][e] = 0.f;
+          }
+      }
       const bool complete = (g * a.UPG >= u_begin) && (j == a.UPG - 1);
       if (complete) {
         epi.template group<WT, NT>(a, loc, g, w, lane, acc);
@@ -312,18 +398,20 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
           __stcg(reinterpret_cast<float2*>(slot + r0 * R + c0), make_float2(acc[t][0], acc[t][1]));
           __stcg(reinterpret_cast<float2*>(slot + (r0 + 8) * R + c0), make_float2(acc[t][2], acc[t][3]));
         }
-        __threadfence();
+        // the CTA's stores, ordered by the barrier, are released by thread 0's
+        // fence before its counter increment; the last arriver acquires them
         named_bar_sync(1, 128);
         const long long ufirst = static_cast<long long>(g) * a.UPG;
         const int c_first = cta_of_unit(ufirst, G, a.U);
         const int c_last = cta_of_unit(ufirst + a.UPG - 1, G, a.U);
         if (tid == 0) {
+          __threadfence();
           const int old = atomicAdd(&a.counters[g], 1);
           sflag[0] = (old == c_last - c_first);
+          __threadfence();
         }
         named_bar_sync(1, 128);
         if (sflag[0]) {
-          __threadfence();
 #pragma unroll
           for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
@@ -352,6 +440,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     }
   }
   if constexpr (Epi::kFinish) epi.template finish<NT>(a, loc, w, lane, tid, sstage, sflag);
+  if (tid == 0) DFLASH_STAMP(7);
 }
 
 }  // namespace dflash

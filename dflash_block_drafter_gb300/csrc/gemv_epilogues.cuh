@@ -65,32 +65,35 @@ struct EpiResid {
 
 // SwiGLU: the packed gate/up matrix holds, in every 16-row m-tile, 8 gate
 // rows then the 8 up rows of the same outputs, so a lane owns gate (m = r)
-// and up (m = r + 8) of output o = g*32 + w*8 + r:  h[n][o] = silu(g) * u.
+// and up (m = r + 8) of output o = g*32 + w*8 + r:  h[n][o] = silu(g) * u,
+// written in the chunked layout the down projection streams (FP16, or BF16
+// hi and lo planes).
 template <bool kF16>
 struct EpiSwiglu {
   static constexpr bool kAfterGroup = false, kFinish = false;
   using Local = NoLocal;
-  void* h;  // [R, ldh] bf16 / fp16
-  int ldh;
+  void* h;
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
   __device__ static float silu(float v) { return v / (1.f + __expf(-v)); }
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    constexpr int R = NT * 8, KU = Fmt<WT>::CB * 32, P = kF16 ? 1 : 2;
     const int o = g * 32 + w * 8 + (lane >> 2);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int n = t * 8 + (lane & 3) * 2;
-      const float h0 = silu(acc[t][0]) * acc[t][2];
-      const float h1 = silu(acc[t][1]) * acc[t][3];
-      if constexpr (kF16) {
-        __half* hp = static_cast<__half*>(h);
-        hp[static_cast<size_t>(n) * ldh + o] = __float2half_rn(h0);
-        hp[static_cast<size_t>(n + 1) * ldh + o] = __float2half_rn(h1);
-      } else {
-        __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(h);
-        hp[static_cast<size_t>(n) * ldh + o] = __float2bfloat16_rn(h0);
-        hp[static_cast<size_t>(n + 1) * ldh + o] = __float2bfloat16_rn(h1);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = silu(acc[t][e]) * acc[t][e + 2];
+        if constexpr (kF16) {
+          static_cast<__half*>(h)[xchunk_index(o, n + e, 0, R, KU, P)] = __float2half_rn(v);
+        } else {
+          __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(h);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+          hp[xchunk_index(o, n + e, 0, R, KU, P)] = hi;
+          hp[xchunk_index(o, n + e, 1, R, KU, P)] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        }
       }
     }
   }
@@ -121,7 +124,7 @@ struct EpiHeads {
   const float* k_norm;   // mode 0: this layer's [d]; mode 1: all layers [L, d]
   const uint64_t* turns; // [d/2]
   float eps, q_scale;
-  __half* q_ready;       // [R, n_q, d]
+  __half* q_ready;       // [slots, n_kv, n_q / n_kv * 8, d]
   __half* Kst;
   __half* Vst;
   int layer, n_slots, cap;
@@ -155,11 +158,11 @@ struct EpiHeads {
         __threadfence();
         const int old = atomicAdd(&head_cnt[head], 1);
         sflag[1] = (old == gph - 1);
+        __threadfence();
+        if (sflag[1]) head_cnt[head] = 0;
       }
       named_bar_sync(1, 128);
       if (!sflag[1]) return;
-      __threadfence();
-      if (tid == 0) head_cnt[head] = 0;
     }
     process_head(head, tid);
   }
@@ -205,37 +208,41 @@ struct EpiHeads {
         if (!write_state && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
       }
       const float* y = raw + static_cast<size_t>(n) * ldr + static_cast<size_t>(hh) * d;
+      if (kind != 0 && !write_state) continue;
+      // the row's d values, lane-strided: element lane + 32 j (d <= 256)
+      float yv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) yv[j] = (lane + 32 * j < d) ? __ldcg(y + lane + 32 * j) : 0.f;
+      const size_t cell = ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
       if (kind == 2) {
-        if (!write_state) continue;
-        __half* dst = Vst + ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
-        for (int i = lane; i < d; i += 32) dst[i] = __float2half_rn(__ldcg(y + i));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (lane + 32 * j < d) Vst[cell + lane + 32 * j] = __float2half_rn(yv[j]);
         continue;
       }
-      if (kind == 1 && !write_state) continue;
       float ss = 0.f;
-      for (int i = lane; i < d; i += 32) {
-        const float v = __ldcg(y + i);
-        ss += v * v;
-      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss += yv[j] * yv[j];
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float rs = rsqrtf(ss / d + eps);
-      __half* dst;
-      float scale;
-      if (kind == 0) {
-        dst = q_ready + (static_cast<size_t>(n) * n_q + hh) * d;
-        scale = q_scale;
-      } else {
-        dst = Kst + ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
-        scale = 1.f;
-      }
-      for (int i = lane; i < half; i += 32) {
-        const float a = __ldcg(y + i) * rs * wn[i];
-        const float b = __ldcg(y + i + half) * rs * wn[i + half];
-        float sn, cs;
-        rope_sincos(turns[i], pos, sn, cs);
-        dst[i] = __float2half_rn((a * cs - b * sn) * scale);
-        dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+      // queries: [slot][kv head][m = local head * 8 + block row][d] (contiguous per slot and kv head)
+      const int gq = n_q / n_kv;
+      __half* dst = kind == 0 ? q_ready + ((static_cast<size_t>(s * n_kv + hh / gq) * gq + hh % gq) * 8 + (n & 7)) * d
+                              : Kst + cell;
+      const float scale = kind == 0 ? q_scale : 1.f;
+      const int hj = d / 64;  // pairs per lane; element i + d/2 sits at yv[j + hj]
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < hj) {
+          const int i = lane + 32 * j;
+          const float a = yv[j] * rs * wn[i];
+          const float b = yv[j + hj] * rs * wn[i + half];
+          float sn, cs;
+          rope_sincos(turns[i], pos, sn, cs);
+          dst[i] = __float2half_rn((a * cs - b * sn) * scale);
+          dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+        }
       }
     }
   }
@@ -341,15 +348,15 @@ struct EpiArgmax {
       }
       __stcg(slots + static_cast<size_t>(blockIdx.x) * R + tid, k);
     }
-    __threadfence();
     named_bar_sync(1, 128);
     if (tid == 0) {
+      __threadfence();
       const int old = atomicAdd(grid_cnt, 1);
       sflag[2] = (old == static_cast<int>(gridDim.x) - 1);
+      __threadfence();
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;
-    __threadfence();
     if (tid < R) {
       unsigned long long k = 0ull;
       for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {

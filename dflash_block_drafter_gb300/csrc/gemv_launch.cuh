@@ -92,26 +92,32 @@ cudaError_t gemv_resid(int nt, const GemvArgs& a, const EpiResid& e, const Launc
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
-// SwiGLU gate/up; X resident (RMSNorm prologue) for one n-tile, else streamed.
+// The RMSNorm-fed GEMVs (q/k/v, gate/up, LM head, fusion K/V) read X
+// resident (fp32 rows staged, normalised in the consumer) for one n-tile when
+// the hidden size fits its shared memory, else streamed from a separate
+// RMSNorm kernel's chunked output.
+inline bool resident_ok(int nt, int K) { return nt == 1 && K <= 2560; }
+
+// SwiGLU gate/up.
 template <int WT>
-cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, int ldh, const LaunchCfg& lc) {
-  const EpiSwiglu<Fmt<WT>::kF16> e{h, ldh};
-  DFLASH_NT_SWITCH(nt, if constexpr (NT == 1) return launch_gemv<WT, NT, X_RESIDENT>(a, e, lc);
-                   else return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
+cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, const LaunchCfg& lc) {
+  const EpiSwiglu<Fmt<WT>::kF16> e{h};
+  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+  DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
 // Per-head epilogue (draft QKV / fusion K/V).
 template <int WT>
 cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
+  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
   if (e.mode == 1) {
     switch (nt) {
-      case 1: return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+      case 1: return launch_gemv<WT, 1, X_STREAM>(a, e, lc);
       case 16: return launch_gemv<WT, 16, X_STREAM>(a, e, lc);
       default: return cudaErrorInvalidValue;
     }
   }
-  DFLASH_NT_SWITCH(nt, if constexpr (NT == 1) return launch_gemv<WT, NT, X_RESIDENT>(a, e, lc);
-                   else return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
+  DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
 // LM head + argmax over the borrowed row-major BF16 head.
@@ -119,21 +125,9 @@ inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParam
   DFLASH_NT_SWITCH(
       nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.grid_cnt, p.final_hidden, p.x,
                           p.norm_w, p.H, p.status};
-      if constexpr (NT == 1) return launch_gemv<WT_HEAD, NT, X_RESIDENT>(a, e, lc);
-      else return launch_gemv<WT_HEAD, NT, X_STREAM>(a, e, lc);)
-}
-
-// Shared-memory bytes of the configuration a launcher will pick.
-template <int WT>
-int gemv_smem_for(int nt, int xmode, int K) {
-  switch (nt) {
-    case 1: return xmode == X_RESIDENT ? gemv_smem<WT, 1, X_RESIDENT>(K) : gemv_smem<WT, 1, X_STREAM>(K);
-    case 2: return gemv_smem<WT, 2, X_STREAM>(K);
-    case 4: return gemv_smem<WT, 4, X_STREAM>(K);
-    case 8: return gemv_smem<WT, 8, X_STREAM>(K);
-    case 16: return gemv_smem<WT, 16, X_STREAM>(K);
-  }
-  return 0;
+      if constexpr (NT == 1) {
+        if (resident_ok(nt, a.K)) return launch_gemv<WT_HEAD, NT, X_RESIDENT>(a, e, lc);
+      } return launch_gemv<WT_HEAD, NT, X_STREAM>(a, e, lc);)
 }
 
 }  // namespace dflash

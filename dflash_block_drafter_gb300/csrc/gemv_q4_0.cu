@@ -4,6 +4,6 @@
 namespace dflash {
 template cudaError_t gemv_store<WT_Q4_0>(int, const GemvArgs&, const EpiStore&, const LaunchCfg&);
 template cudaError_t gemv_resid<WT_Q4_0>(int, const GemvArgs&, const EpiResid&, const LaunchCfg&);
-template cudaError_t gemv_swiglu<WT_Q4_0>(int, const GemvArgs&, void*, int, const LaunchCfg&);
+template cudaError_t gemv_swiglu<WT_Q4_0>(int, const GemvArgs&, void*, const LaunchCfg&);
 template cudaError_t gemv_heads<WT_Q4_0>(int, const GemvArgs&, const EpiHeads&, const LaunchCfg&);
 }  // namespace dflash

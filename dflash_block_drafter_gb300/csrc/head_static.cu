@@ -13,7 +13,7 @@
 // input row.  Its scratch -- the hidden rows rounded to BF16, the split-group
 // partial sums and their counters, and the per-CTA argmax keys -- lives in
 // g_head_scratch below: a file-scope __device__ array of kStaticScratchBytes
-// (about 1.2 MB) that every GPU that loads the library holds until exit.
+// (about 1.35 MB) that every GPU that loads the library holds until exit.
 //
 // Host code never uses the symbol itself as an address (in host code it is
 // only a stand-in): on the first call on each device, with that device
@@ -45,7 +45,8 @@ constexpr size_t kOffGridCnt = ((kOffCounters + kCountersBytes + 255) / 256) * 2
 constexpr size_t kOffSlots = kOffGridCnt + 256;                                 // u64[grid][8]
 constexpr size_t kOffPartials = kOffSlots + size_t(kStaticMaxGrid) * kStaticMaxRows * 8;  // f32[grid][2][64][8]
 constexpr size_t kOffX = kOffPartials + size_t(kStaticMaxGrid) * 2 * 64 * kStaticMaxRows * 4;  // bf16[8][H]
-constexpr size_t kStaticScratchBytes = kOffX + size_t(kStaticMaxRows) * kStaticMaxHidden * 2;
+// the rows in the head GEMV's chunked X layout: 8 rows, 128-input units, BF16 hi + lo planes
+constexpr size_t kStaticScratchBytes = kOffX + size_t(kStaticMaxHidden / 128) * 2 * kStaticMaxRows * (128 + 32) * 2;
 
 static __device__ __align__(256) uint8_t g_head_scratch[kStaticScratchBytes];
 
@@ -70,13 +71,21 @@ cudaError_t scratch_for_current_device(uint8_t** out) {
   return cudaSuccess;
 }
 
+// Rows -> the head GEMV's streamed X: BF16 hi = bf16(v) and lo = bf16(v - hi)
+// planes in the chunked layout of 8 rows and 128-input units; rows n..7 are
+// zero.
 __global__ void __launch_bounds__(256) rows_to_bf16_kernel(const float* __restrict__ in, int n, int H,
                                                            __nv_bfloat16* __restrict__ out) {
   pdl_wait();
   pdl_launch_dependents();
-  const int total = n * H;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x)
-    out[i] = __float2bfloat16_rn(in[i]);
+  const int total = kStaticMaxRows * H;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int r = i / H, k = i - r * H;
+    const float v = r < n ? in[i] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    out[xchunk_index(k, r, 0, kStaticMaxRows, 128, 2)] = hi;
+    out[xchunk_index(k, r, 1, kStaticMaxRows, 128, 2)] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
 }
 
 // The draft pass's argmax epilogue, finishing with one id per input row.
@@ -109,15 +118,15 @@ struct EpiArgmaxRows : public EpiArgmax<1> {
       }
       __stcg(slots + static_cast<size_t>(blockIdx.x) * R + tid, k);
     }
-    __threadfence();
     named_bar_sync(1, 128);
     if (tid == 0) {
+      __threadfence();
       const int old = atomicAdd(grid_cnt, 1);
       sflag[2] = (old == static_cast<int>(gridDim.x) - 1);
+      __threadfence();
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;
-    __threadfence();
     if (tid < n_rows) {
       unsigned long long k = 0ull;
       for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
@@ -159,7 +168,7 @@ extern "C" int dflash_head_argmax_static(const dflash_model* m, const float* hid
   a.K = c.hidden;
   a.UPG = c.hidden / 128;
   a.U = (a.N / 64) * a.UPG;
-  a.n_valid_rows = n_rows;
+  a.n_valid_rows = kStaticMaxRows;  // rows n_rows..7 of the staged X are zero
   a.X = scratch + kOffX;
   a.ldx = c.hidden;
   a.partials = reinterpret_cast<float*>(scratch + kOffPartials);
@@ -185,7 +194,7 @@ extern "C" int dflash_head_argmax_static(const dflash_model* m, const float* hid
     return DFLASH_ERR_CUDA;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((n_rows * c.hidden + 255) / 256);
+    cfg.gridDim = dim3((kStaticMaxRows * c.hidden + 255) / 256);
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

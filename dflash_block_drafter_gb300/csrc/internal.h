@@ -72,13 +72,14 @@ struct State {
   int rows = 0;            // R = 8 * NT activation rows of a pass
   int nt = 0;              // n8 tiles of a pass (power of two >= n_slots)
   int attn_chunks = 0;     // context chunks per (slot, kv head)
+  int attn_chunks_max = 0; // chunks the partial buffers are sized for
   // per-layer FP16 K/V arenas: [L][slot][n_kv][capacity][d]
   __half* K = nullptr;
   __half* V = nullptr;
   // pass workspace
   float* x = nullptr;          // [R, H] residual stream
   float* qkv_raw = nullptr;    // [R, (n_q + 2 n_kv) d]
-  __half* q_ready = nullptr;   // [R, n_q, d] normed, rotated, pre-scaled queries
+  __half* q_ready = nullptr;   // [slots, n_kv, M = 8 n_q / n_kv, d] normed, rotated, pre-scaled queries
   void* attn_out = nullptr;    // [R, n_q d] activation type
   void* hbuf = nullptr;        // [R, I] activation type (SwiGLU output)
   void* xnorm = nullptr;       // [R, H] activation type (normed rows for streamed-X GEMVs)
@@ -96,8 +97,15 @@ struct State {
   void* fuse_xnorm = nullptr;  // [fuse_rows, H] activation type
   int32_t* status = nullptr;   // [1] the state's own device status word
   int max_grid = 0;
+  void* prof_events[256] = {};     // optional per-kernel event marks
+  int prof_n = 0;
+  int prof_k = 0;
+  unsigned long long* trace = nullptr;  // diagnostic builds: [launch][max_grid][8] timestamps
+  int trace_launches = 0;
+  int trace_k = 0;
   void* head_ev_begin = nullptr;  // optional cudaEvent_t pair around the LM head
   void* head_ev_end = nullptr;
+  CUtensorMap q_map;  // q_ready as [slots*n_kv*M, d], 64 x M boxes, 128-byte swizzle
   CUtensorMap k_map;  // K arena as [L*slots*n_kv*cap, d], 64x64 boxes, 128-byte swizzle
   CUtensorMap v_map;
   size_t device_bytes = 0;

@@ -20,6 +20,8 @@ struct EmbedArgs {
   int32_t* status;
 };
 
+// out = RMSNorm(x) * w in the chunked streamed-X layout (layout.cuh) of a
+// GEMV with R = gridDim.x rows: FP16 (out_f16) or BF16 hi and lo planes.
 struct NormArgs {
   const float* x;
   const float* w;
@@ -29,6 +31,7 @@ struct NormArgs {
   float eps;
   float* f32_out;  // optional fp32 copy of rows [0, rows_f32)
   int rows_f32;
+  int ku;           // chunked layout of the consuming GEMV: inputs per unit
 };
 
 cudaError_t launch_repack(int wtype, const void* src, int rows, int K, uint8_t* dst, int row_off, int interleave,
@@ -41,7 +44,7 @@ cudaError_t launch_accept(const int32_t* drafts, const int32_t* tgt, const int32
                           int32_t* accept_len, int32_t* next_anchor, int32_t* anchor_pos, cudaStream_t st);
 cudaError_t launch_kv_copy(bool write, __half* cells, int cap, int d, int n_kv, int pos0, int n, float* out,
                            const uint16_t* in, cudaStream_t st);
-cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, const int32_t* anchor_pos,
+cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,
                              const int32_t* block_len, int32_t* status, cudaStream_t stream);
 int attn_smem_bytes(int D, int gq);
 

@@ -46,25 +46,25 @@ struct Fmt;
 
 template <>
 struct Fmt<WT_BF16> {
-  static constexpr int CB = 4, SUBB = 1, CHUNK = 1024, STAGES = 4;
+  static constexpr int CB = 4, SUBB = 1, CHUNK = 1024, STAGES = 8;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 16384
   static constexpr bool kF16 = false;                   // activations bf16
 };
 template <>
 struct Fmt<WT_Q8_0> {
-  static constexpr int CB = 8, SUBB = 1, CHUNK = 544, STAGES = 4;
+  static constexpr int CB = 8, SUBB = 1, CHUNK = 544, STAGES = 8;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 17408
   static constexpr bool kF16 = true;
 };
 template <>
 struct Fmt<WT_Q4_0> {
-  static constexpr int CB = 8, SUBB = 2, CHUNK = 576, STAGES = 7;
+  static constexpr int CB = 8, SUBB = 2, CHUNK = 576, STAGES = 14;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 9216
   static constexpr bool kF16 = true;
 };
 template <>
 struct Fmt<WT_Q5_0> {
-  static constexpr int CB = 8, SUBB = 2, CHUNK = 704, STAGES = 6;
+  static constexpr int CB = 8, SUBB = 2, CHUNK = 704, STAGES = 12;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 11264
   static constexpr bool kF16 = true;
 };
@@ -72,7 +72,7 @@ struct Fmt<WT_Q5_0> {
 // two 64x64 TMA boxes with the 128-byte swizzle.
 template <>
 struct Fmt<WT_HEAD> {
-  static constexpr int CB = 4, SUBB = 1, CHUNK = 0, STAGES = 4;
+  static constexpr int CB = 4, SUBB = 1, CHUNK = 0, STAGES = 8;
   static constexpr int UNIT = 64 * 128 * 2;  // 16384
   static constexpr bool kF16 = false;
 };
@@ -85,6 +85,21 @@ inline size_t packed_bytes(int wtype, int n, int k) {
     case WT_Q5_0: return size_t(n / 64) * (k / (32 * Fmt<WT_Q5_0>::CB)) * Fmt<WT_Q5_0>::UNIT;
   }
   return 0;
+}
+
+// Streamed activations ("chunked" layout).  A GEMV that streams X copies,
+// with each weight unit, the unit's KU input columns of all R activation rows
+// as one contiguous chunk per plane.  Element (row r, column k, plane p):
+//   ((j * planes + p) * R + r) * (KU + 32) + (k - j * KU),   j = k / KU
+// in 16-bit elements; rows are padded by 32 elements so that the consumer's
+// 16-byte lane loads of neighbouring rows fall in different banks.  BF16
+// activations have two planes (hi, lo = x - hi), FP16 ones a single plane.
+__host__ __device__ __forceinline__ size_t xchunk_index(int k, int r, int p, int R, int KU, int planes) {
+  const int j = k / KU;
+  return ((static_cast<size_t>(j) * planes + p) * R + r) * (KU + 32) + (k - j * KU);
+}
+inline size_t xchunk_elems(int K, int R, int KU, int planes) {
+  return static_cast<size_t>(K / KU) * planes * R * (KU + 32);
 }
 
 // Row of the 64-row group that mma row m (0..15) of m-tile w computes.  The

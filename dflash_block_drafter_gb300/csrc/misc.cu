@@ -248,8 +248,15 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const __grid_constant
   const float rs = r < a.rows_valid ? rsqrtf(tot / a.H + a.eps) : 0.f;
   for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
     const float v = r < a.rows_valid ? __ldcg(xr + k) * rs * a.w[k] : 0.f;
-    if (a.out_f16) static_cast<__half*>(a.out)[static_cast<size_t>(r) * a.H + k] = __float2half_rn(v);
-    else static_cast<__nv_bfloat16*>(a.out)[static_cast<size_t>(r) * a.H + k] = __float2bfloat16_rn(v);
+    const int R = gridDim.x;
+    if (a.out_f16) {
+      static_cast<__half*>(a.out)[xchunk_index(k, r, 0, R, a.ku, 1)] = __float2half_rn(v);
+    } else {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      o[xchunk_index(k, r, 0, R, a.ku, 2)] = hi;
+      o[xchunk_index(k, r, 1, R, a.ku, 2)] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
     if (a.f32_out && r < a.rows_f32) a.f32_out[static_cast<size_t>(r) * a.H + k] = v;
   }
 }

@@ -274,12 +274,29 @@ int32_t dflash_fuse_launches(const dflash_state* state, int32_t n);
  * pass.  NULL, NULL switches it off. */
 int dflash_state_set_head_events(dflash_state* state, void* ev_begin, void* ev_end);
 
+/* Profiling aid: with n_events > 0, every following dflash_fuse_context and
+ * dflash_draft_block call on this state records events[0], events[1], ... on
+ * its stream, one immediately before each kernel it launches and one after
+ * the last, up to n_events (cudaEvent_t handles created by the caller; the
+ * array is copied).  Elapsed time between consecutive events is the time of
+ * one kernel (recording between kernels removes their launch overlap, so
+ * this is for breakdowns, not for headline timing).  n_events = 0 switches it
+ * off.  At most 256 events. */
+int dflash_state_set_profile_events(dflash_state* state, void* const* events, int32_t n_events);
+
+/* Tuning: number of context chunks the attention of a draft pass splits each
+ * (sequence, kv head) into (split-context / flash-decode).  The default is
+ * chosen at state creation from the capacity and the SM count; valid values
+ * are 1 .. the maximum the state was sized for (returned in *max_chunks when
+ * non-NULL; pass chunks = 0 to only query).  Applies to later calls. */
+int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* max_chunks);
+
 /* Greedy ids over the target's LM head for n_rows (1..8) rows of final
  * hidden states, for callers that cannot allocate device memory: code that
  * runs while a CUDA graph is being captured, engines that own all device
  * memory as one arena reserved up front, or loops that must never enter the
  * allocator.  It needs no dflash_state: its scratch is a fixed array of about
- * 1.2 MB inside the library (held by every GPU that loads it until exit), and
+ * 1.35 MB inside the library (held by every GPU that loads it until exit), and
  * it allocates nothing.  The pages have no counterpart of this entry point.
  *   hidden: [n_rows, H] float, rows already through the final RMSNorm (the
  *           final_hidden output of dflash_draft_block is such a row set).

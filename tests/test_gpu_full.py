@@ -92,7 +92,7 @@ def test_full_quantised(wtype):
     st.draft(1)
     res = O.draft_block(om, ost, anchor, ctx, B)
     _check_pass(st, ost, res, 0, ctx, B, f"full {wtype}")
-    for which, name in ((0, "fc"), (4, "layers.0.wo"), (34, "layers.4.w_down")):
+    for which, name in ((0, "fc"), (4, "layers.0.wo"), (35, "layers.4.w_down")):
         got = model.dequantize(which).cpu().numpy().astype(np.float64)
         assert np.array_equal(got, om.mat(name)), name
     assert st.take_status() == 0

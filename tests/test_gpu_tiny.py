@@ -234,3 +234,23 @@ def test_accept_matches_oracle():
     for s in range(n_seq):
         n, bonus = O.accept(drafts[s], tgt[s], int(Bs[s]))
         assert int(d_acc[s]) == n and int(d_next[s]) == bonus and int(d_pos[s]) == pos[s] + n + 1, s
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 7, 10])
+def test_attention_context_chunks(chunks):
+    """The split-context attention and its log-sum-exp merge: a 600-position
+    context split into 1..10 chunks (7 leaves empty chunks) gives the
+    oracle's pass."""
+    import dflash_block_drafter_gb300 as D
+    cfg = synth.CONFIGS["tiny"]
+    ck, model, om = _model(cfg, seed=30)
+    cap = 640
+    st = _state(model, 1, cap)
+    assert D.dflash_state_set_attn_chunks(st.handle, 0) >= 10
+    D.dflash_state_set_attn_chunks(st.handle, chunks)
+    ost = _ostate(om, cfg, cap)
+    _fuse_both(st, ost, 0, cfg, synth.make_taps(cfg, 600, seed=30), np.arange(600))
+    (res,) = _draft_both(st, [ost], [77], [600], [6])
+    check_hidden(st.final_hidden[0, :6].cpu().numpy(), res.final_hidden)
+    check_drafts(st.drafts[0].cpu().numpy(), res, 6)
+    assert st.take_status() == 0
