@@ -25,6 +25,15 @@ DFLASH_DECLARE_GEMV(WT_Q5_0)
 DFLASH_DECLARE_GEMV(WT_Q4_0)
 cudaError_t gemv_argmax(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc);
 
+// Diagnostic builds: the next per-CTA timestamp slot of a launch.
+unsigned long long* trace_slot(State& st) {
+#ifdef DFLASH_TRACE
+  if (st.trace && st.trace_k < st.trace_launches)
+    return st.trace + static_cast<size_t>(st.trace_k++) * st.max_grid * 8;
+#endif
+  (void)st;
+  return nullptr;
+}
 }  // namespace dflash
 
 using namespace dflash;
@@ -169,15 +178,6 @@ int pow2ceil(int v) {
   return p;
 }
 
-// Diagnostic builds: the next per-CTA timestamp slot of a GEMV launch.
-unsigned long long* trace_slot(State& st) {
-#ifdef DFLASH_TRACE
-  if (st.trace && st.trace_k < st.trace_launches)
-    return st.trace + static_cast<size_t>(st.trace_k++) * st.max_grid * 8;
-#endif
-  (void)st;
-  return nullptr;
-}
 
 GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* status) {
   GemvArgs a;
@@ -282,7 +282,9 @@ int dflash_config_check(const dflash_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return DFLASH_ERR_UNSUPPORTED;
   if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return DFLASH_ERR_UNSUPPORTED;
   const int gq = c->n_q_heads / c->n_kv_heads;
-  if ((gq * 8) % 16 || gq * 8 > 224) return DFLASH_ERR_UNSUPPORTED;
+  if ((gq * 8) % 16 || gq * 8 > 128) return DFLASH_ERR_UNSUPPORTED;
+  // the attention CTA holds the M = 8 * gq query rows, two K and two V tiles and P in shared memory
+  if (attn_smem_bytes(c->head_dim, gq * 8) > 232448) return DFLASH_ERR_UNSUPPORTED;
   if (c->hidden < 256 || c->hidden % 256) return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_q_heads * c->head_dim) % 256 || c->intermediate < 256 || c->intermediate % 256)
     return DFLASH_ERR_UNSUPPORTED;
@@ -445,16 +447,18 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   const int gq = nq / nkv;
   const int M = gq * 8;
   {
-    // default: ~2 key tiles per CTA, at most 2 CTAs per SM; buffers sized for
-    // up to 4 CTAs per SM (and at most 512 chunks, the merge kernel's limit)
-    const long long tiles = (capacity + 63) / 64;
+    // default: one 128-key super-tile per CTA, at most one CTA per SM (each
+    // holds 225 KB of shared memory and 512 TMEM columns); buffers sized for
+    // up to 4 CTAs' worth of chunks per SM (and at most 512 chunks, the merge
+    // kernel's limit)
+    const long long tiles = (capacity + 127) / 128;
     const long long per = static_cast<long long>(n_slots) * nkv;
     long long cmax = (4LL * m->sm_count) / per;
     cmax = cmax < 1 ? 1 : (cmax > 512 ? 512 : cmax);
     if (cmax > tiles) cmax = tiles;
-    long long cdef = (tiles + 1) / 2;
-    const long long cap2 = (2LL * m->sm_count) / per;
-    if (cdef > cap2) cdef = cap2;
+    long long cdef = tiles;
+    const long long cap1 = m->sm_count / per;
+    if (cdef > cap1) cdef = cap1;
     if (cdef > cmax) cdef = cmax;
     if (cdef < 1) cdef = 1;
     s->attn_chunks = static_cast<int>(cdef);
@@ -474,7 +478,7 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->attn_out, xchunk_elems(nq * d, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->hbuf, xchunk_elems(I, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->xnorm, xchunk_elems(H, R, 128, 2) * 2, &total));
-  STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 4, &total));
+  STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 2, &total));
   STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks_max * M * 8, &total));
   s->max_grid = 2 * m->sm_count;
   const int rmax = 128;
@@ -498,6 +502,8 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   if (cudaMemset(s->status, 0, 16) != cudaSuccess) return fail(cuda_fail(cudaGetLastError(), "cudaMemset"));
   STRY(make_map_2d(&s->q_map, s->q_ready, static_cast<uint64_t>(s->nt) * nkv * M, d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                    static_cast<uint32_t>(M)));
+  STRY(make_map_2d(&s->part_map, s->attn_part, static_cast<uint64_t>(n_slots) * nkv * s->attn_chunks_max * M, d,
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<uint32_t>(M)));
   STRY(make_map_2d(&s->k_map, s->K, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   STRY(make_map_2d(&s->v_map, s->V, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   {

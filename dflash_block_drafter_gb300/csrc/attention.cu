@@ -4,18 +4,15 @@
 // runtime" -- GQA 24 Q / 2 KV, head dim 256).
 //
 // For one slot and one kv head the queries are the GQ = n_q / n_kv q heads
-// of the block's 8 rows: M = 8 * GQ rows (96 for DFlash) sharing every key.
-// The keys are the slot's position-addressed cells [0, p + B): the fused
-// context plus the block's own rows, which the QKV epilogue wrote at
-// [p, p + B).  The context is split into C chunks (split-K / flash-decode):
-// CTA (chunk, kv head, slot) streams its 64-key K and V tiles through a
-// 2-stage ring with 2-D TMA copies (64 x 64 boxes, 128-byte swizzle) issued
-// by a producer warp, and each consumer warp owns 16 query rows:
-//   S = Q K^T (mma.sync m16n8k16, fp16 in, fp32 out) -> online softmax in
-//   base 2 -> O += P V.
-// With C > 1 every chunk writes (O unnormalised, running max, sum) and
-// attn_combine_kernel merges them with the log-sum-exp rule; with C == 1 the
-// CTA normalises and writes the output directly.
+// of the block's 8 rows: M = 8 * GQ rows (96 for DFlash) sharing every key,
+// so QK^T and PV are real matrix products and run on the tcgen05 tensor
+// cores.  The keys are the slot's position-addressed cells [0, p + B): the
+// fused context plus the block's own rows, which the QKV epilogue wrote at
+// [p, p + B).  The context is split into C chunks of 128-key super-tiles
+// (split-K / flash-decode).  With C > 1 every chunk writes (O unnormalised,
+// running max, sum) and attn_combine_kernel merges them with the
+// log-sum-exp rule; with C == 1 the CTA normalises and writes the output
+// directly.
 #include "kernels.h"
 #include "layout.cuh"
 
@@ -27,385 +24,619 @@ struct AttnArgs {
   CUtensorMap vmap;
   const int32_t* anchor_pos;
   const int32_t* block_len;
-  float* part;            // [slots, n_kv, C, M, d]
-  float2* ml;             // [slots, n_kv, C, M]
+  CUtensorMap pmap;       // chunk partials O / l: [slots * n_kv * C * M, d] fp16, 64 x M boxes
+  float2* ml;             // [slots, n_kv, C, M]: running max (log2 units) and sum per row
   void* out;              // attention output in the o-projection's chunked X layout (C == 1)
   int out_f16;            // 1: one FP16 plane; 0: BF16 hi and lo planes
   int out_rows, out_ku;   // chunked layout: rows R of the pass and inputs per unit
   int layer, n_slots, n_kv, n_q, gq, cap, C, n_seq;
   int32_t* status;
+  unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
 
-constexpr int kAttnKT = 64;      // keys per tile
-constexpr int kAttnStages = 2;
+#ifdef DFLASH_TRACE
+#define DFLASH_ATTN_STAMP(k)                                                                                  \
+  do {                                                                                                        \
+    if (a.trace)                                                                                              \
+      a.trace[(static_cast<size_t>(blockIdx.z) * gridDim.y * gridDim.x + blockIdx.y * gridDim.x + blockIdx.x) * 8 + \
+              (k)] = globaltimer_ns();                                                                        \
+  } while (0)
+#else
+#define DFLASH_ATTN_STAMP(k) \
+  do {                       \
+  } while (0)
+#endif
+
+// ---------------------------------------------------------------------------
+// tcgen05 attention.  Per CTA (chunk, kv head, slot) the M = 8 * GQ query rows
+// (96 for DFlash) are multiplied against the chunk's keys in super-tiles of
+// 128 keys:
+//   warp 0       TMA producer: Q once, then per super-tile two 64-key K tiles
+//                and two V tiles (64 x 64 boxes, 128-byte swizzle);
+//   warp 1       owns the tensor memory and, from one thread, issues
+//                tcgen05.mma: S[j % 2] = Q K_j^T (M 128, N 64, K 16 per
+//                instruction, FP32 in TMEM) and O += P_j V_j (N = d, V read
+//                MN-major straight from its TMA tile);
+//   warps 2..17  softmax: warp w reads TMEM lane quarter w % 4 (query rows
+//                32 (w % 4) ..) and key slice (w - 2) / 4 (32 of the 128 keys;
+//                d / 4 columns of O).  Row maxima are combined across the 4
+//                slices through shared memory; P = 2^(s - m) goes to shared
+//                memory as FP16 in the 128-byte-swizzled K-major layout the
+//                MMA reads; O is rescaled in TMEM when a row's maximum grows.
+// S is double-buffered in TMEM so the next super-tile's QK^T overlaps the
+// softmax; O (d columns) accumulates in TMEM across the chunk.
+//
+// Q occupies only its M rows per 64-column box; the MMA's rows M..127 read
+// whatever follows (the next box, or the K buffer): finite values whose
+// scores, probabilities and outputs stay in those rows and are never used.
+// A lane quarter with no query row skips the softmax arithmetic.
+//
+// Every wait is bounded.  After a timeout a warp stops waiting but still
+// takes every named barrier of the softmax group, so all warps finish.
+constexpr int kTcKT = 64;                             // keys per TMA tile
+constexpr int kTcKS = 2 * kTcKT;                      // keys per super-tile
+constexpr int kTcTmemCols = 512;                      // S0 [0,128), S1 [128,256), O [256, 256 + d)
+constexpr int kTcSoftWarps = 16;                      // 4 per TMEM lane quarter
+constexpr int kTcSoftThreads = 32 * kTcSoftWarps;
+constexpr int kTcThreads = 64 + kTcSoftThreads;
 
 template <int D>
-struct AttnGeom {
+struct TcGeom {
   static constexpr int BOXES = D / 64;
-  static constexpr int TILE_BYTES = kAttnKT * D * 2;  // one K (or V) tile
+  static constexpr int TILE_BYTES = kTcKT * D * 2;
+  static constexpr int P_BYTES = 128 * kTcKS * 2;
+  static constexpr int RED_BYTES = (2 * 4 * 128 + 4 * 128) * 4;  // row maxima (double-buffered), row sums
+  // Q rows: M x D FP16 (a multiple of 1024 bytes for M % 16 == 0)
   static __host__ __device__ constexpr int q_bytes(int M) { return M * D * 2; }
   static __host__ __device__ constexpr int smem(int M) {
-    return 1024 + q_bytes(M) + 2 * kAttnStages * TILE_BYTES + 4 * kAttnStages * 8 + 64 + 8;
+    return 1024 + q_bytes(M) + 4 * TILE_BYTES + P_BYTES + RED_BYTES + 256;
   }
 };
 
-// Address of element-chunk (row, 16-byte chunk q within the 64-wide box)
-// inside a run of 64-column boxes of `rows` rows with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int rows, int row, int col8) {
-  const int box = col8 >> 3, q = col8 & 7;
-  return base + box * rows * 128 + row * 128 + ((q ^ (row & 7)) << 4);
+// N consecutive columns (16, 32 or 64) of this thread's TMEM lane, times `scale`.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t addr, float (&v)[N], float scale) {
+  if constexpr (N == 16) {
+    uint32_t r[16];
+    tmem_ld16(addr, r);
+    tmem_wait_ld();
+    tmem_reg_fence(r);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]) * scale;
+  } else {
+    static_assert(N % 32 == 0 && N <= 64, "column count");
+    uint32_t r[N / 32][32];
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) tmem_ld32(addr + h * 32, r[h]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+      tmem_reg_fence(r[h]);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[h * 32 + e] = __uint_as_float(r[h][e]) * scale;
+    }
+  }
+}
+
+// Multiply N consecutive columns of this thread's TMEM lane by `scale` in place.
+template <int N>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t addr, float scale) {
+  if constexpr (N == 16) {
+    uint32_t r[16];
+    tmem_ld16(addr, r);
+    tmem_wait_ld();
+    tmem_reg_fence(r);
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            addr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]),
+        "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+        : "memory");
+  } else {
+#pragma unroll 1
+    for (int h = 0; h < N / 32; ++h) {
+      uint32_t r[32];
+      tmem_ld32(addr + h * 32, r);
+      tmem_wait_ld();
+      tmem_reg_fence(r);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
+      tmem_st32(addr + h * 32, r);
+    }
+  }
+  tmem_wait_st();
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) attn_kernel(const __grid_constant__ AttnArgs a) {
-  using Geo = AttnGeom<D>;
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
+  using Geo = TcGeom<D>;
+  constexpr int OC = D / 4;  // O columns per softmax warp
   const int M = a.gq * 8;
-  const int NW = M / 16;  // consumer warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem;
-  uint8_t* sk = sq + ((Geo::q_bytes(M) + 1023) / 1024) * 1024;
-  uint8_t* sv = sk + kAttnStages * Geo::TILE_BYTES;
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(sv + kAttnStages * Geo::TILE_BYTES);
-  uint64_t* vfull = kfull + kAttnStages;
-  uint64_t* empty = vfull + kAttnStages;
-  uint64_t* qbar = empty + kAttnStages;
+  uint8_t* sq = smem;                                  // [D/64 boxes][M rows][128 B]
+  uint8_t* sk = sq + Geo::q_bytes(M);                  // 2 tiles of [D/64 boxes][64 keys][128 B]
+  uint8_t* sv = sk + 2 * Geo::TILE_BYTES;              // 2 tiles
+  uint8_t* sp = sv + 2 * Geo::TILE_BYTES;              // [2 boxes][128 rows][128 B]
+  float* red_max = reinterpret_cast<float*>(sp + Geo::P_BYTES);  // [2][4 slices][128 rows]
+  float* red_l = red_max + 2 * 4 * 128;                          // [4 slices][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 128);
+  uint64_t* qfull = bars + 0;
+  uint64_t* kfull = bars + 1;
+  uint64_t* kfree = bars + 2;
+  uint64_t* vfull = bars + 3;
+  uint64_t* vfree = bars + 4;
+  uint64_t* sfull = bars + 5;   // [2]
+  uint64_t* sfree = bars + 7;   // [2]
+  uint64_t* pfull = bars + 9;
+  uint64_t* pfree = bars + 10;
+  uint64_t* mdone = bars + 11;  // every MMA of the CTA has completed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  if (tid == 0) DFLASH_ATTN_STAMP(0);
 
-  // key range of this chunk
+  // key range of this chunk, in super-tiles
   const int p = a.anchor_pos[s];
   int B = a.block_len[s];
   B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
   int T = p + B;
   T = T < 0 ? 0 : (T > a.cap ? a.cap : T);
-  const int ntiles = (T + kAttnKT - 1) / kAttnKT;
-  const int tpc = (ntiles + a.C - 1) / a.C;
-  const int t0 = c * tpc;
-  const int t1 = min(ntiles, t0 + tpc);
-  const int nt = t1 > t0 ? t1 - t0 : 0;
+  const int nst_all = (T + kTcKS - 1) / kTcKS;
+  const int spc = (nst_all + a.C - 1) / a.C;
+  const int st0 = c * spc;
+  const int st1 = min(nst_all, st0 + spc);
+  const int nst = st1 > st0 ? st1 - st0 : 0;
   const int row0 = ((a.layer * a.n_slots + s) * a.n_kv + g) * a.cap;
 
   if (tid == 0) {
-    for (int i = 0; i < kAttnStages; ++i) {
-      mbar_init(&kfull[i], 1);
-      mbar_init(&vfull[i], 1);
-      mbar_init(&empty[i], NW);
-    }
-    mbar_init(qbar, 1);
+    mbar_init(qfull, 1);
+    mbar_init(kfull, 1);
+    mbar_init(kfree, 1);
+    mbar_init(vfull, 1);
+    mbar_init(vfree, 1);
+    mbar_init(&sfull[0], 1);
+    mbar_init(&sfull[1], 1);
+    mbar_init(&sfree[0], kTcSoftWarps);
+    mbar_init(&sfree[1], kTcSoftWarps);
+    mbar_init(pfull, kTcSoftWarps);
+    mbar_init(pfree, 1);
+    mbar_init(mdone, 1);
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTcTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  bool ok = true;
 
-  if (warp == NW) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && nst > 0) {
       prefetch_tensormap(&a.qmap);
       prefetch_tensormap(&a.kmap);
       prefetch_tensormap(&a.vmap);
-      auto issue = [&](int it) {
-        const int st = it % kAttnStages;
-        const int y = row0 + (t0 + it) * kAttnKT;
-        mbar_arrive_expect_tx(&kfull[st], Geo::TILE_BYTES);
-        for (int b = 0; b < Geo::BOXES; ++b)
-          tma_load_2d(sk + st * Geo::TILE_BYTES + b * kAttnKT * 128, &a.kmap, b * 64, y, &kfull[st]);
-        mbar_arrive_expect_tx(&vfull[st], Geo::TILE_BYTES);
-        for (int b = 0; b < Geo::BOXES; ++b)
-          tma_load_2d(sv + st * Geo::TILE_BYTES + b * kAttnKT * 128, &a.vmap, b * 64, y, &vfull[st]);
+      auto issue_k = [&](int j) {
+        const int y = row0 + (st0 + j) * kTcKS;
+        mbar_arrive_expect_tx(kfull, 2 * Geo::TILE_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int b = 0; b < Geo::BOXES; ++b)
+            tma_load_2d(sk + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.kmap, b * 64, y + t * kTcKT, kfull);
       };
-      // Tiles wholly inside the fused context [0, p) do not depend on the
-      // previous kernel (which writes the block cells) and may start early.
-      int it = 0;
-      const int n_pre = nt < kAttnStages ? nt : kAttnStages;
-      for (; it < n_pre && (t0 + it + 1) * kAttnKT <= p; ++it) issue(it);
+      auto issue_v = [&](int j) {
+        const int y = row0 + (st0 + j) * kTcKS;
+        mbar_arrive_expect_tx(vfull, 2 * Geo::TILE_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int b = 0; b < Geo::BOXES; ++b)
+            tma_load_2d(sv + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.vmap, b * 64, y + t * kTcKT, vfull);
+      };
+      // A first super-tile wholly inside the fused context [0, p) does not
+      // depend on the previous kernel (which writes the block cells).
+      const bool early = (st0 + 1) * kTcKS <= p;
+      if (early) {
+        issue_k(0);
+        issue_v(0);
+      }
       pdl_wait();
-      // the queries (written by the previous kernel): one 64-column box each
-      mbar_arrive_expect_tx(qbar, Geo::q_bytes(M));
-      for (int b = 0; b < Geo::BOXES; ++b)
-        tma_load_2d(sq + b * M * 128, &a.qmap, b * 64, (s * a.n_kv + g) * M, qbar);
-      int issued = it;
-      for (; it < nt; ++it) {
-        if (it >= kAttnStages && !mbar_wait(&empty[it % kAttnStages], ((it / kAttnStages) - 1) & 1)) {
-          set_status(a.status, DFLASH_DEV_TIMEOUT);
-          break;
-        }
-        issue(it);
-        issued = it + 1;
+      mbar_arrive_expect_tx(qfull, M * D * 2);
+      for (int b = 0; b < Geo::BOXES; ++b) tma_load_2d(sq + b * (M * 128), &a.qmap, b * 64, (s * a.n_kv + g) * M, qfull);
+      if (!early) {
+        issue_k(0);
+        issue_v(0);
       }
-      for (int j = (issued > kAttnStages ? issued - kAttnStages : 0); j < issued; ++j) {
-        if (!mbar_wait(&kfull[j % kAttnStages], (j / kAttnStages) & 1) ||
-            !mbar_wait(&vfull[j % kAttnStages], (j / kAttnStages) & 1)) {
-          set_status(a.status, DFLASH_DEV_TIMEOUT);
-          break;
-        }
+      int nk = 1, nv = 1;  // super-tiles issued
+      for (int j = 1; j < nst; ++j) {
+        if (!mbar_wait(kfree, (j - 1) & 1)) { ok = false; break; }
+        issue_k(j);
+        ++nk;
+        if (!mbar_wait(vfree, (j - 1) & 1)) { ok = false; break; }
+        issue_v(j);
+        ++nv;
       }
+      // Only the last K and V copies can still be in flight (each earlier one
+      // was consumed before its buffer was refilled); they and Q must land
+      // before the CTA may exit, also after a timeout.
+      if (!mbar_wait(qfull, 0)) ok = false;
+      if (!mbar_wait(kfull, (nk - 1) & 1)) ok = false;
+      if (!mbar_wait(vfull, (nv - 1) & 1)) ok = false;
+      if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
     }
-    return;
-  }
-  if (warp > NW) return;
-
-  // -------------------------------------------------------------- consumers
-  pdl_wait();
-  pdl_launch_dependents();
-  if (!mbar_wait(qbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
-
-  constexpr float LOG2E = 1.4426950408889634f;
-  constexpr int NDT = D / 8;  // output n-tiles
-  float o[NDT][4];
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nst > 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_f16(128, kTcKT, false, false);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(128, D, false, true);
+      const uint32_t q_s = smem_u32(sq), k_s = smem_u32(sk), v_s = smem_u32(sv), p_s = smem_u32(sp);
+      const uint32_t q_box = static_cast<uint32_t>(M) * 128;
+      // S[j % 2] = Q K_j^T; the K buffer is released when it completes
+      auto issue_qk = [&](int j) -> bool {
+        if (!mbar_wait(kfull, j & 1)) return false;
+        if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-  for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_r = -INFINITY, m_r8 = -INFINITY, l_r = 0.f, l_r8 = 0.f;
-
-  const uint32_t qb = smem_u32(sq);
-  const int wr0 = warp * 16;
-  // ldmatrix row/col selectors
-  const int a_row = wr0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int a_c8 = lane >> 4;
-  const int b_key = (lane & 7) + (lane >> 4) * 8;
-  const int b_c8 = (lane >> 3) & 1;
-  const int v_key = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int v_c8 = lane >> 4;
-
-  bool ok = true;
-  for (int it = 0; it < nt && ok; ++it) {
-    const int st = it % kAttnStages;
-    const uint32_t par = (it / kAttnStages) & 1;
-    if (!mbar_wait(&kfull[st], par)) {
-      set_status(a.status, DFLASH_DEV_TIMEOUT);
-      ok = false;
-      break;
-    }
-    const uint32_t kb = smem_u32(sk + st * Geo::TILE_BYTES);
-    const uint32_t vb = smem_u32(sv + st * Geo::TILE_BYTES);
-    float sacc[8][4];
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da = umma_desc_sw128(q_s + (kk >> 2) * q_box + (kk & 3) * 32, 16, 1024);
+            const uint64_t db =
+                umma_desc_sw128(k_s + t * Geo::TILE_BYTES + (kk >> 2) * (kTcKT * 128) + (kk & 3) * 32, 16, 1024);
+            umma_f16(tmem + (j & 1) * kTcKS + t * kTcKT, da, db, idesc_qk, kk > 0);
+          }
+        umma_commit(&sfull[j & 1]);
+        umma_commit(kfree);
+        return true;
+      };
+      // QK^T of super-tile j + 1 is issued before the PV of super-tile j, so it
+      // runs while the softmax warps work on S[j % 2].
+      if (!mbar_wait(qfull, 0) || !issue_qk(0)) ok = false;
+      for (int j = 0; j < nst && ok; ++j) {
+        if (j + 1 < nst && !issue_qk(j + 1)) { ok = false; break; }
+        if (!mbar_wait(pfull, j & 1) || !mbar_wait(vfull, j & 1)) { ok = false; break; }
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll 4
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(a0, a1, a2, a3, swz(qb, M, a_row, kk * 2 + a_c8));
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, swz(kb, kAttnKT, np * 16 + b_key, kk * 2 + b_c8));
-        mma_f16_16816(sacc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_f16_16816(sacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+          for (int kk = 0; kk < kTcKT / 16; ++kk) {
+            const uint64_t da = umma_desc_sw128(p_s + t * 16384 + kk * 32, 16, 1024);
+            const uint64_t db = umma_desc_sw128(v_s + t * Geo::TILE_BYTES + kk * 2048, kTcKT * 128, 1024);
+            umma_f16(tmem + 2 * kTcKS, da, db, idesc_pv, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
+          }
+        umma_commit(pfree);
+        umma_commit(vfree);
       }
-    }
-    // mask keys beyond T, scale to base 2, online softmax
-    const int kbase = (t0 + it) * kAttnKT + (lane & 3) * 2;
-    float mx = -INFINITY, mx8 = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = kbase + n * 8 + (e & 1);
-        const float v = key < T ? sacc[n][e] * LOG2E : -INFINITY;
-        sacc[n][e] = v;
-        if (e < 2) mx = fmaxf(mx, v); else mx8 = fmaxf(mx8, v);
-      }
-#pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      mx8 = fmaxf(mx8, __shfl_xor_sync(0xffffffffu, mx8, off));
-    }
-    const float mn = fmaxf(m_r, mx), mn8 = fmaxf(m_r8, mx8);
-    const float base = mn == -INFINITY ? 0.f : mn;
-    const float base8 = mn8 == -INFINITY ? 0.f : mn8;
-    const float corr = exp2f(m_r - base), corr8 = exp2f(m_r8 - base8);
-    m_r = mn;
-    m_r8 = mn8;
-    float ls = 0.f, ls8 = 0.f;
-    uint32_t pa[4][4];  // P as A fragments, 4 k-steps of 16 keys
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const float p0 = exp2f(sacc[n][0] - base), p1 = exp2f(sacc[n][1] - base);
-      const float p2 = exp2f(sacc[n][2] - base8), p3 = exp2f(sacc[n][3] - base8);
-      ls += p0 + p1;
-      ls8 += p2 + p3;
-      const int ks = n >> 1, hi = n & 1;
-      pa[ks][hi * 2 + 0] = pack_f16x2(p0, p1);
-      pa[ks][hi * 2 + 1] = pack_f16x2(p2, p3);
-    }
-    l_r = l_r * corr + ls;
-    l_r8 = l_r8 * corr8 + ls8;
-#pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-      o[i][0] *= corr; o[i][1] *= corr;
-      o[i][2] *= corr8; o[i][3] *= corr8;
-    }
-    if (!mbar_wait(&vfull[st], par)) {
-      set_status(a.status, DFLASH_DEV_TIMEOUT);
-      ok = false;
-      break;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(b0, b1, b2, b3, swz(vb, kAttnKT, ks * 16 + v_key, dp * 2 + v_c8));
-        mma_f16_16816(o[2 * dp], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
-        mma_f16_16816(o[2 * dp + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-
-  // row sums across the quad
-#pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
-    l_r += __shfl_xor_sync(0xffffffffu, l_r, off);
-    l_r8 += __shfl_xor_sync(0xffffffffu, l_r8, off);
-  }
-  const int m0 = wr0 + (lane >> 2), m1 = m0 + 8;
-  if (a.C == 1) {
-    const float inv = l_r > 0.f ? 1.f / l_r : 0.f, inv8 = l_r8 > 0.f ? 1.f / l_r8 : 0.f;
-    if (!(l_r > 0.f) || !(l_r8 > 0.f)) set_status(a.status, DFLASH_DEV_NONFINITE);
-    const int P = a.out_f16 ? 1 : 2;
-    const int row0 = s * 8 + (m0 & 7), row1 = s * 8 + (m1 & 7);
-    const int c0 = (g * a.gq + (m0 >> 3)) * D, c1 = (g * a.gq + (m1 >> 3)) * D;
-#pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-      const int col = i * 8 + (lane & 3) * 2;
-      const size_t o0 = xchunk_index(c0 + col, row0, 0, a.out_rows, a.out_ku, P);
-      const size_t o1 = xchunk_index(c1 + col, row1, 0, a.out_rows, a.out_ku, P);
-      if (a.out_f16) {
-        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + o0) = pack_f16x2(o[i][0] * inv, o[i][1] * inv);
-        *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + o1) = pack_f16x2(o[i][2] * inv8, o[i][3] * inv8);
-      } else {
-        uint32_t h0, l0, h1, l1;
-        split_bf16x2(o[i][0] * inv, o[i][1] * inv, h0, l0);
-        split_bf16x2(o[i][2] * inv8, o[i][3] * inv8, h1, l1);
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out);
-        const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);  // next plane of the chunk
-        *reinterpret_cast<uint32_t*>(ob + o0) = h0;
-        *reinterpret_cast<uint32_t*>(ob + o1) = h1;
-        *reinterpret_cast<uint32_t*>(ob + o0 + lo_off) = l0;
-        *reinterpret_cast<uint32_t*>(ob + o1 + lo_off) = l1;
-      }
+      // tensor memory may only be freed once every issued MMA has finished
+      umma_commit(mdone);
+      if (!mbar_wait(mdone, 0)) ok = false;
+      if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
     }
   } else {
-    const size_t pbase = ((static_cast<size_t>(s) * a.n_kv + g) * a.C + c) * M;
+    // ------------------------------------------------------------ softmax
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr float LOG2E = 1.4426950408889634f;
+    const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
+    const int cs = (warp - 2) >> 2;          // key slice (32 of 128) and O column slice (d / 4)
+    const int m = q4 * 32 + lane;            // query row = TMEM lane
+    const bool live = q4 * 32 < M;           // warp-uniform: the quarter holds query rows
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t o_addr = lane_addr + 2 * kTcKS + cs * OC;
+    float m_run = -INFINITY, l_part = 0.f;
+    for (int j = 0; j < nst; ++j) {
+      const int b = j & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sfull[b], (j >> 1) & 1));
+      if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(1);
+      tc_fence_after();
+      uint32_t r[32];
+      if (live) {
+        tmem_ld32(lane_addr + b * kTcKS + cs * 32, r);
+        tmem_wait_ld();
+        tmem_reg_fence(r);
+      }
+      // S[b] has been read: the next-but-one QK^T may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[b]);
+      // keys of this slice before T (the last super-tile's tail takes no weight)
+      const int nk = min(T - (st0 + j) * kTcKS, kTcKS) - cs * 32;
+      float mx = -INFINITY;
+      if (live) {
+        if (nk >= 32) {
 #pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-      const int col = i * 8 + (lane & 3) * 2;
-      __stcg(reinterpret_cast<float2*>(a.part + (pbase + m0) * D + col), make_float2(o[i][0], o[i][1]));
-      __stcg(reinterpret_cast<float2*>(a.part + (pbase + m1) * D + col), make_float2(o[i][2], o[i][3]));
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < nk) mx = fmaxf(mx, __uint_as_float(r[e]));
+        }
+      }
+      if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(2);
+      // row maximum over the 4 key slices
+      red_max[b * 512 + cs * 128 + m] = mx;
+      named_bar_sync(1, kTcSoftThreads);
+      {
+        const float* rm = red_max + b * 512 + m;
+        mx = fmaxf(fmaxf(rm[0], rm[128]), fmaxf(rm[256], rm[384]));
+      }
+      if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(3);
+      const float m_new = fmaxf(m_run, mx * LOG2E);
+      const float base = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - base);  // 0 on the first super-tile
+      // P buffer and O are free once the previous super-tile's PV is done
+      if (j > 0) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pfree, (j - 1) & 1));
+        tc_fence_after();
+        if (live && __any_sync(0xffffffffu, alpha < 1.f)) tmem_scale_cols<OC>(o_addr, alpha);
+      }
+      // P = 2^(s - m) as FP16: keys 32 cs .. 32 cs + 31 are box cs / 2,
+      // 16-byte chunks (cs % 2) * 4 .. + 3 of the row
+      float ls = 0.f;
+      if (live) {
+        uint32_t pk[16];
+        if (nk >= 32) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), LOG2E, -base));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), LOG2E, -base));
+            ls += p0 + p1;
+            pk[e >> 1] = pack_f16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = e < nk ? ex2_approx(fmaf(__uint_as_float(r[e]), LOG2E, -base)) : 0.f;
+            const float p1 = e + 1 < nk ? ex2_approx(fmaf(__uint_as_float(r[e + 1]), LOG2E, -base)) : 0.f;
+            ls += p0 + p1;
+            pk[e >> 1] = pack_f16x2(p0, p1);
+          }
+        }
+        uint8_t* prow = sp + (cs >> 1) * 16384 + m * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = ((cs & 1) * 4 + q) ^ (m & 7);
+          *reinterpret_cast<uint4*>(prow + ch * 16) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(4);
+      l_part = l_part * alpha + ls;
+      m_run = m_new;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+      if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(5);
     }
-    if ((lane & 3) == 0) {
-      __stcg(a.ml + pbase + m0, make_float2(m_r, l_r));
-      __stcg(a.ml + pbase + m1, make_float2(m_r8, l_r8));
+    // final O (after the last PV)
+    if (ok && nst > 0) ok = __all_sync(0xffffffffu, mbar_wait(pfree, (nst - 1) & 1));
+    tc_fence_after();
+    if (tid == 64) DFLASH_ATTN_STAMP(6);
+    if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
+    // row sum over the 4 key slices, in a fixed order
+    red_l[cs * 128 + m] = l_part;
+    named_bar_sync(1, kTcSoftThreads);
+    const float l_run = (red_l[m] + red_l[128 + m]) + (red_l[256 + m] + red_l[384 + m]);
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (a.C == 1) {
+      // normalised rows straight into the o-projection's input layout
+      if (live) {
+        float v[OC];
+        if (nst > 0) {
+          tmem_load_cols<OC>(o_addr, v, inv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < OC; ++e) v[e] = 0.f;
+        }
+        if (m < M) {
+          if (cs == 0 && !(l_run > 0.f)) set_status(a.status, DFLASH_DEV_NONFINITE);
+          const int hl = m >> 3, i = m & 7;
+          const int P = a.out_f16 ? 1 : 2;
+          const int row = s * 8 + i, col0 = (g * a.gq + hl) * D + cs * OC;
+          const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);
+#pragma unroll
+          for (int e8 = 0; e8 < OC; e8 += 8) {
+            const size_t o = xchunk_index(col0 + e8, row, 0, a.out_rows, a.out_ku, P);
+            if (a.out_f16) {
+              *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + o) =
+                  make_uint4(pack_f16x2(v[e8], v[e8 + 1]), pack_f16x2(v[e8 + 2], v[e8 + 3]),
+                             pack_f16x2(v[e8 + 4], v[e8 + 5]), pack_f16x2(v[e8 + 6], v[e8 + 7]));
+            } else {
+              uint4 hi, lo;
+              split_bf16x2(v[e8], v[e8 + 1], hi.x, lo.x);
+              split_bf16x2(v[e8 + 2], v[e8 + 3], hi.y, lo.y);
+              split_bf16x2(v[e8 + 4], v[e8 + 5], hi.z, lo.z);
+              split_bf16x2(v[e8 + 6], v[e8 + 7], hi.w, lo.w);
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) = hi;
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o + lo_off) = lo;
+            }
+          }
+        }
+      }
+    } else {
+      // The chunk's partial: O / l as FP16 rows plus (m, l) per row.  The rows
+      // are staged in the K buffer (free: the last QK^T completed before the
+      // last softmax) as D/64 boxes of M rows x 128 bytes with the 128-byte
+      // swizzle, then written by tensor-map stores.  An empty chunk writes
+      // only (m, l) = (-inf, 0); the merge gives it no weight.
+      const size_t pbase = ((static_cast<size_t>(s) * a.n_kv + g) * a.C + c) * M;
+      if (nst > 0) {
+        if (live) {
+          float v[OC];
+          tmem_load_cols<OC>(o_addr, v, inv);
+          if (m < M) {
+            const int col0 = cs * OC;
+            uint8_t* row = sk + (col0 >> 6) * (M * 128) + m * 128;
+#pragma unroll
+            for (int q = 0; q < OC / 8; ++q)
+              *reinterpret_cast<uint4*>(row + (((((col0 & 63) >> 3) + q) ^ (m & 7)) << 4)) =
+                  make_uint4(pack_f16x2(v[8 * q], v[8 * q + 1]), pack_f16x2(v[8 * q + 2], v[8 * q + 3]),
+                             pack_f16x2(v[8 * q + 4], v[8 * q + 5]), pack_f16x2(v[8 * q + 6], v[8 * q + 7]));
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kTcSoftThreads);
+        if (tid == 64) {
+          for (int h = 0; h < D / 64; ++h) tma_store_2d(&a.pmap, h * 64, static_cast<int>(pbase), sk + h * (M * 128));
+          bulk_commit_group();
+          bulk_wait_group_0();
+        }
+      }
+      if (cs == 0 && m < M) __stcg(a.ml + pbase + m, make_float2(m_run, l_run));
     }
+  }
+  // release the tensor memory once every tcgen05 operation of the CTA is done
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) DFLASH_ATTN_STAMP(7);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
   }
 }
 
 // Log-sum-exp merge of the C chunk partials of one (slot, q head): all 8 block
-// rows, a 64-column slice of the head (blockIdx.y).  The per-row merge weights
-// 2^(m_c - M) / L are computed once into shared memory; then 8 groups of 32
-// threads each sum every 8th chunk for 2 columns x 8 rows with independent
-// loads, and the groups are reduced through shared memory.
+// rows, a 32-column slice of the head (blockIdx.y).  Chunk c of row m carries
+// O_c / l_c (FP16) and (m_c, l_c); the row's output is
+//   sum_c w_c O_c / l_c,   w_c = l_c 2^(m_c - mx) / sum_c' l_c' 2^(m_c' - mx).
+// Lane = (row i = lane / 4, 8 columns from (lane % 4) * 8); warp w takes
+// chunks w, w + 8, ...  Each thread issues the loads of up to 8 of its chunks
+// (partial values and (m, l)) at once and folds them into a running
+// (max, sum, sum of weighted rows); the 8 warps' results are then combined
+// through shared memory in a fixed order (deterministic).
 struct CombineArgs {
-  const float* part;
+  const __half* part;
   const float2* ml;
   void* out;
   int out_f16;
   int out_rows, out_ku;
   int d, n_q, n_kv, gq, C;
   int32_t* status;
+  unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
 
 constexpr int kCombineMaxC = 512;
 
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineArgs a) {
-  __shared__ float sw[8][kCombineMaxC];
-  __shared__ float2 sacc[8][8][32];  // [chunk group][row][lane] partial sums of 2 columns
+  __shared__ float smx[8][32];
+  __shared__ float ssum[8][32];
+  __shared__ float4 sacc[8][32][2];
   const int hq = blockIdx.x, cb = blockIdx.y, s = blockIdx.z;
   const int g = hq / a.gq, hl = hq - g * a.gq;
   const int M = a.gq * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) DFLASH_ATTN_STAMP(0);
   pdl_wait();
+  if (threadIdx.x == 0) DFLASH_ATTN_STAMP(1);
   pdl_launch_dependents();
   const size_t base = (static_cast<size_t>(s) * a.n_kv + g) * a.C * M;
-  {
-    // warp i: merge weights of block row i
-    const int m = hl * 8 + warp;
+  const int i = lane >> 2, mrow = hl * 8 + i, col = cb * 32 + (lane & 3) * 8;
+  const __half* pr = a.part + (base + mrow) * a.d + col;
+  const float2* pml = a.ml + base + mrow;
+  const size_t cstride = static_cast<size_t>(M) * a.d;
+  float mw = -INFINITY, lw = 0.f, acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  constexpr int U = 8;
+  for (int c0 = warp; c0 < a.C; c0 += 8 * U) {
+    uint4 v[U];
+    float2 ml[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 8 * u;
+      if (c < a.C) {
+        ml[u] = __ldcg(pml + static_cast<size_t>(c) * M);
+        v[u] = __ldcg(reinterpret_cast<const uint4*>(pr + c * cstride));
+      } else {
+        ml[u] = make_float2(-INFINITY, 0.f);
+        v[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float bm = mw;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ml[u].y > 0.f) bm = fmaxf(bm, ml[u].x);
+    const float sc = mw == -INFINITY ? 0.f : ex2_approx(mw - bm);
+    lw *= sc;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= sc;
+    mw = bm;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ml[u].y > 0.f) {  // chunks without keys hold no partial
+        const float w = ml[u].y * ex2_approx(ml[u].x - bm);
+        lw += w;
+        const __half2* h = reinterpret_cast<const __half2*>(&v[u]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h[e]);
+          acc[2 * e] = fmaf(f.x, w, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(f.y, w, acc[2 * e + 1]);
+        }
+      }
+    }
+  }
+  smx[warp][lane] = mw;
+  ssum[warp][lane] = lw;
+  sacc[warp][lane][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  sacc[warp][lane][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (threadIdx.x == 0) DFLASH_ATTN_STAMP(2);
+  if (warp == 0) {
     float mx = -INFINITY;
-    for (int c = lane; c < a.C; c += 32) {
-      const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
-      if (v.y > 0.f) mx = fmaxf(mx, v.x);
-    }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float L = 0.f;
-    for (int c = lane; c < a.C; c += 32) {
-      const float2 v = __ldcg(a.ml + base + static_cast<size_t>(c) * M + m);
-      const float e = v.y > 0.f ? exp2f(v.x - mx) : 0.f;
-      sw[warp][c] = e;
-      L += v.y * e;
-    }
+    for (int w = 0; w < 8; ++w) mx = fmaxf(mx, smx[w][lane]);
+    float L = 0.f, r[8];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int e = 0; e < 8; ++e) r[e] = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float sc = smx[w][lane] == -INFINITY ? 0.f : ex2_approx(smx[w][lane] - mx);
+      L = fmaf(ssum[w][lane], sc, L);
+      const float4 x = sacc[w][lane][0], y = sacc[w][lane][1];
+      r[0] = fmaf(x.x, sc, r[0]);
+      r[1] = fmaf(x.y, sc, r[1]);
+      r[2] = fmaf(x.z, sc, r[2]);
+      r[3] = fmaf(x.w, sc, r[3]);
+      r[4] = fmaf(y.x, sc, r[4]);
+      r[5] = fmaf(y.y, sc, r[5]);
+      r[6] = fmaf(y.z, sc, r[6]);
+      r[7] = fmaf(y.w, sc, r[7]);
+    }
     if (!(L > 0.f)) {
-      if (lane == 0) set_status(a.status, DFLASH_DEV_NONFINITE);
+      if ((lane & 3) == 0) set_status(a.status, DFLASH_DEV_NONFINITE);
       L = 1.f;
     }
     const float inv = 1.f / L;
-    __syncwarp();
-    for (int c = lane; c < a.C; c += 32) sw[warp][c] *= inv;
-  }
-  __syncthreads();
-  // chunk group = warp; columns cb*64 + 2*lane, +1
-  const int col = cb * 64 + lane * 2;
-  float2 acc[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll 4
-  for (int c = warp; c < a.C; c += 8) {
-    const float* pc = a.part + (base + static_cast<size_t>(c) * M + hl * 8) * a.d + col;
-    float2 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __ldcg(reinterpret_cast<const float2*>(pc + static_cast<size_t>(i) * a.d));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float wgt = sw[i][c];
-      acc[i].x = fmaf(v[i].x, wgt, acc[i].x);
-      acc[i].y = fmaf(v[i].y, wgt, acc[i].y);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) sacc[warp][i][lane] = acc[i];
-  __syncthreads();
-  // warp i writes row i
-  {
-    const int i = warp;
-    float2 r = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      r.x += sacc[k][i][lane].x;
-      r.y += sacc[k][i][lane].y;
-    }
+    for (int e = 0; e < 8; ++e) r[e] *= inv;
     const int P = a.out_f16 ? 1 : 2;
     const size_t ob = xchunk_index(hq * a.d + col, s * 8 + i, 0, a.out_rows, a.out_ku, P);
     if (a.out_f16) {
-      *reinterpret_cast<uint32_t*>(static_cast<__half*>(a.out) + ob) = pack_f16x2(r.x, r.y);
+      *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + ob) =
+          make_uint4(pack_f16x2(r[0], r[1]), pack_f16x2(r[2], r[3]), pack_f16x2(r[4], r[5]), pack_f16x2(r[6], r[7]));
     } else {
-      uint32_t hi, lo;
-      split_bf16x2(r.x, r.y, hi, lo);
+      uint4 hi, lo;
+      split_bf16x2(r[0], r[1], hi.x, lo.x);
+      split_bf16x2(r[2], r[3], hi.y, lo.y);
+      split_bf16x2(r[4], r[5], hi.z, lo.z);
+      split_bf16x2(r[6], r[7], hi.w, lo.w);
       const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);
-      *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + ob) = hi;
-      *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + ob + lo_off) = lo;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + ob) = hi;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + ob + lo_off) = lo;
     }
+    if (threadIdx.x == 0) DFLASH_ATTN_STAMP(7);
   }
 }
 
 static cudaError_t launch_attn_impl(int D, const AttnArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  const int M = a.gq * 8;
-  cfg.blockDim = dim3((M / 16 + 1) * 32);
+  cfg.blockDim = dim3(kTcThreads);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
@@ -413,34 +644,26 @@ static cudaError_t launch_attn_impl(int D, const AttnArgs& a, dim3 grid, cudaStr
   cfg.numAttrs = 1;
   cfg.stream = st;
   switch (D) {
-    case 64: {
-      cfg.dynamicSmemBytes = AttnGeom<64>::smem(M);
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-      if (e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, attn_kernel<64>, a);
-    }
-    case 128: {
-      cfg.dynamicSmemBytes = AttnGeom<128>::smem(M);
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-      if (e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, attn_kernel<128>, a);
-    }
-    case 256: {
-      cfg.dynamicSmemBytes = AttnGeom<256>::smem(M);
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-      if (e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, attn_kernel<256>, a);
-    }
+#define DFLASH_ATTN_CASE(DD)                                                                                  \
+  case DD: {                                                                                                  \
+    cfg.dynamicSmemBytes = TcGeom<DD>::smem(a.gq * 8);                                                        \
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448); \
+    if (e != cudaSuccess) return e;                                                                           \
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<DD>, a);                                                   \
+  }
+    DFLASH_ATTN_CASE(64)
+    DFLASH_ATTN_CASE(128)
+    DFLASH_ATTN_CASE(256)
+#undef DFLASH_ATTN_CASE
   }
   return cudaErrorInvalidValue;
 }
 
-int attn_smem_bytes(int D, int gq) {
-  const int M = gq * 8;
+int attn_smem_bytes(int D, int M) {
   switch (D) {
-    case 64: return AttnGeom<64>::smem(M);
-    case 128: return AttnGeom<128>::smem(M);
-    case 256: return AttnGeom<256>::smem(M);
+    case 64: return TcGeom<64>::smem(M);
+    case 128: return TcGeom<128>::smem(M);
+    case 256: return TcGeom<256>::smem(M);
   }
   return 0;
 }
@@ -455,7 +678,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.vmap = st.v_map;
   a.anchor_pos = anchor_pos;
   a.block_len = block_len;
-  a.part = st.attn_part;
+  a.pmap = st.part_map;
   a.ml = st.attn_ml;
   a.out = st.attn_out;
   a.out_f16 = m.wtype != DFLASH_WT_BF16;
@@ -471,6 +694,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.n_seq = n_seq;
   a.status = status;
   a.qmap = st.q_map;
+  a.trace = trace_slot(st);
   cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.C, a.n_kv, n_seq), stream, true);
   if (e != cudaSuccess || a.C == 1) return e;
   if (st.prof_n > 0 && st.prof_k < st.prof_n)
@@ -488,8 +712,9 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cb.gq = a.gq;
   cb.C = a.C;
   cb.status = status;
+  cb.trace = trace_slot(st);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(c.n_q_heads, c.head_dim / 64, n_seq);
+  cfg.gridDim = dim3(c.n_q_heads, c.head_dim / 32, n_seq);
   cfg.blockDim = dim3(256);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

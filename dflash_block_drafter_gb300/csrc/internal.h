@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -83,7 +84,7 @@ struct State {
   void* attn_out = nullptr;    // [R, n_q d] activation type
   void* hbuf = nullptr;        // [R, I] activation type (SwiGLU output)
   void* xnorm = nullptr;       // [R, H] activation type (normed rows for streamed-X GEMVs)
-  float* attn_part = nullptr;  // [slots, n_kv, C, Gq*8, d]
+  __half* attn_part = nullptr;  // [slots, n_kv, C, Gq*8, d] chunk partials O / l
   float2* attn_ml = nullptr;   // [slots, n_kv, C, Gq*8] (max in log2 units, sum)
   float* partials = nullptr;   // GEMV split fix-up slots [max_grid, 2, 64, R_max]
   int* counters = nullptr;     // [CNT_REGIONS][counter_stride]
@@ -105,7 +106,8 @@ struct State {
   int trace_k = 0;
   void* head_ev_begin = nullptr;  // optional cudaEvent_t pair around the LM head
   void* head_ev_end = nullptr;
-  CUtensorMap q_map;  // q_ready as [slots*n_kv*M, d], 64 x M boxes, 128-byte swizzle
+  CUtensorMap q_map;     // q_ready as [slots*n_kv*M, d], 64 x M boxes, 128-byte swizzle
+  CUtensorMap part_map;  // attn_part as [slots*n_kv*C_max*M, d], 64 x M boxes, 128-byte swizzle
   CUtensorMap k_map;  // K arena as [L*slots*n_kv*cap, d], 64x64 boxes, 128-byte swizzle
   CUtensorMap v_map;
   size_t device_bytes = 0;

@@ -46,6 +46,9 @@ cudaError_t launch_kv_copy(bool write, __half* cells, int cap, int d, int n_kv, 
                            const uint16_t* in, cudaStream_t st);
 cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,
                              const int32_t* block_len, int32_t* status, cudaStream_t stream);
-int attn_smem_bytes(int D, int gq);
+// Dynamic shared memory of the attention kernel for head dim D and M query rows.
+int attn_smem_bytes(int D, int M);
+// Diagnostic builds: the next per-CTA timestamp slot of a launch (else null).
+unsigned long long* trace_slot(State& st);
 
 }  // namespace dflash

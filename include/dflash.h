@@ -154,7 +154,9 @@ const char* dflash_last_cuda_error(void);
 /* Host-only check of a configuration: DFLASH_OK if this build can run it.
  * Requirements: 1 <= n_layers <= DFLASH_MAX_LAYERS; head_dim in {64, 128,
  * 256}; n_q_heads % n_kv_heads == 0 and (n_q_heads / n_kv_heads) * 8 a
- * multiple of 16; hidden, n_q_heads*head_dim, intermediate multiples of 256;
+ * multiple of 16 and at most 128 (the attention's query rows per kv head
+ * fill one 128-row tensor-core tile; at most 112 when head_dim is 256, for
+ * shared memory); hidden, n_q_heads*head_dim, intermediate multiples of 256;
  * vocab >= 2; 0 <= mask_token_id < vocab; n_taps >= 1; rope_theta > 0;
  * norm_eps >= 0; a known weight_type.  No device is touched. */
 int dflash_config_check(const dflash_config* cfg);
