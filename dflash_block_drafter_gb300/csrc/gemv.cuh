@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         if constexpr (kStream) issue_x(it, u_begin + it);
         issued = it + 1;
       }
-      DFLASH_STAMP(2);
       // Every issued copy must land before the CTA may exit.
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
         if (!mbar_wait(&full[it % STAGES], (it / STAGES) & 1)) {
@@ -237,9 +236,8 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
 
   if constexpr (XMODE == X_RESIDENT) {
     // Stage the fp32 rows and the norm weight with bulk copies, compute
-    // 1 / RMS per row, then overwrite every fp32 value v = x * (1/RMS) * w in
-    // place with the 16-bit operand(s) the MMA needs: BF16 hi | lo << 16, or
-    // FP16 in the low half.  The consumer pairs neighbouring values with PRMT.
+    // 1 / RMS per row, then overwrite the fp32 values v = x * (1/RMS) * w in
+    // place with the 16-bit operand(s) the MMA needs (BF16 hi and lo, or FP16).
     float* wsm = reinterpret_cast<float*>(xres + R * xstride);
     if (tid == 0) {
       const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 4;
@@ -250,6 +248,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       bulk_g2s(wsm, a.norm_w, row_bytes, xbar);
     }
     if (!mbar_wait(xbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
+    if (tid == 0) DFLASH_STAMP(2);
     for (int r = w; r < R; r += 4) {
       const float4* xr = reinterpret_cast<const float4*>(xres + r * xstride);
       float ss = 0.f;
@@ -263,29 +262,35 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
     }
     named_bar_sync(1, 128);
-    const int k4 = a.K / 4;
-#pragma unroll 4
-    for (int i = tid; i < R * k4; i += 128) {
-      const int r = i / k4, kq = i - r * k4;
-      float4* xp = reinterpret_cast<float4*>(xres + r * xstride) + kq;
-      const float4 v = *xp;
-      const float4 wv = reinterpret_cast<const float4*>(wsm)[kq];
+    if (tid == 0) DFLASH_STAMP(6);
+    // Row by row, 128 threads across the row (independent iterations).  The
+    // packed operand of 8 consecutive inputs k..k+7 takes the start of their
+    // 32 fp32 bytes, in the order the MMA fragments use: FP16 pairs
+    // {k01, k23, k45, k67}, or BF16 {hi01, hi23, lo01, lo23} per 4 inputs.
+    const float4* wv4 = reinterpret_cast<const float4*>(wsm);
+    for (int r = 0; r < R; ++r) {
       const float sc = srs[r];
-      const float y[4] = {v.x * sc * wv.x, v.y * sc * wv.y, v.z * sc * wv.z, v.w * sc * wv.w};
-      uint4 o;
-      uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (kF16) {
-          op[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(y[e])));
-        } else {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(y[e]);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(y[e] - __bfloat162float(hi));
-          op[e] = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
-                  (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+      float4* xr = reinterpret_cast<float4*>(xres + r * xstride);
+      if constexpr (kF16) {
+#pragma unroll 3
+        for (int q = tid; q < a.K / 8; q += 128) {
+          const float4 v0 = xr[2 * q], v1 = xr[2 * q + 1];
+          const float4 w0 = wv4[2 * q], w1 = wv4[2 * q + 1];
+          *reinterpret_cast<uint4*>(xr + 2 * q) =
+              make_uint4(pack_f16x2(v0.x * sc * w0.x, v0.y * sc * w0.y), pack_f16x2(v0.z * sc * w0.z, v0.w * sc * w0.w),
+                         pack_f16x2(v1.x * sc * w1.x, v1.y * sc * w1.y), pack_f16x2(v1.z * sc * w1.z, v1.w * sc * w1.w));
+        }
+      } else {
+#pragma unroll 5
+        for (int kq = tid; kq < a.K / 4; kq += 128) {
+          const float4 v = xr[kq];
+          const float4 wv = wv4[kq];
+          uint4 o;
+          split_bf16x2(v.x * sc * wv.x, v.y * sc * wv.y, o.x, o.z);
+          split_bf16x2(v.z * sc * wv.z, v.w * sc * wv.w, o.y, o.w);
+          xr[kq] = *reinterpret_cast<const float4*>(&o);
         }
       }
-      *reinterpret_cast<uint4*>(xp) = o;
     }
   }
   epi.prologue(a, tid, XMODE == X_RESIDENT ? srs : nullptr);
@@ -325,15 +330,15 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       for (int t = 0; t < NT; ++t) {
         uint4 xf, xl;
         if constexpr (XMODE == X_RESIDENT) {
-          // 8 packed values of this lane's row: (hi | lo << 16) or FP16 in the low half
+          // this lane's 8 packed inputs of its row (layout of the prologue above)
           const uint8_t* xp = xres + (t * 8 + xrow) * xstride + xofs;
-          const uint4 p0 = *reinterpret_cast<const uint4*>(xp);
-          const uint4 p1 = *reinterpret_cast<const uint4*>(xp + 16);
-          xf.x = prmt(p0.x, p0.y, 0x5410); xf.y = prmt(p0.z, p0.w, 0x5410);
-          xf.z = prmt(p1.x, p1.y, 0x5410); xf.w = prmt(p1.z, p1.w, 0x5410);
           if constexpr (kSplit) {
-            xl.x = prmt(p0.x, p0.y, 0x7632); xl.y = prmt(p0.z, p0.w, 0x7632);
-            xl.z = prmt(p1.x, p1.y, 0x7632); xl.w = prmt(p1.z, p1.w, 0x7632);
+            const uint4 p0 = *reinterpret_cast<const uint4*>(xp);
+            const uint4 p1 = *reinterpret_cast<const uint4*>(xp + 16);
+            xf = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            xl = make_uint4(p0.z, p0.w, p1.z, p1.w);
+          } else {
+            xf = *reinterpret_cast<const uint4*>(xp);
           }
         } else {
           const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
+    if (XMODE != X_RESIDENT && tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
 
     if (j == a.UPG - 1 || u == u_end - 1) {
       if constexpr (kSplit && (WT == WT_BF16 || WT == WT_HEAD)) {
@@ -414,17 +419,37 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         if (sflag[0]) {
 #pragma unroll
           for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int cfg = static_cast<int>((static_cast<long long>(c) * a.U) / G) / a.UPG;
-            const int wc = (g == cfg) ? 0 : 1;
-            const float* sl = a.partials + (static_cast<size_t>(c) * 2 + wc) * 64 * R;
+          // the CTAs' partials in ascending order; FB of them are loaded at once
+          constexpr int FB = NT <= 2 ? 8 : (NT <= 4 ? 4 : 2);
+          for (int cb = c_first; cb <= c_last; cb += FB) {
+            float2 p0[FB][NT], p1[FB][NT];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              const int c0 = t * 8 + (lane & 3) * 2;
-              const float2 p0 = __ldcg(reinterpret_cast<const float2*>(sl + r0 * R + c0));
-              const float2 p1 = __ldcg(reinterpret_cast<const float2*>(sl + (r0 + 8) * R + c0));
-              acc[t][0] += p0.x; acc[t][1] += p0.y; acc[t][2] += p1.x; acc[t][3] += p1.y;
+            for (int q = 0; q < FB; ++q) {
+              const int c = cb + q;
+              if (c <= c_last) {
+                const int cfg = static_cast<int>((static_cast<long long>(c) * a.U) / G) / a.UPG;
+                const int wc = (g == cfg) ? 0 : 1;
+                const float* sl = a.partials + (static_cast<size_t>(c) * 2 + wc) * 64 * R;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                  const int c0 = t * 8 + (lane & 3) * 2;
+                  p0[q][t] = __ldcg(reinterpret_cast<const float2*>(sl + r0 * R + c0));
+                  p1[q][t] = __ldcg(reinterpret_cast<const float2*>(sl + (r0 + 8) * R + c0));
+                }
+              } else {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) p0[q][t] = p1[q][t] = make_float2(0.f, 0.f);
+              }
             }
+#pragma unroll
+            for (int q = 0; q < FB; ++q)
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                acc[t][0] += p0[q][t].x;
+                acc[t][1] += p0[q][t].y;
+                acc[t][2] += p1[q][t].x;
+                acc[t][3] += p1[q][t].y;
+              }
           }
           if (tid == 0) a.counters[g] = 0;
           epi.template group<WT, NT>(a, loc, g, w, lane, acc);
