@@ -249,6 +249,17 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool a_mn, b
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------- arrival counters
+// atomicAdd with acquire-release semantics at GPU scope.  Used by thread 0 of
+// a CTA after a CTA barrier: the release publishes every store the CTA made
+// before the barrier (cumulativity), the acquire makes the other CTAs'
+// published stores visible to the loads that follow the next CTA barrier.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ----------------------------------------------------------- named barriers
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

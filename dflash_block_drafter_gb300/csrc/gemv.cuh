@@ -404,16 +404,16 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
           __stcg(reinterpret_cast<float2*>(slot + (r0 + 8) * R + c0), make_float2(acc[t][2], acc[t][3]));
         }
         // the CTA's stores, ordered by the barrier, are released by thread 0's
-        // fence before its counter increment; the last arriver acquires them
+        // acquire-release counter increment; the last arriver acquires the others'
+        float pre[NT][4];
+        if constexpr (Epi::kPreload) epi.template preload<WT, NT>(g, w, lane, pre);
         named_bar_sync(1, 128);
         const long long ufirst = static_cast<long long>(g) * a.UPG;
         const int c_first = cta_of_unit(ufirst, G, a.U);
         const int c_last = cta_of_unit(ufirst + a.UPG - 1, G, a.U);
         if (tid == 0) {
-          __threadfence();
-          const int old = atomicAdd(&a.counters[g], 1);
+          const int old = atomic_add_acq_rel(&a.counters[g], 1);
           sflag[0] = (old == c_last - c_first);
-          __threadfence();
         }
         named_bar_sync(1, 128);
         if (sflag[0]) {
@@ -452,7 +452,10 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
               }
           }
           if (tid == 0) a.counters[g] = 0;
-          epi.template group<WT, NT>(a, loc, g, w, lane, acc);
+          if constexpr (Epi::kPreload)
+            epi.template group_pre<WT, NT>(g, w, lane, acc, pre);
+          else
+            epi.template group<WT, NT>(a, loc, g, w, lane, acc);
           if constexpr (Epi::kAfterGroup) {
             named_bar_sync(1, 128);
             epi.after_group(a, g, tid, sflag);

@@ -14,7 +14,7 @@ struct NoLocal {};
 
 // Y stored as fp32 [R, ldo] (activation row major).  Feature fusion: fc.
 struct EpiStore {
-  static constexpr bool kAfterGroup = false, kFinish = false;
+  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
   using Local = NoLocal;
   float* out;
   int ldo;
@@ -41,6 +41,9 @@ struct EpiStore {
 // projection.  Every element has exactly one owner thread.
 struct EpiResid {
   static constexpr bool kAfterGroup = false, kFinish = false;
+  // a split group's finisher loads its residual values before it knows it
+  // is the finisher, overlapping that load with the arrival counter
+  static constexpr bool kPreload = true;
   using Local = NoLocal;
   float* x;
   int ldx;
@@ -58,6 +61,30 @@ struct EpiResid {
       x[static_cast<size_t>(n + 1) * ldx + m1] += acc[t][3];
     }
   }
+  template <int WT, int NT>
+  __device__ void preload(int g, int w, int lane, float (&pre)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      pre[t][0] = __ldcg(x + static_cast<size_t>(n) * ldx + m0);
+      pre[t][1] = __ldcg(x + static_cast<size_t>(n + 1) * ldx + m0);
+      pre[t][2] = __ldcg(x + static_cast<size_t>(n) * ldx + m1);
+      pre[t][3] = __ldcg(x + static_cast<size_t>(n + 1) * ldx + m1);
+    }
+  }
+  template <int WT, int NT>
+  __device__ void group_pre(int g, int w, int lane, const float (&acc)[NT][4], const float (&pre)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      x[static_cast<size_t>(n) * ldx + m0] = pre[t][0] + acc[t][0];
+      x[static_cast<size_t>(n + 1) * ldx + m0] = pre[t][1] + acc[t][1];
+      x[static_cast<size_t>(n) * ldx + m1] = pre[t][2] + acc[t][2];
+      x[static_cast<size_t>(n + 1) * ldx + m1] = pre[t][3] + acc[t][3];
+    }
+  }
   __device__ void after_group(const GemvArgs&, int, int, int*) const {}
   template <int NT>
   __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
@@ -70,7 +97,7 @@ struct EpiResid {
 // hi and lo planes).
 template <bool kF16>
 struct EpiSwiglu {
-  static constexpr bool kAfterGroup = false, kFinish = false;
+  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
   using Local = NoLocal;
   void* h;
   __device__ void init(Local&) const {}
@@ -113,7 +140,7 @@ struct EpiSwiglu {
 //   mode 1 (fusion K/V): per layer l, n_kv key heads then n_kv value heads;
 //     activation row n is committed position positions[n].
 struct EpiHeads {
-  static constexpr bool kAfterGroup = true, kFinish = false;
+  static constexpr bool kAfterGroup = true, kFinish = false, kPreload = false;
   using Local = NoLocal;
   int mode;
   float* raw;       // [R, ldr]
@@ -155,10 +182,8 @@ struct EpiHeads {
     const int head = g / gph;
     if (gph > 1) {
       if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(&head_cnt[head], 1);
+        const int old = atomic_add_acq_rel(&head_cnt[head], 1);
         sflag[1] = (old == gph - 1);
-        __threadfence();
         if (sflag[1]) head_cnt[head] = 0;
       }
       named_bar_sync(1, 128);
@@ -260,7 +285,7 @@ struct EpiHeads {
 // the largest logit with ties going to the lowest id.
 template <int NT_>
 struct EpiArgmax {
-  static constexpr bool kAfterGroup = false, kFinish = true;
+  static constexpr bool kAfterGroup = false, kFinish = true, kPreload = false;
   struct Local {
     float v[NT_][2];
     int id[NT_][2];
@@ -350,10 +375,8 @@ struct EpiArgmax {
     }
     named_bar_sync(1, 128);
     if (tid == 0) {
-      __threadfence();
-      const int old = atomicAdd(grid_cnt, 1);
+      const int old = atomic_add_acq_rel(grid_cnt, 1);
       sflag[2] = (old == static_cast<int>(gridDim.x) - 1);
-      __threadfence();
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;

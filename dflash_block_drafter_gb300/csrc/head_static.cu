@@ -120,10 +120,8 @@ struct EpiArgmaxRows : public EpiArgmax<1> {
     }
     named_bar_sync(1, 128);
     if (tid == 0) {
-      __threadfence();
-      const int old = atomicAdd(grid_cnt, 1);
+      const int old = atomic_add_acq_rel(grid_cnt, 1);
       sflag[2] = (old == static_cast<int>(gridDim.x) - 1);
-      __threadfence();
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;
