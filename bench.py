@@ -41,6 +41,10 @@ METRIC = "draft passes/s and drafted tok/s at 8K ctx, block 8; HBM GB/s vs roofl
 UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
+# DRAM bytes (read + write) of one LM-head launch at this workload, from the
+# ncu capture summarised in profiles/lm_head_argmax_full_bf16.md (5.814 TB/s x
+# 134.37 us).  Reset to None whenever the head kernel changes.
+HEAD_TRAFFIC_BYTES = 781.2e6
 
 
 def load_peaks():
@@ -346,7 +350,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "algorithmic_bytes_per_step": ab["step"],
         "roofline": {"bound": "hbm", "kernel": "lm_head_argmax (gemv_kernel<WT_HEAD>)",
                      "achieved": head_gbs, "peak": peak, "unit": "GB/s", "frac": head_gbs / peak,
-                     "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": ab["head"],
+                     "peak_kind": peak_kind, "traffic": HEAD_TRAFFIC_BYTES, "bytes_per_launch": ab["head"],
                      "avg_launch_ms": head_avg_ms},
         "step_roofline": {"achieved": step_gbs, "peak": peak, "frac": step_gbs / peak, "unit": "GB/s"},
         "e2e": {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
