@@ -129,6 +129,28 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
+# replicas: timing reduction over ranks
+# --------------------------------------------------------------------------
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of this rank's timings over all ranks.  Every
+    rank runs an independent replica (sequences are independent and the
+    weights are replicated), so this timing reduction is the only collective;
+    none touches the data path."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_throughput(world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job cycles/s: every rank ran `steps` cycles; the job took the
+    slowest rank's time."""
+    return world * steps / (elapsed_ms / 1000.0)
+
+
+# --------------------------------------------------------------------------
 # CPU oracle baseline (also the reference arm)
 # --------------------------------------------------------------------------
 def oracle_baseline(ckpt, cfg, budget_s: float = 12.0, max_steps: int = 1000):
@@ -325,14 +347,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     d2h = 9 * 4
 
     # ---- gather over ranks (max time), replicas only
-    times = torch.tensor([elapsed_ms, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_s = float(times[0]), float(times[1])
+    elapsed_ms, e2e_s = max_over_ranks([elapsed_ms, e2e_s], device=dev)
     if rank != 0:
         return
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1000.0)
+    value = replica_throughput(world, args.steps, elapsed_ms)
     ab = algorithmic_bytes(cfg, ctx, B, FUSE_PER_STEP)
     peak, peak_kind = load_peaks()
     head_avg_ms = statistics.mean(head_ms)
@@ -353,7 +372,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                      "peak_kind": peak_kind, "traffic": HEAD_TRAFFIC_BYTES, "bytes_per_launch": ab["head"],
                      "avg_launch_ms": head_avg_ms},
         "step_roofline": {"achieved": step_gbs, "peak": peak, "frac": step_gbs / peak, "unit": "GB/s"},
-        "e2e": {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": replica_throughput(world, n_e2e, e2e_s * 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e},
         "gpu_launches": launches * args.steps,
         "launches_per_step": launches,
