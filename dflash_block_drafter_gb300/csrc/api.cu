@@ -168,7 +168,7 @@ void free_state(State* s) {
   if (!s) return;
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
-  f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
+  f(s->xpk); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
   f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->status);
 }
 
@@ -478,6 +478,8 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->attn_out, xchunk_elems(nq * d, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->hbuf, xchunk_elems(I, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->xnorm, xchunk_elems(H, R, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->xpk, size_t(8) * H * 4, &total));
+  STRY(dev_alloc(&s->ssq, size_t(H / 64) * 8 * 4, &total));
   STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 2, &total));
   STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks_max * M * 8, &total));
   s->max_grid = 2 * m->sm_count;
@@ -616,9 +618,23 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   const bool f16 = wt != WT_BF16;
 
   s->prof_k = 0;
+  // one-slot passes: every RMSNorm-fed GEMV reads the packed rows that the
+  // kernel producing x wrote (embed, o-proj and down residual epilogues)
+  const bool packed = resident_ok(nt, H);
+  auto set_packed = [&](GemvArgs& a) {
+    a.X = s->xpk;
+    a.ldx = H;
+    a.ssq = s->ssq;
+    a.n_ssq = H / 64;
+  };
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
-                 s->capacity, status};
+                 s->capacity, status, nullptr, nullptr, nullptr};
+    if (packed) {
+      ea.xpk = s->xpk;
+      ea.ssq = s->ssq;
+      ea.w_next = m->attn_norm;
+    }
     prof_mark(s, stream);
     TRY(check_gemv(launch_embed(ea, nt, stream), "embed"));
   }
@@ -628,10 +644,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       GemvArgs a = base_args(m->qkv[l], *s, CNT_QKV, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
-      if (resident_ok(nt, H)) {
-        a.X = s->x;
-        a.ldx = H;
-        a.norm_w = m->attn_norm + size_t(l) * H;
+      if (packed) {
+        set_packed(a);
       } else {
         NormArgs na{s->x, m->attn_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
                     ku_of(wt)};
@@ -678,7 +692,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->attn_out;
       a.ldx = nq * d;
-      EpiResid e{s->x, H};
+      EpiResid e{s->x, H, packed ? s->xpk : nullptr, s->ssq, m->mlp_norm + size_t(l) * H};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
@@ -687,10 +701,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
-      if (resident_ok(nt, H)) {
-        a.X = s->x;
-        a.ldx = H;
-        a.norm_w = m->mlp_norm + size_t(l) * H;
+      if (packed) {
+        set_packed(a);
       } else {
         NormArgs na{s->x, m->mlp_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
                     ku_of(wt)};
@@ -709,7 +721,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->hbuf;
       a.ldx = I;
-      EpiResid e{s->x, H};
+      EpiResid e{s->x, H, packed ? s->xpk : nullptr, s->ssq,
+                 l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
@@ -742,10 +755,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.x = s->x;
     p.norm_w = m->final_norm;
     p.status = status;
-    if (resident_ok(nt, H)) {
-      a.X = s->x;
-      a.ldx = H;
-      a.norm_w = m->final_norm;
+    if (packed) {
+      set_packed(a);
     } else {
       NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8,
                   32 * Fmt<WT_HEAD>::CB};

@@ -37,6 +37,11 @@ struct GemvArgs {
   int ldx;
   const float* norm_w;
   float eps;
+  // X_PACKED: X holds rows of packed x * w (uint32 per input, MMA operand
+  // order) and ssq[g * 8 + r] the sum of x^2 over inputs [64 g, 64 g + 64)
+  // of row r, g < n_ssq
+  const float* ssq;
+  int n_ssq;
   float* partials;               // [gridDim.x, 2, 64, R]
   int* counters;                 // [N / 64]
   int32_t* status;
@@ -63,7 +68,9 @@ struct GemvGeom {
   static constexpr int XS_STRIDE = XSE * 2;             // ... in bytes
   static constexpr bool kStream = XMODE == X_STREAM || XMODE == X_STREAM_BF16;
   // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
-  static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16;
+  static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16 && XMODE != X_PACKED;
+  // activations staged whole in shared memory (fp32 rows, or already packed)
+  static constexpr bool kRes = XMODE == X_RESIDENT || XMODE == X_PACKED;
   // BF16 activations computed in fp32 are carried as two BF16 planes, hi and
   // lo = x - hi (about 16 significant bits), each multiplied on the tensor
   // cores; the caller's BF16 taps (X_STREAM_BF16) are exact and need no lo.
@@ -75,9 +82,10 @@ struct GemvGeom {
   static constexpr int kResK = 2560;
   static __host__ __device__ constexpr int xres_stride(int K) { return K * 4 + 16; }
   static __host__ __device__ constexpr int xres_bytes(int K) {
-    return (XMODE == X_RESIDENT) ? ((R * xres_stride(K) + K * 4 + 127) / 128) * 128 : 0;
+    return (XMODE == X_RESIDENT || XMODE == X_PACKED) ? ((R * xres_stride(K) + K * 4 + 127) / 128) * 128 : 0;
   }
-  static constexpr int RING_BUDGET = (XMODE == X_RESIDENT) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
+  static constexpr int RING_BUDGET =
+      (XMODE == X_RESIDENT || XMODE == X_PACKED) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.U) / G);
   const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
   const int n_units = u_end - u_begin;
-  const int xstride = (XMODE == X_RESIDENT) ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
+  const int xstride = Geo::kRes ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       }
     }
   }
-  if constexpr (XMODE == X_RESIDENT) {
+  if constexpr (Geo::kRes) {
     for (int i = tid; i < (R - a.n_valid_rows) * (a.K / 4); i += Geo::THREADS) {
       const int rr = a.n_valid_rows + i / (a.K / 4);
       reinterpret_cast<float4*>(xres + rr * xstride)[i % (a.K / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -293,7 +301,27 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       }
     }
   }
-  epi.prologue(a, tid, XMODE == X_RESIDENT ? srs : nullptr);
+  if constexpr (XMODE == X_PACKED) {
+    // Copy the packed rows in; meanwhile 1 / RMS per row from the producing
+    // kernel's partial sums of squares (fixed summation order).
+    if (tid == 0) {
+      const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 4;
+      mbar_arrive_expect_tx(xbar, a.n_valid_rows * row_bytes);
+      const uint8_t* x = static_cast<const uint8_t*>(a.X);
+      for (int r = 0; r < a.n_valid_rows; ++r)
+        bulk_g2s(xres + r * xstride, x + static_cast<size_t>(r) * a.ldx * 4, row_bytes, xbar);
+    }
+    for (int r = w; r < R; r += 4) {
+      float ss = 0.f;
+      for (int g = lane; g < a.n_ssq; g += 32) ss += __ldcg(a.ssq + g * 8 + r);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
+    }
+    if (!mbar_wait(xbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
+    named_bar_sync(1, 128);
+  }
+  epi.prologue(a, tid, Geo::kRes ? srs : nullptr);
   named_bar_sync(1, 128);
   if (tid == 0) DFLASH_STAMP(4);
 
@@ -309,27 +337,28 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int xrow = lane >> 2;
   bool ok = true;
 
-  for (int it = 0; it < n_units && ok; ++it) {
+  // After a timeout the loop keeps running (without waiting) so every warp
+  // takes the same named barriers; the outputs are then unspecified.
+  for (int it = 0; it < n_units; ++it) {
     const int u = u_begin + it;
     const int s = it % STAGES;
-    if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
+    const int g = u / a.UPG, j = u - g * a.UPG;
+    if (ok && !mbar_wait(&full[s], (it / STAGES) & 1)) {
       set_status(a.status, DFLASH_DEV_TIMEOUT);
       ok = false;
-      break;
     }
     if (tid == 0 && it == 0) DFLASH_STAMP(5);
-    const int g = u / a.UPG, j = u - g * a.UPG;
     const uint32_t ubase = ring_s + s * Geo::STAGE;
 
 #pragma unroll
     for (int bl = 0; bl < F::CB; ++bl) {
       const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
       uint32_t xofs = 0;
-      if constexpr (XMODE == X_RESIDENT) xofs = ((j * F::CB + bl) * 32 + (lane & 3) * 8) * 4;
+      if constexpr (Geo::kRes) xofs = ((j * F::CB + bl) * 32 + (lane & 3) * 8) * 4;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         uint4 xf, xl;
-        if constexpr (XMODE == X_RESIDENT) {
+        if constexpr (Geo::kRes) {
           // this lane's 8 packed inputs of its row (layout of the prologue above)
           const uint8_t* xp = xres + (t * 8 + xrow) * xstride + xofs;
           if constexpr (kSplit) {
@@ -374,7 +403,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (XMODE != X_RESIDENT && tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
+    if (!Geo::kRes && tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
 
     if (j == a.UPG - 1 || u == u_end - 1) {
       if constexpr (kSplit && (WT == WT_BF16 || WT == WT_HEAD)) {
@@ -384,6 +413,17 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
             acc[t][e] += acc2[t][e];
             acc2[t][e] = 0.f;
           }
+      }
+      if constexpr (XMODE == X_PACKED) {
+        // the rows were multiplied unnormalised: scale each output by 1 / RMS of its row
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int n = t * 8 + (lane & 3) * 2;
+          acc[t][0] *= srs[n];
+          acc[t][1] *= srs[n + 1];
+          acc[t][2] *= srs[n];
+          acc[t][3] *= srs[n + 1];
+        }
       }
       const bool complete = (g * a.UPG >= u_begin) && (j == a.UPG - 1);
       if (complete) {

@@ -47,19 +47,68 @@ struct EpiResid {
   using Local = NoLocal;
   float* x;
   int ldx;
+  // Optional (8-row passes): the next RMSNorm-fed GEMV's packed operand.
+  // For each finished 64-column group g: xpk[n * ldx + m] = BF16 hi/lo of
+  // x_new[n][m] * w_next[m] in the MMA operand order (per 4 columns {hi01,
+  // hi23, lo01, lo23}), and ssq[g * 8 + n] = sum of x_new[n][m]^2 over the
+  // group.  Null xpk: none.
+  uint32_t* xpk;
+  float* ssq;
+  const float* w_next;
+
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+
+  template <int WT, int NT>
+  __device__ void pack_next(int g, int w, int lane, const float (&v)[NT][4]) const {
+    if constexpr (NT == 1) {
+      if (xpk == nullptr) return;
+      __shared__ __align__(16) float tile[8][64 + 4];
+      const int r0 = frag_row<WT>(w, lane >> 2), r1 = frag_row<WT>(w, (lane >> 2) + 8);
+      const int n = (lane & 3) * 2;
+      tile[n][r0] = v[0][0];
+      tile[n + 1][r0] = v[0][1];
+      tile[n][r1] = v[0][2];
+      tile[n + 1][r1] = v[0][3];
+      named_bar_sync(1, 128);
+      // thread (row = tid / 16, q = tid % 16): columns 4q .. 4q + 3 of the group
+      const int tid = w * 32 + lane, row = tid >> 4, q = tid & 15;
+      const float4 xv = *reinterpret_cast<const float4*>(&tile[row][4 * q]);
+      const int m = g * 64 + 4 * q;
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(w_next + m));
+      uint4 o;
+      split_bf16x2(xv.x * wv.x, xv.y * wv.y, o.x, o.z);
+      split_bf16x2(xv.z * wv.z, xv.w * wv.w, o.y, o.w);
+      *reinterpret_cast<uint4*>(xpk + static_cast<size_t>(row) * ldx + m) = o;
+      float ss = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+#pragma unroll
+      for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (q == 0) ssq[g * 8 + row] = ss;
+      named_bar_sync(1, 128);  // the tile is reused by the next group
+    }
+  }
+
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+    float v[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int n = t * 8 + (lane & 3) * 2;
-      x[static_cast<size_t>(n) * ldx + m0] += acc[t][0];
-      x[static_cast<size_t>(n + 1) * ldx + m0] += acc[t][1];
-      x[static_cast<size_t>(n) * ldx + m1] += acc[t][2];
-      x[static_cast<size_t>(n + 1) * ldx + m1] += acc[t][3];
+      float* p00 = x + static_cast<size_t>(n) * ldx + m0;
+      float* p10 = x + static_cast<size_t>(n + 1) * ldx + m0;
+      float* p01 = x + static_cast<size_t>(n) * ldx + m1;
+      float* p11 = x + static_cast<size_t>(n + 1) * ldx + m1;
+      v[t][0] = *p00 + acc[t][0];
+      v[t][1] = *p10 + acc[t][1];
+      v[t][2] = *p01 + acc[t][2];
+      v[t][3] = *p11 + acc[t][3];
+      *p00 = v[t][0];
+      *p10 = v[t][1];
+      *p01 = v[t][2];
+      *p11 = v[t][3];
     }
+    pack_next<WT, NT>(g, w, lane, v);
   }
   template <int WT, int NT>
   __device__ void preload(int g, int w, int lane, float (&pre)[NT][4]) const {
@@ -76,14 +125,18 @@ struct EpiResid {
   template <int WT, int NT>
   __device__ void group_pre(int g, int w, int lane, const float (&acc)[NT][4], const float (&pre)[NT][4]) const {
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+    float v[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int n = t * 8 + (lane & 3) * 2;
-      x[static_cast<size_t>(n) * ldx + m0] = pre[t][0] + acc[t][0];
-      x[static_cast<size_t>(n + 1) * ldx + m0] = pre[t][1] + acc[t][1];
-      x[static_cast<size_t>(n) * ldx + m1] = pre[t][2] + acc[t][2];
-      x[static_cast<size_t>(n + 1) * ldx + m1] = pre[t][3] + acc[t][3];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[t][e] = pre[t][e] + acc[t][e];
+      x[static_cast<size_t>(n) * ldx + m0] = v[t][0];
+      x[static_cast<size_t>(n + 1) * ldx + m0] = v[t][1];
+      x[static_cast<size_t>(n) * ldx + m1] = v[t][2];
+      x[static_cast<size_t>(n + 1) * ldx + m1] = v[t][3];
     }
+    pack_next<WT, NT>(g, w, lane, v);
   }
   __device__ void after_group(const GemvArgs&, int, int, int*) const {}
   template <int NT>

@@ -32,27 +32,41 @@ inline int gemv_smem(int K) {
   return GemvGeom<WT, NT, XMODE>::smem_bytes(K);
 }
 
-// Raise the dynamic shared-memory cap once per (kernel instantiation, device).
+// Raise the dynamic shared-memory cap once per (kernel instantiation, device)
+// to what the per-CTA limit leaves beside the kernel's static shared memory;
+// returns that cap in *cap.
 template <int WT, int NT, int XMODE, class Epi>
-inline cudaError_t ensure_smem_attr() {
+inline cudaError_t ensure_smem_attr(int* cap) {
   static unsigned set_mask = 0;
+  static int dyn_cap = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned bit = 1u << (dev & 31);
-  if (__atomic_load_n(&set_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(gemv_kernel<WT, NT, XMODE, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-  if (e == cudaSuccess) __atomic_fetch_or(&set_mask, bit, __ATOMIC_RELEASE);
-  return e;
+  if (__atomic_load_n(&set_mask, __ATOMIC_ACQUIRE) & bit) {
+    *cap = __atomic_load_n(&dyn_cap, __ATOMIC_ACQUIRE);
+    return cudaSuccess;
+  }
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, gemv_kernel<WT, NT, XMODE, Epi>);
+  if (e != cudaSuccess) return e;
+  const int c = kMaxDynSmem - static_cast<int>(fa.sharedSizeBytes);
+  e = cudaFuncSetAttribute(gemv_kernel<WT, NT, XMODE, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, c);
+  if (e != cudaSuccess) return e;
+  __atomic_store_n(&dyn_cap, c, __ATOMIC_RELEASE);
+  __atomic_fetch_or(&set_mask, bit, __ATOMIC_RELEASE);
+  *cap = c;
+  return cudaSuccess;
 }
 
 template <int WT, int NT, int XMODE, class Epi>
 inline cudaError_t launch_gemv(const GemvArgs& a, const Epi& epi, const LaunchCfg& lc) {
   auto kern = gemv_kernel<WT, NT, XMODE, Epi>;
-  cudaError_t e = ensure_smem_attr<WT, NT, XMODE, Epi>();
+  int cap = 0;
+  cudaError_t e = ensure_smem_attr<WT, NT, XMODE, Epi>(&cap);
   if (e != cudaSuccess) return e;
   const int smem = GemvGeom<WT, NT, XMODE>::smem_bytes(a.K);
-  if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
+  if (smem > cap) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(lc.grid);
   cfg.blockDim = dim3(GemvGeom<WT, NT, XMODE>::THREADS);
@@ -92,24 +106,27 @@ cudaError_t gemv_resid(int nt, const GemvArgs& a, const EpiResid& e, const Launc
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
-// The RMSNorm-fed GEMVs (q/k/v, gate/up, LM head, fusion K/V) read X
-// resident (fp32 rows staged, normalised in the consumer) for one n-tile when
-// the hidden size fits its shared memory, else streamed from a separate
-// RMSNorm kernel's chunked output.
+// The RMSNorm-fed GEMVs read X whole into shared memory for one n-tile when
+// the hidden size fits: in the draft pass (q/k/v, gate/up, LM head) as the
+// packed rows the previous kernel wrote (X_PACKED); in the fusion (K/V) as
+// fp32 rows normalised in the prologue (X_RESIDENT).  Otherwise X is streamed
+// from a separate RMSNorm kernel's chunked output.
 inline bool resident_ok(int nt, int K) { return nt == 1 && K <= 2560; }
 
 // SwiGLU gate/up.
 template <int WT>
 cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, const LaunchCfg& lc) {
+  // h is written in the format the down projection streams (FP16 for quantised weights)
   const EpiSwiglu<Fmt<WT>::kF16> e{h};
-  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_PACKED>(a, e, lc);
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
 // Per-head epilogue (draft QKV / fusion K/V).
 template <int WT>
 cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
-  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+  if (resident_ok(nt, a.K))
+    return e.mode == 0 ? launch_gemv<WT, 1, X_PACKED>(a, e, lc) : launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
   if (e.mode == 1) {
     switch (nt) {
       case 1: return launch_gemv<WT, 1, X_STREAM>(a, e, lc);
@@ -126,7 +143,7 @@ inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParam
       nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.grid_cnt, p.final_hidden, p.x,
                           p.norm_w, p.H, p.status};
       if constexpr (NT == 1) {
-        if (resident_ok(nt, a.K)) return launch_gemv<WT_HEAD, NT, X_RESIDENT>(a, e, lc);
+        if (resident_ok(nt, a.K)) return launch_gemv<WT_HEAD, NT, X_PACKED>(a, e, lc);
       } return launch_gemv<WT_HEAD, NT, X_STREAM>(a, e, lc);)
 }
 

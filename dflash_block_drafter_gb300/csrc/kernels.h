@@ -18,6 +18,11 @@ struct EmbedArgs {
   float* x;
   int H, vocab, mask_id, n_seq, cap;
   int32_t* status;
+  // optional (one slot): the first QKV GEMV's packed operand, as EpiResid
+  // writes it (BF16 hi/lo of x * w_next, per-64-column sums of squares)
+  uint32_t* xpk;
+  float* ssq;
+  const float* w_next;
 };
 
 // out = RMSNorm(x) * w in the chunked streamed-X layout (layout.cuh) of a

@@ -208,7 +208,32 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
     }
   }
   const uint16_t* er = a.embed + static_cast<size_t>(tok) * a.H;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) xr[k] = bf16_bits_to_float(er[k]);
+  if (a.xpk == nullptr) {
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) xr[k] = bf16_bits_to_float(er[k]);
+    return;
+  }
+  // 4 columns per thread: the fp32 row, its packed x * w_next and the sum of
+  // squares of each 64-column group (16 consecutive lanes, fixed order)
+  const int n = s * 8 + i;
+  for (int c0 = 0; c0 < a.H / 4; c0 += blockDim.x) {
+    const int c = c0 + threadIdx.x;
+    float ss = 0.f;
+    if (c < a.H / 4) {
+      const uint2 e = *reinterpret_cast<const uint2*>(er + 4 * c);
+      const float4 v = make_float4(__uint_as_float(e.x << 16), __uint_as_float(e.x & 0xffff0000u),
+                                   __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xffff0000u));
+      reinterpret_cast<float4*>(xr)[c] = v;
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w_next) + c);
+      uint4 o;
+      split_bf16x2(v.x * wv.x, v.y * wv.y, o.x, o.z);
+      split_bf16x2(v.z * wv.z, v.w * wv.w, o.y, o.w);
+      reinterpret_cast<uint4*>(a.xpk + static_cast<size_t>(n) * a.H)[c] = o;
+      ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 15) == 0 && c < a.H / 4) a.ssq[(c / 16) * 8 + n] = ss;
+  }
 }
 
 cudaError_t launch_embed(const EmbedArgs& a, int nt, cudaStream_t st) {
