@@ -9,6 +9,10 @@ vocab 151936) with an 8192-position context and an 8-row block:
 All of it runs in libdflash's CUDA kernels through the C ABI.  The anchor
 position stays at p = 8192 so every step does identical work.
 
+The cycle is captured once in a CUDA graph (the C ABI reads positions, block
+lengths and ids from device memory, so a captured cycle stays valid) and the
+timed region replays it.
+
 Printed (rank 0): one JSON line with the metric, device-timed passes/s, the
 end-to-end number through the C ABI with host buffers, the dominant kernel's
 roofline, the CPU oracle timed on the host cores as a baseline, SM clocks
@@ -272,13 +276,24 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if status:
         raise RuntimeError(f"device status {status} during warm-up")
 
-    # ---- device-timed region: K steps, head kernel timed with events inside
-    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    # ---- the cycle as a CUDA graph: G cycles per graph, each with its own
+    # pair of events around the LM-head launch (event-record nodes), so the
+    # head's duration is read from the last replay inside the timed region
+    G = 10 if args.steps % 10 == 0 else 1
+    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
     with torch.cuda.stream(stream):
         for a, b in head_ev:  # CUDA events are created lazily on first record
             a.record(stream)
             b.record(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            D.dflash_state_set_head_events(st.handle, head_ev[i][0].cuda_event, head_ev[i][1].cuda_event)
+            step()
+    D.dflash_state_set_head_events(st.handle, 0, 0)
+    with torch.cuda.stream(stream):
+        graph.replay()
     stream.synchronize()
     t_beg = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -289,13 +304,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         time.sleep(0.15)
         with torch.cuda.stream(stream):
             t_beg.record(stream)
-            for i in range(args.steps):
-                D.dflash_state_set_head_events(st.handle, head_ev[i][0].cuda_event, head_ev[i][1].cuda_event)
-                step()
+            for _ in range(args.steps // G):
+                graph.replay()
             t_end.record(stream)
         torch.cuda.synchronize(dev)
         time.sleep(0.15)
-    D.dflash_state_set_head_events(st.handle, 0, 0)
     if world > 1:
         dist.barrier()
     elapsed_ms = t_beg.elapsed_time(t_end)
@@ -304,16 +317,23 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if status:
         raise RuntimeError(f"device status {status} during the timed region")
 
-    # ---- draft-only device timing (context for the reader)
+    # ---- draft-only device timing (context for the reader), also as a graph
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph, stream=stream):
+        st.draft(1, want_hidden=False, stream=stream)
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_draft = max(20, args.steps // 4)
+        dgraph.replay()
         e0.record(stream)
         for _ in range(n_draft):
-            st.draft(1, want_hidden=False, stream=stream)
+            dgraph.replay()
         e1.record(stream)
     torch.cuda.synchronize(dev)
     draft_only_ms = e0.elapsed_time(e1) / n_draft
+    one = torch.cuda.CUDAGraph()  # one cycle, for the end-to-end loop
+    with torch.cuda.graph(one, stream=stream):
+        step()
 
     # ---- end to end through the C ABI with host buffers
     h_taps = torch.empty_like(fuse_taps, device="cpu").pin_memory()
@@ -337,7 +357,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             st.anchor_pos[:1].copy_(d_scalars[1:2])
             st.block_len[:1].copy_(d_scalars[2:3])
             tgt.copy_(h_tgt, non_blocking=True)
-            step()
+            one.replay()
             h_out[:7].copy_(st.drafts[0], non_blocking=True)
             h_out[7:8].copy_(acc_len, non_blocking=True)
             h_out[8:9].copy_(next_anchor, non_blocking=True)
@@ -375,6 +395,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "e2e": {"value": replica_throughput(world, n_e2e, e2e_s * 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e},
         "gpu_launches": launches * args.steps,
+        "cuda_graph": f"{G} cycles per graph, replayed {args.steps // G} times",
         "launches_per_step": launches,
         "clocks": clocks.summary(),
         "setup_s": setup_s,

@@ -244,7 +244,8 @@ cudaError_t gemv_heads_any(int wt, int nt, const GemvArgs& a, const EpiHeads& e,
 
 // Record the next profiling event on `stream` (no-op unless profiling is on).
 void prof_mark(State* s, cudaStream_t stream) {
-  if (s->prof_n > 0 && s->prof_k < s->prof_n) cudaEventRecord(static_cast<cudaEvent_t>(s->prof_events[s->prof_k++]), stream);
+  if (s->prof_n > 0 && s->prof_k < s->prof_n)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->prof_events[s->prof_k++]), stream, cudaEventRecordExternal);
 }
 
 bool is_dev_ptr(const void* p) {
@@ -767,10 +768,10 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       p.final_hidden = nullptr;
     }
     LaunchCfg lc{stream, grid_for(*m, a), true};
-    if (s->head_ev_begin) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_begin), stream));
+    if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
     prof_mark(s, stream);
     TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
-    if (s->head_ev_end) CK(cudaEventRecord(static_cast<cudaEvent_t>(s->head_ev_end), stream));
+    if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
   }
   prof_mark(s, stream);
   return DFLASH_OK;

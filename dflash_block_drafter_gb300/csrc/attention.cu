@@ -698,7 +698,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.C, a.n_kv, n_seq), stream, true);
   if (e != cudaSuccess || a.C == 1) return e;
   if (st.prof_n > 0 && st.prof_k < st.prof_n)
-    cudaEventRecord(static_cast<cudaEvent_t>(st.prof_events[st.prof_k++]), stream);
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(st.prof_events[st.prof_k++]), stream, cudaEventRecordExternal);
   CombineArgs cb;
   cb.part = st.attn_part;
   cb.ml = st.attn_ml;

@@ -273,7 +273,8 @@ int32_t dflash_fuse_launches(const dflash_state* state, int32_t n);
  * caller), every following dflash_draft_block on this state records
  * ev_begin on its stream immediately before the LM-head kernel and ev_end
  * right after it, so the dominant kernel can be timed inside a running
- * pass.  NULL, NULL switches it off. */
+ * pass; during stream capture the records become event-record nodes of the
+ * graph, so every replay records them.  NULL, NULL switches it off. */
 int dflash_state_set_head_events(dflash_state* state, void* ev_begin, void* ev_end);
 
 /* Profiling aid: with n_events > 0, every following dflash_fuse_context and
