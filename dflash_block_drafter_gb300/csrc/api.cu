@@ -549,7 +549,9 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       a.n_valid_rows = rows;
       a.X = taps + static_cast<size_t>(base) * tw;
       a.ldx = tw;
-      EpiStore e{s->h_raw, H};
+      // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
+      const bool fpacked = resident_ok(nt, H);
+      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xpk : nullptr, s->ssq, m->hidden_norm, H}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
@@ -560,9 +562,10 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       a.n_valid_rows = rows;
       a.eps = c.norm_eps;
       if (resident_ok(nt, H)) {
-        a.X = s->h_raw;
+        a.X = s->xpk;
         a.ldx = H;
-        a.norm_w = m->hidden_norm;
+        a.ssq = s->ssq;
+        a.n_ssq = H / 64;
       } else {
         NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0,
                     ku_of(wt)};
@@ -693,7 +696,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->attn_out;
       a.ldx = nq * d;
-      EpiResid e{s->x, H, packed ? s->xpk : nullptr, s->ssq, m->mlp_norm + size_t(l) * H};
+      EpiResid e{s->x, H, PackNext{packed ? s->xpk : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, H}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
@@ -722,8 +725,9 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->hbuf;
       a.ldx = I;
-      EpiResid e{s->x, H, packed ? s->xpk : nullptr, s->ssq,
-                 l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm};
+      EpiResid e{s->x, H,
+                 PackNext{packed ? s->xpk : nullptr, s->ssq,
+                          l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm, H}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));

@@ -29,13 +29,10 @@ struct GemvArgs {
   int UPG;                       // units per 64-row group
   int U;                         // total units
   int n_valid_rows;              // activation rows that exist (others read as zero)
-  // X_RESIDENT: fp32 rows X[r * ldx + k] and the RMSNorm weight norm_w[K]
-  //             (fp32); staged by bulk copies, normalised in the consumer
   // X_STREAM: activations in the chunked layout (layout.cuh), R = 8 * NT rows
   // X_STREAM_BF16: BF16 rows X[r * ldx + k] (the caller's taps)
   const void* X;
   int ldx;
-  const float* norm_w;
   float eps;
   // X_PACKED: X holds rows of packed x * w (uint32 per input, MMA operand
   // order) and ssq[g * 8 + r] the sum of x^2 over inputs [64 g, 64 g + 64)
@@ -70,7 +67,7 @@ struct GemvGeom {
   // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
   static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16 && XMODE != X_PACKED;
   // activations staged whole in shared memory (fp32 rows, or already packed)
-  static constexpr bool kRes = XMODE == X_RESIDENT || XMODE == X_PACKED;
+  static constexpr bool kRes = XMODE == X_PACKED;
   // BF16 activations computed in fp32 are carried as two BF16 planes, hi and
   // lo = x - hi (about 16 significant bits), each multiplied on the tensor
   // cores; the caller's BF16 taps (X_STREAM_BF16) are exact and need no lo.
@@ -78,14 +75,14 @@ struct GemvGeom {
   static constexpr int XPLANES = kSplit ? 2 : 1;
   static constexpr int XS_BYTES = kStream ? XPLANES * R * XS_STRIDE : 0;
   static constexpr int STAGE = ((F::UNIT + XS_BYTES + 1023) / 1024) * 1024;
-  // Resident X holds fp32 rows plus the norm weight; sized for K up to kResK.
+  // Packed X (X_PACKED): R rows of K packed inputs (4 bytes each); sized for K up to kResK.
   static constexpr int kResK = 2560;
   static __host__ __device__ constexpr int xres_stride(int K) { return K * 4 + 16; }
   static __host__ __device__ constexpr int xres_bytes(int K) {
-    return (XMODE == X_RESIDENT || XMODE == X_PACKED) ? ((R * xres_stride(K) + K * 4 + 127) / 128) * 128 : 0;
+    return (XMODE == X_PACKED) ? ((R * xres_stride(K) + 127) / 128) * 128 : 0;
   }
   static constexpr int RING_BUDGET =
-      (XMODE == X_RESIDENT || XMODE == X_PACKED) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
+      (XMODE == X_PACKED) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
@@ -242,65 +239,6 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int w = warp;
   if (tid == 0) DFLASH_STAMP(3);
 
-  if constexpr (XMODE == X_RESIDENT) {
-    // Stage the fp32 rows and the norm weight with bulk copies, compute
-    // 1 / RMS per row, then overwrite the fp32 values v = x * (1/RMS) * w in
-    // place with the 16-bit operand(s) the MMA needs (BF16 hi and lo, or FP16).
-    float* wsm = reinterpret_cast<float*>(xres + R * xstride);
-    if (tid == 0) {
-      const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 4;
-      mbar_arrive_expect_tx(xbar, (a.n_valid_rows + 1) * row_bytes);
-      const float* x = static_cast<const float*>(a.X);
-      for (int r = 0; r < a.n_valid_rows; ++r)
-        bulk_g2s(xres + r * xstride, x + static_cast<size_t>(r) * a.ldx, row_bytes, xbar);
-      bulk_g2s(wsm, a.norm_w, row_bytes, xbar);
-    }
-    if (!mbar_wait(xbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
-    if (tid == 0) DFLASH_STAMP(2);
-    for (int r = w; r < R; r += 4) {
-      const float4* xr = reinterpret_cast<const float4*>(xres + r * xstride);
-      float ss = 0.f;
-#pragma unroll 4
-      for (int i = lane; i < a.K / 4; i += 32) {
-        const float4 v = xr[i];
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
-    }
-    named_bar_sync(1, 128);
-    if (tid == 0) DFLASH_STAMP(6);
-    // Row by row, 128 threads across the row (independent iterations).  The
-    // packed operand of 8 consecutive inputs k..k+7 takes the start of their
-    // 32 fp32 bytes, in the order the MMA fragments use: FP16 pairs
-    // {k01, k23, k45, k67}, or BF16 {hi01, hi23, lo01, lo23} per 4 inputs.
-    const float4* wv4 = reinterpret_cast<const float4*>(wsm);
-    for (int r = 0; r < R; ++r) {
-      const float sc = srs[r];
-      float4* xr = reinterpret_cast<float4*>(xres + r * xstride);
-      if constexpr (kF16) {
-#pragma unroll 3
-        for (int q = tid; q < a.K / 8; q += 128) {
-          const float4 v0 = xr[2 * q], v1 = xr[2 * q + 1];
-          const float4 w0 = wv4[2 * q], w1 = wv4[2 * q + 1];
-          *reinterpret_cast<uint4*>(xr + 2 * q) =
-              make_uint4(pack_f16x2(v0.x * sc * w0.x, v0.y * sc * w0.y), pack_f16x2(v0.z * sc * w0.z, v0.w * sc * w0.w),
-                         pack_f16x2(v1.x * sc * w1.x, v1.y * sc * w1.y), pack_f16x2(v1.z * sc * w1.z, v1.w * sc * w1.w));
-        }
-      } else {
-#pragma unroll 5
-        for (int kq = tid; kq < a.K / 4; kq += 128) {
-          const float4 v = xr[kq];
-          const float4 wv = wv4[kq];
-          uint4 o;
-          split_bf16x2(v.x * sc * wv.x, v.y * sc * wv.y, o.x, o.z);
-          split_bf16x2(v.z * sc * wv.z, v.w * sc * wv.w, o.y, o.w);
-          xr[kq] = *reinterpret_cast<const float4*>(&o);
-        }
-      }
-    }
-  }
   if constexpr (XMODE == X_PACKED) {
     // Copy the packed rows in; meanwhile 1 / RMS per row from the producing
     // kernel's partial sums of squares (fixed summation order).

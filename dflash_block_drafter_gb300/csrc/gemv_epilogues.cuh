@@ -13,54 +13,19 @@ namespace dflash {
 struct NoLocal {};
 
 // Y stored as fp32 [R, ldo] (activation row major).  Feature fusion: fc.
-struct EpiStore {
-  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
-  using Local = NoLocal;
-  float* out;
-  int ldo;
-  __device__ void init(Local&) const {}
-  __device__ void prologue(const GemvArgs&, int, const float*) const {}
-  template <int WT, int NT>
-  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
-    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int n = t * 8 + (lane & 3) * 2;
-      out[static_cast<size_t>(n) * ldo + m0] = acc[t][0];
-      out[static_cast<size_t>(n + 1) * ldo + m0] = acc[t][1];
-      out[static_cast<size_t>(n) * ldo + m1] = acc[t][2];
-      out[static_cast<size_t>(n + 1) * ldo + m1] = acc[t][3];
-    }
-  }
-  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
-  template <int NT>
-  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
-};
-
-// Residual update x[R, ldx] += Y: attention output projection and MLP down
-// projection.  Every element has exactly one owner thread.
-struct EpiResid {
-  static constexpr bool kAfterGroup = false, kFinish = false;
-  // a split group's finisher loads its residual values before it knows it
-  // is the finisher, overlapping that load with the arrival counter
-  static constexpr bool kPreload = true;
-  using Local = NoLocal;
-  float* x;
-  int ldx;
-  // Optional (8-row passes): the next RMSNorm-fed GEMV's packed operand.
-  // For each finished 64-column group g: xpk[n * ldx + m] = BF16 hi/lo of
-  // x_new[n][m] * w_next[m] in the MMA operand order (per 4 columns {hi01,
-  // hi23, lo01, lo23}), and ssq[g * 8 + n] = sum of x_new[n][m]^2 over the
-  // group.  Null xpk: none.
+// Optional output of an epilogue that produces the rows x of a pass with 8
+// rows: the next RMSNorm-fed GEMV's packed operand.  For each finished
+// 64-column group g: xpk[n * ld + m] = BF16 hi/lo of x[n][m] * w_next[m] in
+// the MMA operand order (per 4 columns {hi01, hi23, lo01, lo23}), and
+// ssq[g * 8 + n] = sum of x[n][m]^2 over the group.  Null xpk: none.
+struct PackNext {
   uint32_t* xpk;
   float* ssq;
   const float* w_next;
-
-  __device__ void init(Local&) const {}
-  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  int ld;
 
   template <int WT, int NT>
-  __device__ void pack_next(int g, int w, int lane, const float (&v)[NT][4]) const {
+  __device__ void operator()(int g, int w, int lane, const float (&v)[NT][4]) const {
     if constexpr (NT == 1) {
       if (xpk == nullptr) return;
       __shared__ __align__(16) float tile[8][64 + 4];
@@ -79,7 +44,7 @@ struct EpiResid {
       uint4 o;
       split_bf16x2(xv.x * wv.x, xv.y * wv.y, o.x, o.z);
       split_bf16x2(xv.z * wv.z, xv.w * wv.w, o.y, o.w);
-      *reinterpret_cast<uint4*>(xpk + static_cast<size_t>(row) * ldx + m) = o;
+      *reinterpret_cast<uint4*>(xpk + static_cast<size_t>(row) * ld + m) = o;
       float ss = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
 #pragma unroll
       for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -87,6 +52,48 @@ struct EpiResid {
       named_bar_sync(1, 128);  // the tile is reused by the next group
     }
   }
+};
+
+struct EpiStore {
+  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
+  using Local = NoLocal;
+  float* out;
+  int ldo;
+  PackNext pack;  // optional (the fusion's fc output feeds the context K/V GEMV)
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  template <int WT, int NT>
+  __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int n = t * 8 + (lane & 3) * 2;
+      out[static_cast<size_t>(n) * ldo + m0] = acc[t][0];
+      out[static_cast<size_t>(n + 1) * ldo + m0] = acc[t][1];
+      out[static_cast<size_t>(n) * ldo + m1] = acc[t][2];
+      out[static_cast<size_t>(n + 1) * ldo + m1] = acc[t][3];
+    }
+    pack.template operator()<WT, NT>(g, w, lane, acc);
+  }
+  __device__ void after_group(const GemvArgs&, int, int, int*) const {}
+  template <int NT>
+  __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
+};
+
+// Residual update x[R, ldx] += Y: attention output projection and MLP down
+// projection.  Every element has exactly one owner thread.
+struct EpiResid {
+  static constexpr bool kAfterGroup = false, kFinish = false;
+  // a split group's finisher loads its residual values before it knows it
+  // is the finisher, overlapping that load with the arrival counter
+  static constexpr bool kPreload = true;
+  using Local = NoLocal;
+  float* x;
+  int ldx;
+  PackNext pack;  // optional: the next RMSNorm-fed GEMV's operand from x_new
+
+  __device__ void init(Local&) const {}
+  __device__ void prologue(const GemvArgs&, int, const float*) const {}
 
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
@@ -108,7 +115,7 @@ struct EpiResid {
       *p01 = v[t][2];
       *p11 = v[t][3];
     }
-    pack_next<WT, NT>(g, w, lane, v);
+    pack.template operator()<WT, NT>(g, w, lane, v);
   }
   template <int WT, int NT>
   __device__ void preload(int g, int w, int lane, float (&pre)[NT][4]) const {
@@ -136,7 +143,7 @@ struct EpiResid {
       x[static_cast<size_t>(n) * ldx + m1] = v[t][2];
       x[static_cast<size_t>(n + 1) * ldx + m1] = v[t][3];
     }
-    pack_next<WT, NT>(g, w, lane, v);
+    pack.template operator()<WT, NT>(g, w, lane, v);
   }
   __device__ void after_group(const GemvArgs&, int, int, int*) const {}
   template <int NT>
@@ -350,7 +357,7 @@ struct EpiArgmax {
   int32_t* drafts;               // [n_seq, 7]
   unsigned long long* slots;     // [gridDim.x, R]
   int* grid_cnt;
-  float* final_hidden;           // optional [n_seq, 8, H] (X_RESIDENT prologue)
+  float* final_hidden;           // optional [n_seq, 8, H] (X_PACKED prologue)
   const float* x;                // residual rows for final_hidden
   const float* norm_w;
   int H;

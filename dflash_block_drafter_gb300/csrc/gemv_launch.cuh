@@ -106,10 +106,9 @@ cudaError_t gemv_resid(int nt, const GemvArgs& a, const EpiResid& e, const Launc
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
-// The RMSNorm-fed GEMVs read X whole into shared memory for one n-tile when
-// the hidden size fits: in the draft pass (q/k/v, gate/up, LM head) as the
-// packed rows the previous kernel wrote (X_PACKED); in the fusion (K/V) as
-// fp32 rows normalised in the prologue (X_RESIDENT).  Otherwise X is streamed
+// The RMSNorm-fed GEMVs (q/k/v, gate/up, LM head, fusion K/V) of an 8-row
+// pass read their rows whole into shared memory, packed by the kernel that
+// produced x (X_PACKED), when the hidden size fits; otherwise X is streamed
 // from a separate RMSNorm kernel's chunked output.
 inline bool resident_ok(int nt, int K) { return nt == 1 && K <= 2560; }
 
@@ -125,8 +124,7 @@ cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, const LaunchCfg& lc)
 // Per-head epilogue (draft QKV / fusion K/V).
 template <int WT>
 cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
-  if (resident_ok(nt, a.K))
-    return e.mode == 0 ? launch_gemv<WT, 1, X_PACKED>(a, e, lc) : launch_gemv<WT, 1, X_RESIDENT>(a, e, lc);
+  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_PACKED>(a, e, lc);
   if (e.mode == 1) {
     switch (nt) {
       case 1: return launch_gemv<WT, 1, X_STREAM>(a, e, lc);

@@ -19,7 +19,6 @@ enum WType : int { WT_BF16 = 0, WT_Q8_0 = 1, WT_Q5_0 = 2, WT_Q4_0 = 3, WT_HEAD =
 
 // How a GEMV kernel obtains its activation rows X.
 enum XMode : int {
-  X_RESIDENT = 0,  // RMSNorm(x) * w computed in the prologue into shared memory
   X_STREAM = 1,    // X chunks copied from global memory with each weight unit
   X_STREAM_BF16 = 2,  // as X_STREAM, but X is BF16 whatever the weight type (the caller's taps)
   X_PACKED = 3        // rows of x * w already split into BF16 hi/lo by the kernel that produced x,
