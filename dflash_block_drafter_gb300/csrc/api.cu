@@ -168,7 +168,7 @@ void free_state(State* s) {
   if (!s) return;
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
-  f(s->xpk); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
+  f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
   f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->status);
 }
 
@@ -479,7 +479,7 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->attn_out, xchunk_elems(nq * d, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->hbuf, xchunk_elems(I, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->xnorm, xchunk_elems(H, R, 128, 2) * 2, &total));
-  STRY(dev_alloc(&s->xpk, size_t(8) * H * 4, &total));
+  STRY(dev_alloc(&s->xn, xchunk_elems(H, 8, 128, 2) * 2, &total));  // largest for 128 inputs per unit
   STRY(dev_alloc(&s->ssq, size_t(H / 64) * 8 * 4, &total));
   STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 2, &total));
   STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks_max * M * 8, &total));
@@ -550,8 +550,8 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       a.X = taps + static_cast<size_t>(base) * tw;
       a.ldx = tw;
       // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
-      const bool fpacked = resident_ok(nt, H);
-      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xpk : nullptr, s->ssq, m->hidden_norm, H}};
+      const bool fpacked = fused_norm(nt);
+      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt)}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
@@ -561,8 +561,8 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       GemvArgs a = base_args(m->kv_all, *s, CNT_KV, status);
       a.n_valid_rows = rows;
       a.eps = c.norm_eps;
-      if (resident_ok(nt, H)) {
-        a.X = s->xpk;
+      if (fused_norm(nt)) {
+        a.X = s->xn;
         a.ldx = H;
         a.ssq = s->ssq;
         a.n_ssq = H / 64;
@@ -624,18 +624,19 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   s->prof_k = 0;
   // one-slot passes: every RMSNorm-fed GEMV reads the packed rows that the
   // kernel producing x wrote (embed, o-proj and down residual epilogues)
-  const bool packed = resident_ok(nt, H);
+  const bool packed = fused_norm(nt);
   auto set_packed = [&](GemvArgs& a) {
-    a.X = s->xpk;
+    a.X = s->xn;
     a.ldx = H;
     a.ssq = s->ssq;
     a.n_ssq = H / 64;
   };
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
-                 s->capacity, status, nullptr, nullptr, nullptr};
+                 s->capacity, status, nullptr, nullptr, nullptr, 0};
     if (packed) {
-      ea.xpk = s->xpk;
+      ea.xn = s->xn;
+      ea.ku = ku_of(wt);
       ea.ssq = s->ssq;
       ea.w_next = m->attn_norm;
     }
@@ -696,7 +697,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->attn_out;
       a.ldx = nq * d;
-      EpiResid e{s->x, H, PackNext{packed ? s->xpk : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, H}};
+      EpiResid e{s->x, H, PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt)}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
@@ -726,8 +727,9 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.X = s->hbuf;
       a.ldx = I;
       EpiResid e{s->x, H,
-                 PackNext{packed ? s->xpk : nullptr, s->ssq,
-                          l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm, H}};
+                 PackNext{packed ? s->xn : nullptr, s->ssq,
+                          l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm,
+                          l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
@@ -868,7 +870,7 @@ int dflash_model_dequantize(const dflash_model* m, int32_t which, float* out, df
 int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   if (!s || n_seq < 1 || n_seq > s->n_slots) return -1;
   const int L = s->model->cfg.n_layers;
-  const bool streamed = !resident_ok(pow2ceil(n_seq), s->model->cfg.hidden);  // separate RMSNorm kernels
+  const bool streamed = !fused_norm(pow2ceil(n_seq));  // separate RMSNorm kernels
   const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
   return 1 + L * per_layer + 1 + (streamed ? 1 : 0);
 }
@@ -878,7 +880,7 @@ int32_t dflash_fuse_launches(const dflash_state* s, int32_t n) {
   int k = 0;
   for (int base = 0; base < n; base += s->fuse_rows) {
     const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
-    k += resident_ok(rows <= 8 ? 1 : 16, s->model->cfg.hidden) ? 2 : 3;
+    k += fused_norm(rows <= 8 ? 1 : 16) ? 2 : 3;
   }
   return k;
 }

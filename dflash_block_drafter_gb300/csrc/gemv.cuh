@@ -34,9 +34,9 @@ struct GemvArgs {
   const void* X;
   int ldx;
   float eps;
-  // X_PACKED: X holds rows of packed x * w (uint32 per input, MMA operand
-  // order) and ssq[g * 8 + r] the sum of x^2 over inputs [64 g, 64 g + 64)
-  // of row r, g < n_ssq
+  // X_NORM: X in the chunked layout (two BF16 planes) holding x * w, not yet
+  // divided by the row's RMS; ssq[g * 8 + r] = sum of x^2 over inputs
+  // [64 g, 64 g + 64) of row r, g < n_ssq; 1 / RMS scales the outputs
   const float* ssq;
   int n_ssq;
   float* partials;               // [gridDim.x, 2, 64, R]
@@ -63,11 +63,9 @@ struct GemvGeom {
   static constexpr int KU = F::CB * 32;                 // inputs per unit
   static constexpr int XSE = KU + 32;                   // streamed X row stride (elements, padded)
   static constexpr int XS_STRIDE = XSE * 2;             // ... in bytes
-  static constexpr bool kStream = XMODE == X_STREAM || XMODE == X_STREAM_BF16;
+  static constexpr bool kStream = true;
   // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
-  static constexpr bool kF16 = F::kF16 && XMODE != X_STREAM_BF16 && XMODE != X_PACKED;
-  // activations staged whole in shared memory (fp32 rows, or already packed)
-  static constexpr bool kRes = XMODE == X_PACKED;
+  static constexpr bool kF16 = F::kF16 && XMODE == X_STREAM;
   // BF16 activations computed in fp32 are carried as two BF16 planes, hi and
   // lo = x - hi (about 16 significant bits), each multiplied on the tensor
   // cores; the caller's BF16 taps (X_STREAM_BF16) are exact and need no lo.
@@ -75,21 +73,14 @@ struct GemvGeom {
   static constexpr int XPLANES = kSplit ? 2 : 1;
   static constexpr int XS_BYTES = kStream ? XPLANES * R * XS_STRIDE : 0;
   static constexpr int STAGE = ((F::UNIT + XS_BYTES + 1023) / 1024) * 1024;
-  // Packed X (X_PACKED): R rows of K packed inputs (4 bytes each); sized for K up to kResK.
-  static constexpr int kResK = 2560;
-  static __host__ __device__ constexpr int xres_stride(int K) { return K * 4 + 16; }
-  static __host__ __device__ constexpr int xres_bytes(int K) {
-    return (XMODE == X_PACKED) ? ((R * xres_stride(K) + 127) / 128) * 128 : 0;
-  }
-  static constexpr int RING_BUDGET =
-      (XMODE == X_PACKED) ? (232448 - 4096 - xres_bytes(kResK)) : 190000;
+  static constexpr int RING_BUDGET = 190000;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
   static constexpr int THREADS = 160;
   static constexpr int MISC = 8 * (2 * STAGES + 1) + 64 + 4 * R * 8 + R * 4;
   // smem: [ring][resident X][barriers][misc]
-  static __host__ __device__ constexpr int smem_bytes(int K) { return 1024 + RING + xres_bytes(K) + MISC; }
+  static __host__ __device__ constexpr int smem_bytes(int) { return 1024 + RING + MISC; }
 };
 
 // Epilogue interface (see gemv_epilogues.cuh):
@@ -123,11 +114,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* xres = ring + Geo::RING;                                   // fp32 rows, then the norm weight
-  uint64_t* full = reinterpret_cast<uint64_t*>(xres + Geo::xres_bytes(a.K));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING);
   uint64_t* empty = full + STAGES;
-  uint64_t* xbar = empty + STAGES;
-  int* sflag = reinterpret_cast<int*>(xbar + 1);                      // 16 ints
+  int* sflag = reinterpret_cast<int*>(empty + STAGES);                 // 16 ints
   float* srs = reinterpret_cast<float*>(sflag + 16);                  // [R] row scales
   unsigned long long* sstage = reinterpret_cast<unsigned long long*>(srs + R);  // [4][R]
 
@@ -138,14 +127,12 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.U) / G);
   const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
   const int n_units = u_end - u_begin;
-  const int xstride = Geo::kRes ? Geo::xres_stride(a.K) : Geo::XS_STRIDE;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
-    mbar_init(xbar, 1);
     fence_barrier_init();
   }
   if constexpr (XMODE == X_STREAM_BF16) {
@@ -160,12 +147,6 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       }
     }
   }
-  if constexpr (Geo::kRes) {
-    for (int i = tid; i < (R - a.n_valid_rows) * (a.K / 4); i += Geo::THREADS) {
-      const int rr = a.n_valid_rows + i / (a.K / 4);
-      reinterpret_cast<float4*>(xres + rr * xstride)[i % (a.K / 4)] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
   __syncthreads();
 
   if (warp == 4) {
@@ -175,7 +156,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       const uint64_t pol = l2_policy_evict_first();
       constexpr int XBYTES_ROW = Geo::KU * 2;
       uint32_t tx = F::UNIT;
-      if constexpr (XMODE == X_STREAM) tx += XPLANES * R * Geo::XS_STRIDE;
+      if constexpr (XMODE == X_STREAM || XMODE == X_NORM) tx += XPLANES * R * Geo::XS_STRIDE;
       if constexpr (XMODE == X_STREAM_BF16) tx += a.n_valid_rows * XBYTES_ROW;
       auto issue_w = [&](int it, int u) {
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
@@ -190,7 +171,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       auto issue_x = [&](int it, int u) {
         const int j = u % a.UPG;
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
-        if constexpr (XMODE == X_STREAM) {
+        if constexpr (XMODE == X_STREAM || XMODE == X_NORM) {
           // one contiguous chunk per plane
           const uint8_t* src =
               static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XPLANES * R * Geo::XS_STRIDE;
@@ -239,16 +220,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int w = warp;
   if (tid == 0) DFLASH_STAMP(3);
 
-  if constexpr (XMODE == X_PACKED) {
-    // Copy the packed rows in; meanwhile 1 / RMS per row from the producing
-    // kernel's partial sums of squares (fixed summation order).
-    if (tid == 0) {
-      const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 4;
-      mbar_arrive_expect_tx(xbar, a.n_valid_rows * row_bytes);
-      const uint8_t* x = static_cast<const uint8_t*>(a.X);
-      for (int r = 0; r < a.n_valid_rows; ++r)
-        bulk_g2s(xres + r * xstride, x + static_cast<size_t>(r) * a.ldx * 4, row_bytes, xbar);
-    }
+  if constexpr (XMODE == X_NORM) {
+    // 1 / RMS per row from the producing kernel's partial sums of squares
+    // (fixed summation order); needed only at the first group's end
     for (int r = w; r < R; r += 4) {
       float ss = 0.f;
       for (int g = lane; g < a.n_ssq; g += 32) ss += __ldcg(a.ssq + g * 8 + r);
@@ -256,10 +230,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
     }
-    if (!mbar_wait(xbar, 0)) set_status(a.status, DFLASH_DEV_TIMEOUT);
     named_bar_sync(1, 128);
   }
-  epi.prologue(a, tid, Geo::kRes ? srs : nullptr);
+  epi.prologue(a, tid, XMODE == X_NORM ? srs : nullptr);
   named_bar_sync(1, 128);
   if (tid == 0) DFLASH_STAMP(4);
 
@@ -291,27 +264,12 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
 #pragma unroll
     for (int bl = 0; bl < F::CB; ++bl) {
       const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
-      uint32_t xofs = 0;
-      if constexpr (Geo::kRes) xofs = ((j * F::CB + bl) * 32 + (lane & 3) * 8) * 4;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         uint4 xf, xl;
-        if constexpr (Geo::kRes) {
-          // this lane's 8 packed inputs of its row (layout of the prologue above)
-          const uint8_t* xp = xres + (t * 8 + xrow) * xstride + xofs;
-          if constexpr (kSplit) {
-            const uint4 p0 = *reinterpret_cast<const uint4*>(xp);
-            const uint4 p1 = *reinterpret_cast<const uint4*>(xp + 16);
-            xf = make_uint4(p0.x, p0.y, p1.x, p1.y);
-            xl = make_uint4(p0.z, p0.w, p1.z, p1.w);
-          } else {
-            xf = *reinterpret_cast<const uint4*>(xp);
-          }
-        } else {
-          const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
-          xf = lds128(xb);
-          if constexpr (kSplit) xl = lds128(xb + R * Geo::XS_STRIDE);
-        }
+        const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
+        xf = lds128(xb);
+        if constexpr (kSplit) xl = lds128(xb + R * Geo::XS_STRIDE);
         if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
           mma_bf16_16816(acc[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
           mma_bf16_16816(acc[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
@@ -341,7 +299,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (!Geo::kRes && tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
+    if (tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
 
     if (j == a.UPG - 1 || u == u_end - 1) {
       if constexpr (kSplit && (WT == WT_BF16 || WT == WT_HEAD)) {
@@ -352,7 +310,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
             acc2[t][e] = 0.f;
           }
       }
-      if constexpr (XMODE == X_PACKED) {
+      if constexpr (XMODE == X_NORM) {
         // the rows were multiplied unnormalised: scale each output by 1 / RMS of its row
 #pragma unroll
         for (int t = 0; t < NT; ++t) {

@@ -14,20 +14,21 @@ struct NoLocal {};
 
 // Y stored as fp32 [R, ldo] (activation row major).  Feature fusion: fc.
 // Optional output of an epilogue that produces the rows x of a pass with 8
-// rows: the next RMSNorm-fed GEMV's packed operand.  For each finished
-// 64-column group g: xpk[n * ld + m] = BF16 hi/lo of x[n][m] * w_next[m] in
-// the MMA operand order (per 4 columns {hi01, hi23, lo01, lo23}), and
-// ssq[g * 8 + n] = sum of x[n][m]^2 over the group.  Null xpk: none.
+// rows: the next RMSNorm-fed GEMV's input.  For each finished 64-column
+// group g: x[n][m] * w_next[m] split into BF16 hi and lo = bf16(v - hi), in
+// the chunked layout of 8 rows and `ku` inputs per unit (planes 0 and 1, see
+// xchunk_index), and ssq[g * 8 + n] = sum of x[n][m]^2 over the group.  The
+// GEMV divides its outputs by the row's RMS.  Null xn: none.
 struct PackNext {
-  uint32_t* xpk;
+  __nv_bfloat16* xn;
   float* ssq;
   const float* w_next;
-  int ld;
+  int ku;
 
   template <int WT, int NT>
   __device__ void operator()(int g, int w, int lane, const float (&v)[NT][4]) const {
     if constexpr (NT == 1) {
-      if (xpk == nullptr) return;
+      if (xn == nullptr) return;
       __shared__ __align__(16) float tile[8][64 + 4];
       const int r0 = frag_row<WT>(w, lane >> 2), r1 = frag_row<WT>(w, (lane >> 2) + 8);
       const int n = (lane & 3) * 2;
@@ -41,10 +42,11 @@ struct PackNext {
       const float4 xv = *reinterpret_cast<const float4*>(&tile[row][4 * q]);
       const int m = g * 64 + 4 * q;
       const float4 wv = __ldg(reinterpret_cast<const float4*>(w_next + m));
-      uint4 o;
-      split_bf16x2(xv.x * wv.x, xv.y * wv.y, o.x, o.z);
-      split_bf16x2(xv.z * wv.z, xv.w * wv.w, o.y, o.w);
-      *reinterpret_cast<uint4*>(xpk + static_cast<size_t>(row) * ld + m) = o;
+      uint2 hi, lo;
+      split_bf16x2(xv.x * wv.x, xv.y * wv.y, hi.x, lo.x);
+      split_bf16x2(xv.z * wv.z, xv.w * wv.w, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(xn + xchunk_index(m, row, 0, 8, ku, 2)) = hi;
+      *reinterpret_cast<uint2*>(xn + xchunk_index(m, row, 1, 8, ku, 2)) = lo;
       float ss = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
 #pragma unroll
       for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -357,7 +359,7 @@ struct EpiArgmax {
   int32_t* drafts;               // [n_seq, 7]
   unsigned long long* slots;     // [gridDim.x, R]
   int* grid_cnt;
-  float* final_hidden;           // optional [n_seq, 8, H] (X_PACKED prologue)
+  float* final_hidden;           // optional [n_seq, 8, H] (X_NORM prologue)
   const float* x;                // residual rows for final_hidden
   const float* norm_w;
   int H;

@@ -107,24 +107,24 @@ cudaError_t gemv_resid(int nt, const GemvArgs& a, const EpiResid& e, const Launc
 }
 
 // The RMSNorm-fed GEMVs (q/k/v, gate/up, LM head, fusion K/V) of an 8-row
-// pass read their rows whole into shared memory, packed by the kernel that
-// produced x (X_PACKED), when the hidden size fits; otherwise X is streamed
-// from a separate RMSNorm kernel's chunked output.
-inline bool resident_ok(int nt, int K) { return nt == 1 && K <= 2560; }
+// pass stream x * w in two BF16 planes written by the kernel that produced x,
+// and scale their outputs by 1 / RMS (X_NORM); larger passes stream the
+// output of a separate RMSNorm kernel.
+inline bool fused_norm(int nt) { return nt == 1; }
 
 // SwiGLU gate/up.
 template <int WT>
 cudaError_t gemv_swiglu(int nt, const GemvArgs& a, void* h, const LaunchCfg& lc) {
   // h is written in the format the down projection streams (FP16 for quantised weights)
   const EpiSwiglu<Fmt<WT>::kF16> e{h};
-  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_PACKED>(a, e, lc);
+  if (fused_norm(nt)) return launch_gemv<WT, 1, X_NORM>(a, e, lc);
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
 // Per-head epilogue (draft QKV / fusion K/V).
 template <int WT>
 cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const LaunchCfg& lc) {
-  if (resident_ok(nt, a.K)) return launch_gemv<WT, 1, X_PACKED>(a, e, lc);
+  if (fused_norm(nt)) return launch_gemv<WT, 1, X_NORM>(a, e, lc);
   if (e.mode == 1) {
     switch (nt) {
       case 1: return launch_gemv<WT, 1, X_STREAM>(a, e, lc);
@@ -141,7 +141,7 @@ inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParam
       nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.grid_cnt, p.final_hidden, p.x,
                           p.norm_w, p.H, p.status};
       if constexpr (NT == 1) {
-        if (resident_ok(nt, a.K)) return launch_gemv<WT_HEAD, NT, X_PACKED>(a, e, lc);
+        if (fused_norm(nt)) return launch_gemv<WT_HEAD, NT, X_NORM>(a, e, lc);
       } return launch_gemv<WT_HEAD, NT, X_STREAM>(a, e, lc);)
 }
 

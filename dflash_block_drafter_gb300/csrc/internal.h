@@ -21,9 +21,9 @@ enum WType : int { WT_BF16 = 0, WT_Q8_0 = 1, WT_Q5_0 = 2, WT_Q4_0 = 3, WT_HEAD =
 enum XMode : int {
   X_STREAM = 1,    // X chunks copied from global memory with each weight unit
   X_STREAM_BF16 = 2,  // as X_STREAM, but X is BF16 whatever the weight type (the caller's taps)
-  X_PACKED = 3        // rows of x * w already split into BF16 hi/lo by the kernel that produced x,
-                      // plus that kernel's per-64-column sums of squares; 1 / RMS is applied to
-                      // the results
+  X_NORM = 3          // as X_STREAM with two BF16 planes of x * w written by the kernel that
+                      // produced x, plus its per-64-column sums of squares; the outputs are
+                      // scaled by 1 / RMS of their row (RMSNorm-fed GEMVs)
 };
 
 // One repacked backbone matrix (library-owned, device memory).
@@ -86,7 +86,7 @@ struct State {
   void* attn_out = nullptr;    // [R, n_q d] activation type
   void* hbuf = nullptr;        // [R, I] activation type (SwiGLU output)
   void* xnorm = nullptr;       // [R, H] activation type (normed rows for streamed-X GEMVs)
-  uint32_t* xpk = nullptr;      // [8, H] packed BF16 hi/lo of x * w (next RMSNorm-fed GEMV), one-slot passes
+  __nv_bfloat16* xn = nullptr;  // 8-row passes: BF16 hi/lo planes of x * w (chunked) for the next RMSNorm-fed GEMV
   float* ssq = nullptr;         // [H / 64, 8] partial sums of squares of x
   __half* attn_part = nullptr;  // [slots, n_kv, C, Gq*8, d] chunk partials O / l
   float2* attn_ml = nullptr;   // [slots, n_kv, C, Gq*8] (max in log2 units, sum)

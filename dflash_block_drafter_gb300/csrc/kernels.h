@@ -18,11 +18,13 @@ struct EmbedArgs {
   float* x;
   int H, vocab, mask_id, n_seq, cap;
   int32_t* status;
-  // optional (one slot): the first QKV GEMV's packed operand, as EpiResid
-  // writes it (BF16 hi/lo of x * w_next, per-64-column sums of squares)
-  uint32_t* xpk;
+  // optional (one slot): the first QKV GEMV's input, as PackNext writes it
+  // (BF16 hi/lo planes of x * w_next in the chunked layout of 8 rows and ku
+  // inputs per unit, per-64-column sums of squares)
+  __nv_bfloat16* xn;
   float* ssq;
   const float* w_next;
+  int ku;
 };
 
 // out = RMSNorm(x) * w in the chunked streamed-X layout (layout.cuh) of a

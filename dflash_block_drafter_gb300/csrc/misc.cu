@@ -208,12 +208,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
     }
   }
   const uint16_t* er = a.embed + static_cast<size_t>(tok) * a.H;
-  if (a.xpk == nullptr) {
+  if (a.xn == nullptr) {
     for (int k = threadIdx.x; k < a.H; k += blockDim.x) xr[k] = bf16_bits_to_float(er[k]);
     return;
   }
-  // 4 columns per thread: the fp32 row, its packed x * w_next and the sum of
-  // squares of each 64-column group (16 consecutive lanes, fixed order)
+  // 4 columns per thread: the fp32 row, the BF16 hi/lo planes of x * w_next
+  // and the sum of squares of each 64-column group (16 consecutive lanes,
+  // fixed order)
   const int n = s * 8 + i;
   for (int c0 = 0; c0 < a.H / 4; c0 += blockDim.x) {
     const int c = c0 + threadIdx.x;
@@ -224,10 +225,11 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
                                    __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xffff0000u));
       reinterpret_cast<float4*>(xr)[c] = v;
       const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w_next) + c);
-      uint4 o;
-      split_bf16x2(v.x * wv.x, v.y * wv.y, o.x, o.z);
-      split_bf16x2(v.z * wv.z, v.w * wv.w, o.y, o.w);
-      reinterpret_cast<uint4*>(a.xpk + static_cast<size_t>(n) * a.H)[c] = o;
+      uint2 hi, lo;
+      split_bf16x2(v.x * wv.x, v.y * wv.y, hi.x, lo.x);
+      split_bf16x2(v.z * wv.z, v.w * wv.w, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(a.xn + xchunk_index(4 * c, n, 0, 8, a.ku, 2)) = hi;
+      *reinterpret_cast<uint2*>(a.xn + xchunk_index(4 * c, n, 1, 8, a.ku, 2)) = lo;
       ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
 #pragma unroll
