@@ -759,6 +759,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.slots = s->argmax_slots;
     p.grid_cnt = s->counters + static_cast<size_t>(CNT_ARGMAX) * s->counter_stride;
     p.final_hidden = final_hidden;
+    a.rs_early = final_hidden != nullptr;
     p.x = s->x;
     p.norm_w = m->final_norm;
     p.status = status;

@@ -39,6 +39,7 @@ struct GemvArgs {
   // [64 g, 64 g + 64) of row r, g < n_ssq; 1 / RMS scales the outputs
   const float* ssq;
   int n_ssq;
+  int rs_early;                  // X_NORM: 1 / RMS needed before the first group (final hidden rows)
   float* partials;               // [gridDim.x, 2, 64, R]
   int* counters;                 // [N / 64]
   int32_t* status;
@@ -220,17 +221,37 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const int w = warp;
   if (tid == 0) DFLASH_STAMP(3);
 
-  if constexpr (XMODE == X_NORM) {
-    // 1 / RMS per row from the producing kernel's partial sums of squares
-    // (fixed summation order); needed only at the first group's end
-    for (int r = w; r < R; r += 4) {
-      float ss = 0.f;
-      for (int g = lane; g < a.n_ssq; g += 32) ss += __ldcg(a.ssq + g * 8 + r);
+  // X_NORM: 1 / RMS per row from the producing kernel's partial sums of
+  // squares.  The loads are issued here and the sums formed at the first
+  // group's end (or at once when the epilogue needs them first), so the
+  // weight stream never waits for them.  Warp w owns rows w and w + 4; lane
+  // holds groups lane and lane + 32; fixed summation order.
+  float ssv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  bool rs_ready = XMODE != X_NORM;
+  auto finish_rs = [&]() {
+    if constexpr (XMODE == X_NORM) {
 #pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = w + 4 * rr;
+        float ss = ssv[rr][0] + ssv[rr][1];
+        for (int g = lane + 64; g < a.n_ssq; g += 32) ss += __ldcg(a.ssq + g * 8 + r);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0 && r < R) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
+      }
+      named_bar_sync(1, 128);
+      rs_ready = true;
     }
-    named_bar_sync(1, 128);
+  };
+  if constexpr (XMODE == X_NORM) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = w + 4 * rr, g = lane + 32 * h;
+        if (r < R && g < a.n_ssq) ssv[rr][h] = __ldcg(a.ssq + g * 8 + r);
+      }
+    if (a.rs_early) finish_rs();
   }
   epi.prologue(a, tid, XMODE == X_NORM ? srs : nullptr);
   named_bar_sync(1, 128);
@@ -312,6 +333,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       }
       if constexpr (XMODE == X_NORM) {
         // the rows were multiplied unnormalised: scale each output by 1 / RMS of its row
+        if (!rs_ready) finish_rs();
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int n = t * 8 + (lane & 3) * 2;
