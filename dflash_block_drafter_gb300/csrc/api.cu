@@ -86,6 +86,29 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+// The caller's BF16 rows [rows, cols] for a streamed-input GEMV: boxes of
+// (ku + 32) columns x box_rows rows without swizzle, so a box lands with the
+// GEMV's padded row stride; columns past the tensor read as zeros.
+int make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t ku, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled unavailable");
+    return DFLASH_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {ku + 32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled (rows) failed (%d)", static_cast<int>(r));
+    return DFLASH_ERR_CUDA;
+  }
+  return DFLASH_OK;
+}
+
 // 2-D row-major 16-bit tensor [rows, cols] with 64-column x box_rows boxes, 128-byte swizzle.
 int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, CUtensorMapDataType dt,
                 uint32_t box_rows = 64) {
@@ -549,6 +572,9 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       a.n_valid_rows = rows;
       a.X = taps + static_cast<size_t>(base) * tw;
       a.ldx = tw;
+      if (ku_of(wt) + 32 <= 256)
+        TRY(make_rows_map(&a.xmap, a.X, static_cast<uint64_t>(rows), static_cast<uint64_t>(tw),
+                          static_cast<uint32_t>(ku_of(wt)), static_cast<uint32_t>(rows)));
       // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
       const bool fpacked = fused_norm(nt);
       EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt)}};

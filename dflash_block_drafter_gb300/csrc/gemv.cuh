@@ -24,13 +24,15 @@ namespace dflash {
 
 struct GemvArgs {
   CUtensorMap wmap;              // WT_HEAD only
+  CUtensorMap xmap;              // X_STREAM_BF16 with KU <= 224: the caller's BF16 rows
+                                 // [n_valid_rows, K], boxes of (KU + 32) inputs x n_valid_rows rows
   const uint8_t* W;              // packed weights (fragment-native formats)
   int N, K;                      // logical rows / inputs
   int UPG;                       // units per 64-row group
   int U;                         // total units
   int n_valid_rows;              // activation rows that exist (others read as zero)
   // X_STREAM: activations in the chunked layout (layout.cuh), R = 8 * NT rows
-  // X_STREAM_BF16: BF16 rows X[r * ldx + k] (the caller's taps)
+  // X_STREAM_BF16: BF16 rows X[r * ldx + k] (the caller's taps), read through xmap
   const void* X;
   int ldx;
   float eps;
@@ -154,11 +156,13 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       if constexpr (WT == WT_HEAD) prefetch_tensormap(&a.wmap);
+      // a TMA box spans at most 256 inputs: wider units copy row by row
+      constexpr bool kXBox = Geo::KU + 32 <= 256;
+      if constexpr (XMODE == X_STREAM_BF16 && kXBox) prefetch_tensormap(&a.xmap);
       const uint64_t pol = l2_policy_evict_first();
-      constexpr int XBYTES_ROW = Geo::KU * 2;
       uint32_t tx = F::UNIT;
       if constexpr (XMODE == X_STREAM || XMODE == X_NORM) tx += XPLANES * R * Geo::XS_STRIDE;
-      if constexpr (XMODE == X_STREAM_BF16) tx += a.n_valid_rows * XBYTES_ROW;
+      if constexpr (XMODE == X_STREAM_BF16) tx += a.n_valid_rows * (kXBox ? Geo::XS_STRIDE : Geo::KU * 2);
       auto issue_w = [&](int it, int u) {
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
         if constexpr (WT == WT_HEAD) {
@@ -178,10 +182,16 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
               static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XPLANES * R * Geo::XS_STRIDE;
           bulk_g2s(dst, src, XPLANES * R * Geo::XS_STRIDE, &full[it % STAGES]);
         } else if constexpr (XMODE == X_STREAM_BF16) {
-          const uint8_t* src = static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XBYTES_ROW;
-          for (int r = 0; r < a.n_valid_rows; ++r)
-            bulk_g2s(dst + r * Geo::XS_STRIDE, src + static_cast<size_t>(r) * a.ldx * 2, XBYTES_ROW,
-                     &full[it % STAGES]);
+          if constexpr (kXBox) {
+            // one box: the valid rows x (KU + 32) inputs from input j * KU,
+            // landing with the padded row stride; the 32 extra inputs are never read
+            tma_load_2d(dst, &a.xmap, j * Geo::KU, 0, &full[it % STAGES]);
+          } else {
+            const uint8_t* src = static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * Geo::KU * 2;
+            for (int r = 0; r < a.n_valid_rows; ++r)
+              bulk_g2s(dst + r * Geo::XS_STRIDE, src + static_cast<size_t>(r) * a.ldx * 2, Geo::KU * 2,
+                       &full[it % STAGES]);
+          }
         }
       };
       const int n_pre = n_units < STAGES ? n_units : STAGES;
