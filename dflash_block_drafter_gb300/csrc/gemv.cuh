@@ -374,7 +374,8 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
         // the CTA's stores, ordered by the barrier, are released by thread 0's
         // acquire-release counter increment; the last arriver acquires the others'
         float pre[NT][4];
-        if constexpr (Epi::kPreload) epi.template preload<WT, NT>(g, w, lane, pre);
+        float4 wpre = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (Epi::kPreload) epi.template preload<WT, NT>(g, w, lane, pre, wpre);
         named_bar_sync(1, 128);
         const long long ufirst = static_cast<long long>(g) * a.UPG;
         const int c_first = cta_of_unit(ufirst, G, a.U);
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
           }
           if (tid == 0) a.counters[g] = 0;
           if constexpr (Epi::kPreload)
-            epi.template group_pre<WT, NT>(g, w, lane, acc, pre);
+            epi.template group_pre<WT, NT>(g, w, lane, acc, pre, wpre);
           else
             epi.template group<WT, NT>(a, loc, g, w, lane, acc);
           if constexpr (Epi::kAfterGroup) {

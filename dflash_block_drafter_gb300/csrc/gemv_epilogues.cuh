@@ -25,11 +25,22 @@ struct PackNext {
   const float* w_next;
   int ku;
 
+  // the four norm weights thread (w, lane) applies in group g (a load with no
+  // dependence on the GEMV, so a finisher can issue it early)
+  __device__ float4 load_w(int g, int w, int lane) const {
+    const int q = (w * 32 + lane) & 15;
+    return __ldg(reinterpret_cast<const float4*>(w_next + g * 64 + 4 * q));
+  }
+
   template <int WT, int NT>
-  __device__ void operator()(int g, int w, int lane, const float (&v)[NT][4]) const {
+  __device__ void operator()(int g, int w, int lane, const float (&v)[NT][4], const float4* wpre = nullptr) const {
     if constexpr (NT == 1) {
       if (xn == nullptr) return;
       __shared__ __align__(16) float tile[8][64 + 4];
+      // thread (row = tid / 16, q = tid % 16): columns 4q .. 4q + 3 of the group
+      const int tid = w * 32 + lane, row = tid >> 4, q = tid & 15;
+      const int m = g * 64 + 4 * q;
+      const float4 wv = wpre ? *wpre : load_w(g, w, lane);
       const int r0 = frag_row<WT>(w, lane >> 2), r1 = frag_row<WT>(w, (lane >> 2) + 8);
       const int n = (lane & 3) * 2;
       tile[n][r0] = v[0][0];
@@ -37,11 +48,7 @@ struct PackNext {
       tile[n][r1] = v[0][2];
       tile[n + 1][r1] = v[0][3];
       named_bar_sync(1, 128);
-      // thread (row = tid / 16, q = tid % 16): columns 4q .. 4q + 3 of the group
-      const int tid = w * 32 + lane, row = tid >> 4, q = tid & 15;
       const float4 xv = *reinterpret_cast<const float4*>(&tile[row][4 * q]);
-      const int m = g * 64 + 4 * q;
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(w_next + m));
       uint2 hi, lo;
       split_bf16x2(xv.x * wv.x, xv.y * wv.y, hi.x, lo.x);
       split_bf16x2(xv.z * wv.z, xv.w * wv.w, hi.y, lo.y);
@@ -120,7 +127,8 @@ struct EpiResid {
     pack.template operator()<WT, NT>(g, w, lane, v);
   }
   template <int WT, int NT>
-  __device__ void preload(int g, int w, int lane, float (&pre)[NT][4]) const {
+  __device__ void preload(int g, int w, int lane, float (&pre)[NT][4], float4& wpre) const {
+    if (NT == 1 && pack.xn != nullptr) wpre = pack.load_w(g, w, lane);
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -132,7 +140,8 @@ struct EpiResid {
     }
   }
   template <int WT, int NT>
-  __device__ void group_pre(int g, int w, int lane, const float (&acc)[NT][4], const float (&pre)[NT][4]) const {
+  __device__ void group_pre(int g, int w, int lane, const float (&acc)[NT][4], const float (&pre)[NT][4],
+                            const float4& wpre) const {
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
     float v[NT][4];
 #pragma unroll
@@ -145,7 +154,7 @@ struct EpiResid {
       x[static_cast<size_t>(n) * ldx + m1] = v[t][2];
       x[static_cast<size_t>(n + 1) * ldx + m1] = v[t][3];
     }
-    pack.template operator()<WT, NT>(g, w, lane, v);
+    pack.template operator()<WT, NT>(g, w, lane, v, &wpre);
   }
   __device__ void after_group(const GemvArgs&, int, int, int*) const {}
   template <int NT>
@@ -272,63 +281,96 @@ struct EpiHeads {
       kvh = rem < n_kv ? rem : rem - n_kv;
       wn = kind == 1 ? k_norm + static_cast<size_t>(l) * d : nullptr;
     }
-    for (int n = w; n < R; n += 4) {
-      int pos, s;
-      bool write_state;
-      if (mode == 0) {
-        s = n >> 3;
-        const int i = n & 7;
-        if (s < n_seq) {
-          int B = block_len[s];
-          B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
-          pos = anchor_pos[s] + i;
-          write_state = (i < B) && pos >= 0 && pos < cap;
-        } else {
-          pos = 0;
-          write_state = false;
+    // the head's per-column constants, loaded once and independent of the rows
+    const int hj = d / 64;  // pairs per lane; element i + d/2 sits at yv[j + hj]
+    float wa[4], wb[4];
+    uint64_t tn[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      wa[j] = wb[j] = 0.f;
+      tn[j] = 0;
+      if (kind != 2 && j < hj) {
+        const int i = lane + 32 * j;
+        wa[j] = __ldg(wn + i);
+        wb[j] = __ldg(wn + i + half);
+        tn[j] = __ldg(turns + i);
+      }
+    }
+    // warp w takes rows w, w + 4, w + 8, ... two at a time, both rows' loads in flight together
+    for (int n0 = w; n0 < R; n0 += 8) {
+      int pos[2], sl[2];
+      bool use[2], write_state[2];
+      float yv[2][8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = n0 + 4 * q;
+        pos[q] = 0;
+        sl[q] = 0;
+        write_state[q] = false;
+        use[q] = n < R;
+        if (use[q]) {
+          if (mode == 0) {
+            sl[q] = n >> 3;
+            const int i = n & 7;
+            if (sl[q] < n_seq) {
+              int B = block_len[sl[q]];
+              B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+              pos[q] = anchor_pos[sl[q]] + i;
+              write_state[q] = (i < B) && pos[q] >= 0 && pos[q] < cap;
+            }
+          } else {
+            sl[q] = slot;
+            if (n >= n_valid) {
+              use[q] = false;
+            } else {
+              pos[q] = positions[n];
+              write_state[q] = pos[q] >= 0 && pos[q] < cap;
+              if (!write_state[q] && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
+            }
+          }
+          if (kind != 0 && !write_state[q]) use[q] = false;
         }
-      } else {
-        s = slot;
-        if (n >= n_valid) continue;
-        pos = positions[n];
-        write_state = pos >= 0 && pos < cap;
-        if (!write_state && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
+        // the row's d values, lane-strided: element lane + 32 j (d <= 256)
+        const float* y = raw + static_cast<size_t>(n) * ldr + static_cast<size_t>(hh) * d;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) yv[q][j] = (use[q] && lane + 32 * j < d) ? __ldcg(y + lane + 32 * j) : 0.f;
       }
-      const float* y = raw + static_cast<size_t>(n) * ldr + static_cast<size_t>(hh) * d;
-      if (kind != 0 && !write_state) continue;
-      // the row's d values, lane-strided: element lane + 32 j (d <= 256)
-      float yv[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) yv[j] = (lane + 32 * j < d) ? __ldcg(y + lane + 32 * j) : 0.f;
-      const size_t cell = ((static_cast<size_t>((l * n_slots + s) * n_kv + kvh) * cap) + pos) * d;
-      if (kind == 2) {
+      for (int q = 0; q < 2; ++q) {
+        if (!use[q]) continue;
+        const int n = n0 + 4 * q;
+        const size_t cell = ((static_cast<size_t>((l * n_slots + sl[q]) * n_kv + kvh) * cap) + pos[q]) * d;
+        if (kind == 2) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (lane + 32 * j < d) Vst[cell + lane + 32 * j] = __float2half_rn(yv[j]);
-        continue;
-      }
-      float ss = 0.f;
+          for (int j = 0; j < 8; ++j)
+            if (lane + 32 * j < d) Vst[cell + lane + 32 * j] = __float2half_rn(yv[q][j]);
+          continue;
+        }
+        float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ss += yv[j] * yv[j];
+        for (int j = 0; j < 8; ++j) ss += yv[q][j] * yv[q][j];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float rs = rsqrtf(ss / d + eps);
-      // queries: [slot][kv head][m = local head * 8 + block row][d] (contiguous per slot and kv head)
-      const int gq = n_q / n_kv;
-      __half* dst = kind == 0 ? q_ready + ((static_cast<size_t>(s * n_kv + hh / gq) * gq + hh % gq) * 8 + (n & 7)) * d
-                              : Kst + cell;
-      const float scale = kind == 0 ? q_scale : 1.f;
-      const int hj = d / 64;  // pairs per lane; element i + d/2 sits at yv[j + hj]
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float rs = rsqrtf(ss / d + eps);
+        // queries: [slot][kv head][m = local head * 8 + block row][d] (contiguous per slot and kv head)
+        const int gq = n_q / n_kv;
+        __half* dst = kind == 0
+                          ? q_ready + ((static_cast<size_t>(sl[q] * n_kv + hh / gq) * gq + hh % gq) * 8 + (n & 7)) * d
+                          : Kst + cell;
+        const float scale = kind == 0 ? q_scale : 1.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j < hj) {
-          const int i = lane + 32 * j;
-          const float a = yv[j] * rs * wn[i];
-          const float b = yv[j + hj] * rs * wn[i + half];
-          float sn, cs;
-          rope_sincos(turns[i], pos, sn, cs);
-          dst[i] = __float2half_rn((a * cs - b * sn) * scale);
-          dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+        for (int j = 0; j < 4; ++j) {
+          if (j < hj) {
+            const int i = lane + 32 * j;
+            const float a = yv[q][j] * rs * wa[j];
+            // element i + d/2 (d = 64, 128 or 256), picked without a runtime register index
+            const float yb = hj == 4 ? yv[q][(j + 4) & 7] : (hj == 2 ? yv[q][(j + 2) & 7] : yv[q][(j + 1) & 7]);
+            const float b = yb * rs * wb[j];
+            float sn, cs;
+            rope_sincos(tn[j], pos[q], sn, cs);
+            dst[i] = __float2half_rn((a * cs - b * sn) * scale);
+            dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+          }
         }
       }
     }
