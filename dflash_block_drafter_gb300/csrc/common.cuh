@@ -264,6 +264,11 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on a named barrier without waiting (the producer side of a
+// producer / consumer pair whose consumers call named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // --------------------------------------------------------------- warp MMA
 // D[16x8] += A[16x16] * B[16x8], fp32 accumulate.

@@ -76,13 +76,19 @@ struct GemvGeom {
   static constexpr int XPLANES = kSplit ? 2 : 1;
   static constexpr int XS_BYTES = kStream ? XPLANES * R * XS_STRIDE : 0;
   static constexpr int STAGE = ((F::UNIT + XS_BYTES + 1023) / 1024) * 1024;
-  static constexpr int RING_BUDGET = 190000;
+  // Two consumer warpgroups split each unit's CB blocks (K halves): a
+  // scheduler runs two consumer warps, hiding the MMA and shared-memory
+  // latencies of one behind the other.  At each group end the second
+  // warpgroup hands its partial sums to the first through a double buffer.
+  static constexpr int CWG = NT <= 4 ? 2 : 1;  // larger tiles keep 160 threads (register budget)
+  static constexpr int SBUF = CWG > 1 ? 2 * 128 * NT * 16 : 0;  // [2][128 threads][NT][4] floats
+  static constexpr int RING_BUDGET = 190000 - SBUF;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
-  static constexpr int THREADS = 160;
-  static constexpr int MISC = 8 * (2 * STAGES + 1) + 64 + 4 * R * 8 + R * 4;
-  // smem: [ring][resident X][barriers][misc]
+  static constexpr int THREADS = 128 * CWG + 32;
+  static constexpr int MISC = SBUF + 8 * (2 * STAGES + 1) + 64 + 4 * R * 8 + R * 4;
+  // smem: [ring][partial-sum double buffer][barriers][misc]
   static __host__ __device__ constexpr int smem_bytes(int) { return 1024 + RING + MISC; }
 };
 
@@ -104,7 +110,8 @@ __device__ __forceinline__ int cta_of_unit(long long u, int G, int U) {
 }
 
 template <int WT, int NT, int XMODE, class Epi>
-__global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ Epi epi) {
+__global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
+    gemv_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ Epi epi) {
   using Geo = GemvGeom<WT, NT, XMODE>;
   using F = Fmt<WT>;
   constexpr int R = Geo::R;
@@ -117,7 +124,8 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING);
+  float4* sbuf = reinterpret_cast<float4*>(ring + Geo::RING);          // [2][128][NT] (second warpgroup's sums)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING + Geo::SBUF);
   uint64_t* empty = full + STAGES;
   int* sflag = reinterpret_cast<int*>(empty + STAGES);                 // 16 ints
   float* srs = reinterpret_cast<float*>(sflag + 16);                  // [R] row scales
@@ -134,7 +142,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], 4 * Geo::CWG);
     }
     fence_barrier_init();
   }
@@ -152,7 +160,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   }
   __syncthreads();
 
-  if (warp == 4) {
+  if (warp == 4 * Geo::CWG) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       if constexpr (WT == WT_HEAD) prefetch_tensormap(&a.wmap);
@@ -228,7 +236,9 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   // -------------------------------------------------------------- consumers
   pdl_wait();
   pdl_launch_dependents();
-  const int w = warp;
+  // warp w of warpgroup kh: m-tile w, blocks [kh * CB / CWG, (kh + 1) * CB / CWG) of every unit
+  const int w = warp & 3, kh = warp >> 2;
+  constexpr int BPW = F::CB / Geo::CWG;
   if (tid == 0) DFLASH_STAMP(3);
 
   // X_NORM: 1 / RMS per row from the producing kernel's partial sums of
@@ -253,18 +263,20 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
       rs_ready = true;
     }
   };
-  if constexpr (XMODE == X_NORM) {
+  if (kh == 0) {
+    if constexpr (XMODE == X_NORM) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+      for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = w + 4 * rr, g = lane + 32 * h;
-        if (r < R && g < a.n_ssq) ssv[rr][h] = __ldcg(a.ssq + g * 8 + r);
-      }
-    if (a.rs_early) finish_rs();
+        for (int h = 0; h < 2; ++h) {
+          const int r = w + 4 * rr, g = lane + 32 * h;
+          if (r < R && g < a.n_ssq) ssv[rr][h] = __ldcg(a.ssq + g * 8 + r);
+        }
+      if (a.rs_early) finish_rs();
+    }
+    epi.prologue(a, tid, XMODE == X_NORM ? srs : nullptr);
+    named_bar_sync(1, 128);
   }
-  epi.prologue(a, tid, XMODE == X_NORM ? srs : nullptr);
-  named_bar_sync(1, 128);
   if (tid == 0) DFLASH_STAMP(4);
 
   typename Epi::Local loc;
@@ -278,6 +290,7 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
   const uint32_t ring_s = smem_u32(ring);
   const int xrow = lane >> 2;
   bool ok = true;
+  int gcount = 0;  // group ends passed (the same sequence in both warpgroups)
 
   // After a timeout the loop keeps running (without waiting) so every warp
   // takes the same named barriers; the outputs are then unspecified.
@@ -293,7 +306,8 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
     const uint32_t ubase = ring_s + s * Geo::STAGE;
 
 #pragma unroll
-    for (int bl = 0; bl < F::CB; ++bl) {
+    for (int bq = 0; bq < BPW; ++bq) {
+      const int bl = kh * BPW + bq;
       const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -340,6 +354,33 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
             acc[t][e] += acc2[t][e];
             acc2[t][e] = 0.f;
           }
+      }
+      if constexpr (Geo::CWG > 1) {
+        // second warpgroup: hand the K-half sums to the first and go on
+        // (barrier 2 + b: buffer b filled; barrier 4 + b: buffer b free again)
+        float4* sb = sbuf + (static_cast<size_t>(gcount & 1) * 128 + (w * 32 + lane)) * NT;
+        if (kh == 1) {
+          if (gcount >= 2) named_bar_sync(4 + (gcount & 1), 256);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            sb[t] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+            acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+          }
+          named_bar_arrive(2 + (gcount & 1), 256);
+          ++gcount;
+          continue;
+        }
+        named_bar_sync(2 + (gcount & 1), 256);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float4 q = sb[t];
+          acc[t][0] += q.x;
+          acc[t][1] += q.y;
+          acc[t][2] += q.z;
+          acc[t][3] += q.w;
+        }
+        named_bar_arrive(4 + (gcount & 1), 256);
+        ++gcount;
       }
       if constexpr (XMODE == X_NORM) {
         // the rows were multiplied unnormalised: scale each output by 1 / RMS of its row
@@ -435,6 +476,12 @@ __global__ void __launch_bounds__(160, 1) gemv_kernel(const __grid_constant__ Ge
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     }
+  }
+  if constexpr (Geo::CWG > 1) {
+    // the first warpgroup's last two buffer releases have no later fill to pair with
+    if (kh == 1)
+      for (int gc = (gcount > 2 ? gcount - 2 : 0); gc < gcount; ++gc) named_bar_sync(4 + (gc & 1), 256);
+    if (kh == 1) return;
   }
   if constexpr (Epi::kFinish) epi.template finish<NT>(a, loc, w, lane, tid, sstage, sflag);
   if (tid == 0) DFLASH_STAMP(7);
