@@ -450,6 +450,50 @@ struct EpiArgmax {
            static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(id));
   }
 
+  // In the last CTA: the largest key of each of the R rows over every CTA's
+  // slot (exact, order-free).  All 128 threads take part: thread t scans row
+  // t % R over CTAs t / R, t / R + 128 / R, ... with 8 loads in flight, then
+  // the stripes of a row are combined.  The result is valid in threads t < R.
+  template <int R>
+  __device__ unsigned long long grid_max(int tid, int w, int lane, unsigned long long* sstage) const {
+    constexpr int NS = 128 / R;
+    const int G = static_cast<int>(gridDim.x);
+    const int r = tid % R, st = tid / R;
+    unsigned long long k = 0ull;
+    for (int c0 = st; c0 < G; c0 += 8 * NS) {
+      unsigned long long v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int c = c0 + q * NS;
+        v[q] = c < G ? __ldcg(slots + static_cast<size_t>(c) * R + r) : 0ull;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) k = v[q] > k ? v[q] : k;
+    }
+    if constexpr (R < 32) {
+      // lanes r, r + R, ... of a warp hold row r
+#pragma unroll
+      for (int o = R; o < 32; o <<= 1) {
+        const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, k, o);
+        k = k2 > k ? k2 : k;
+      }
+      if (lane < R) sstage[w * R + lane] = k;
+    } else {
+      sstage[tid] = k;  // stripe st of row r at st * R + r (at most 4 stripes)
+    }
+    named_bar_sync(1, 128);
+    k = 0ull;
+    if (tid < R) {
+      constexpr int E = R < 32 ? 4 : 128 / R;  // partial maxima per row
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned long long k2 = sstage[e * R + tid];
+        k = k2 > k ? k2 : k;
+      }
+    }
+    return k;
+  }
+
   template <int NT>
   __device__ void finish(const GemvArgs& a, Local& L, int w, int lane, int tid, unsigned long long* sstage,
                          int* sflag) const {
@@ -484,12 +528,8 @@ struct EpiArgmax {
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;
+    const unsigned long long k = grid_max<R>(tid, w, lane, sstage);
     if (tid < R) {
-      unsigned long long k = 0ull;
-      for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
-        const unsigned long long k2 = __ldcg(slots + static_cast<size_t>(c) * R + tid);
-        k = k2 > k ? k2 : k;
-      }
       const int s = tid >> 3, i = tid & 7;
       if (s < n_seq && i >= 1) {
         int B = block_len[s];

@@ -125,12 +125,8 @@ struct EpiArgmaxRows : public EpiArgmax<1> {
     }
     named_bar_sync(1, 128);
     if (!sflag[2]) return;
+    const unsigned long long k = grid_max<R>(tid, w, lane, sstage);
     if (tid < n_rows) {
-      unsigned long long k = 0ull;
-      for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
-        const unsigned long long k2 = __ldcg(slots + static_cast<size_t>(c) * R + tid);
-        k = k2 > k ? k2 : k;
-      }
       int out = -1;
       if (k == 0ull) set_status(status, DFLASH_DEV_NONFINITE);
       else out = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
