@@ -217,8 +217,23 @@ GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* statu
   return a;
 }
 
+// Grid of a GEMV: one CTA per SM at most, with the CTAs' unit ranges aligned
+// to the 64-row groups where the counts allow, so that no CTA meets a group
+// end in the middle of its range (a split group's fix-up, or a whole head's
+// epilogue, then waits for the CTA's own tail instead of stalling its
+// stream).  Groups <= SMs: every group is split into the same number of
+// parts; more groups than SMs: whole groups per CTA if the group count has a
+// divisor within 70 % of the SM count; otherwise plain stream-K over all SMs.
 int grid_for(const Model& m, const GemvArgs& a) {
-  int g = m.sm_count;
+  const int sm = m.sm_count;
+  const int groups = a.UPG > 0 ? a.U / a.UPG : 0;
+  if (groups >= 1 && groups <= sm) {
+    const int parts = sm / groups < a.UPG ? sm / groups : a.UPG;  // at least one unit per CTA
+    return groups * parts;
+  }
+  for (int g = sm; g * 10 >= sm * 7; --g)
+    if (g >= 1 && groups % g == 0) return g;
+  int g = sm;
   if (g > a.U) g = a.U;
   return g < 1 ? 1 : g;
 }
