@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 // O_c / l_c (FP16) and (m_c, l_c); the row's output is
 //   sum_c w_c O_c / l_c,   w_c = l_c 2^(m_c - mx) / sum_c' l_c' 2^(m_c' - mx).
 // Lane = (row i = lane / 4, 8 columns from (lane % 4) * 8); warp w takes
-// chunks w, w + 8, ...  Each thread issues the loads of up to 8 of its chunks
+// chunks w, w + 8, ...  Each thread issues the loads of up to 9 of its chunks
 // (partial values and (m, l)) at once and folds them into a running
 // (max, sum, sum of weighted rows); the 8 warps' results are then combined
 // through shared memory in a fixed order (deterministic).
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   float mw = -INFINITY, lw = 0.f, acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  constexpr int U = 8;
+  constexpr int U = 9;  // 8 warps x 9 loads cover the default 65 chunks in one round
   for (int c0 = warp; c0 < a.C; c0 += 8 * U) {
     uint4 v[U];
     float2 ml[U];
