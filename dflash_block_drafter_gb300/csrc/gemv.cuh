@@ -82,7 +82,7 @@ struct GemvGeom {
   // warpgroup hands its partial sums to the first through a double buffer.
   static constexpr int CWG = NT <= 4 ? 2 : 1;  // larger tiles keep 160 threads (register budget)
   static constexpr int SBUF = CWG > 1 ? 2 * 128 * NT * 16 : 0;  // [2][128 threads][NT][4] floats
-  static constexpr int RING_BUDGET = 190000 - SBUF;
+  static constexpr int RING_BUDGET = 200000 - SBUF;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;

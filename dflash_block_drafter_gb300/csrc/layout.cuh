@@ -46,7 +46,7 @@ struct Fmt;
 
 template <>
 struct Fmt<WT_BF16> {
-  static constexpr int CB = 4, SUBB = 1, CHUNK = 1024, STAGES = 8;
+  static constexpr int CB = 4, SUBB = 1, CHUNK = 1024, STAGES = 9;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 16384
   static constexpr bool kF16 = false;                   // activations bf16
 };
@@ -58,13 +58,13 @@ struct Fmt<WT_Q8_0> {
 };
 template <>
 struct Fmt<WT_Q4_0> {
-  static constexpr int CB = 8, SUBB = 2, CHUNK = 576, STAGES = 14;
+  static constexpr int CB = 8, SUBB = 2, CHUNK = 576, STAGES = 13;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 9216
   static constexpr bool kF16 = true;
 };
 template <>
 struct Fmt<WT_Q5_0> {
-  static constexpr int CB = 8, SUBB = 2, CHUNK = 704, STAGES = 12;
+  static constexpr int CB = 8, SUBB = 2, CHUNK = 704, STAGES = 11;
   static constexpr int UNIT = (CB / SUBB) * 4 * CHUNK;  // 11264
   static constexpr bool kF16 = true;
 };
