@@ -46,9 +46,9 @@ UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
 # DRAM bytes (read + write) of one LM-head launch at this workload, from the
-# ncu capture summarised in profiles/lm_head_argmax_full_bf16.md (6.210 TB/s x
-# 125.86 us).  Reset to None whenever the head kernel changes.
-HEAD_TRAFFIC_BYTES = 781.6e6
+# ncu capture summarised in profiles/lm_head_argmax_full_bf16.md (6.195 TB/s x
+# 126.11 us).  Reset to None whenever the head kernel changes.
+HEAD_TRAFFIC_BYTES = 781.3e6
 
 
 def load_peaks():
