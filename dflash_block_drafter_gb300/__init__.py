@@ -61,6 +61,7 @@ class DflashConfig(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
         ("vocab", ctypes.c_int32), ("n_taps", ctypes.c_int32), ("rope_theta", ctypes.c_float),
         ("norm_eps", ctypes.c_float), ("mask_token_id", ctypes.c_int32), ("weight_type", ctypes.c_int32),
+        ("attn_window", ctypes.c_int32),
     ]
 
 
@@ -231,10 +232,12 @@ def dflash_model_dequantize(model: int, which: int, out: int, stream: int = 0) -
 
 # ------------------------------------------------------------ marshalling aid
 def make_config(n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab, n_taps=5,
-                rope_theta=1e7, norm_eps=1e-6, mask_token_id=None, weight_type="bf16") -> DflashConfig:
+                rope_theta=1e7, norm_eps=1e-6, mask_token_id=None, weight_type="bf16",
+                attn_window=0) -> DflashConfig:
     wt = WEIGHT_TYPE_IDS[weight_type] if isinstance(weight_type, str) else int(weight_type)
     return DflashConfig(n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab, n_taps,
-                        rope_theta, norm_eps, vocab - 1 if mask_token_id is None else mask_token_id, wt)
+                        rope_theta, norm_eps, vocab - 1 if mask_token_id is None else mask_token_id, wt,
+                        attn_window)
 
 
 def make_weights(ptrs: Dict[str, int], n_layers: int) -> DflashWeights:

@@ -39,7 +39,7 @@ class DraftModel:
         self.device = torch.device(device)
         self.ccfg = make_config(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
                                 cfg.intermediate, cfg.vocab, cfg.n_taps, cfg.rope_theta, cfg.norm_eps,
-                                cfg.mask_token_id, cfg.weight_type)
+                                cfg.mask_token_id, cfg.weight_type, getattr(cfg, "attn_window", 0))
         with torch.cuda.device(self.device):
             src = {k: to_device(v, self.device) for k, v in ckpt.items()}
             ptrs = {k: t.data_ptr() for k, t in src.items()}

@@ -49,6 +49,7 @@ class DraftConfig:
     block: int = 4         # block rows B (anchor + B-1 mask rows)
     n_seq: int = 1
     fuse_per_cycle: int = 0  # positions fused each cycle (long-context workload)
+    attn_window: int = 0     # drafter attention window in positions (0: the whole context)
 
     @property
     def mask_token_id(self) -> int:

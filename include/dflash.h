@@ -76,7 +76,8 @@ enum dflash_status {
 enum dflash_device_error {
   DFLASH_DEV_NONFINITE = 1,   /* a logit or hidden value was NaN/Inf ("non-finite refusal") */
   DFLASH_DEV_BAD_TOKEN = 2,   /* anchor token id outside [0, vocab) */
-  DFLASH_DEV_CAPACITY = 4,    /* p + block_len > capacity, or a fuse position outside [0, capacity) */
+  DFLASH_DEV_CAPACITY = 4,    /* p + block_len > capacity, or a fuse position outside [0, capacity)
+                                 (ring states, attn_window > 0: a negative position) */
   DFLASH_DEV_BAD_BLOCK = 8,   /* a block_len outside [2, 8] (clamped) */
   DFLASH_DEV_TIMEOUT = 16     /* a pipeline wait exceeded its time limit (should never happen) */
 };
@@ -113,6 +114,15 @@ typedef struct dflash_config {
   float norm_eps;        /* RMSNorm epsilon (1e-6)                     */
   int32_t mask_token_id; /* token of the block's mask rows             */
   int32_t weight_type;   /* dflash_weight_type of the 36 backbone matrices */
+  int32_t attn_window;   /* 0: a block at p attends over positions [0, p + B)
+                          * and position pos lives in cell pos (< capacity).
+                          * W > 0: drafter attention window ("#1426 ...",
+                          * "Additional constraints": 32768 cells by default
+                          * there): the block attends over positions
+                          * [max(0, p + B - W), p + B), and the state's cells
+                          * form a ring, position pos living in cell
+                          * pos mod capacity (capacity >= W, a multiple of
+                          * 128), so positions may grow without bound.    */
 } dflash_config;
 
 /* Per-layer tensors; names follow the pages' stage names.  Matrices are
@@ -181,7 +191,10 @@ size_t dflash_model_device_bytes(const dflash_model* model);
  * per-layer FP16 K/V of `capacity` positions ("#1426 ...", "Owned DFlash K/V
  * state": five independent draft-layer states in drafter-owned arenas), plus
  * the workspace of one draft pass over n_slots sequences.  Cells start as
- * zeros.  1 <= n_slots <= DFLASH_MAX_SLOTS, capacity >= DFLASH_MAX_BLOCK.
+ * zeros.  1 <= n_slots <= DFLASH_MAX_SLOTS, capacity >= DFLASH_MAX_BLOCK;
+ * with a model attention window W > 0, capacity >= W and capacity % 128 == 0
+ * (else DFLASH_ERR_UNSUPPORTED): the cells are a ring, position pos in cell
+ * pos mod capacity.
  * Layout of the K (and V) arena, FP16: [layer][slot][kv_head][capacity][d]. */
 int dflash_state_create(const dflash_model* model, int32_t n_slots, int32_t capacity,
                         dflash_state** out);
@@ -191,7 +204,8 @@ size_t dflash_state_device_bytes(const dflash_state* state);
 /* Step (1): fuse n newly committed positions of one slot.
  *   taps:      [n, n_taps*H] BF16 (uint16 bits), the five taps of a position
  *              concatenated in tap order.
- *   positions: [n] int32, distinct, each in [0, capacity).
+ *   positions: [n] int32, distinct, each in [0, capacity) (ring states: >= 0,
+ *              and distinct modulo capacity).
  * For every position and layer l: k = RoPE(rmsnorm_head(W_k,l h), pos) and
  * v = W_v,l h are rounded to FP16 and written to the slot's cells,
  * overwriting what was there ("Position-addressed context/KV cells are
@@ -216,7 +230,9 @@ int dflash_fuse_context(const dflash_model* model, dflash_state* state, int32_t 
  * The pass writes each layer's block K/V into the slot's cells [p, p + B)
  * (FP16) and attends over cells [0, p + B), non-causally; no rollback is
  * needed because later fusion overwrites those cells ("Rejected candidate
- * cells do not need drafter-side rollback"). */
+ * cells do not need drafter-side rollback").  With an attention window W
+ * (ring state) the cells are those of positions [max(0, p + B - W), p + B),
+ * each at pos mod capacity; those positions must have been fused. */
 int dflash_draft_block(const dflash_model* model, dflash_state* state, int32_t n_seq,
                        const int32_t* anchor_tok, const int32_t* anchor_pos,
                        const int32_t* block_len, int32_t* drafts, float* final_hidden,
@@ -239,13 +255,16 @@ int dflash_accept(const int32_t* drafts, const int32_t* target_ids, const int32_
                   int32_t n_seq, int32_t max_block_len, int32_t* accept_len,
                   int32_t* next_anchor, int32_t* anchor_pos_inout, dflash_stream_t stream);
 
-/* Debug / parity: copy cells [pos0, pos0 + n) of one slot and layer out as
- * float (exact widening of the FP16 cells), k_out/v_out [n_kv, n, d] device
- * buffers (either may be NULL). */
+/* Debug / parity: copy the cells of positions [pos0, pos0 + n) of one slot
+ * and layer out as float (exact widening of the FP16 cells), k_out/v_out
+ * [n_kv, n, d] device buffers (either may be NULL).  Ring states (attention
+ * window > 0) address position pos at cell pos mod capacity and take any
+ * pos0 >= 0 with n <= capacity. */
 int dflash_state_read_kv(const dflash_state* state, int32_t slot, int32_t layer, int32_t pos0,
                          int32_t n, float* k_out, float* v_out, dflash_stream_t stream);
 
-/* Set cells [pos0, pos0 + n) of one slot and layer from FP16 (uint16 bits)
+/* Set the cells of positions [pos0, pos0 + n) (ring states: pos mod
+ * capacity, as for dflash_state_read_kv) of one slot and layer from FP16 (uint16 bits)
  * arrays [n_kv, n, d] on the device (pre-filled contexts). */
 int dflash_state_write_kv(dflash_state* state, int32_t slot, int32_t layer, int32_t pos0,
                           int32_t n, const uint16_t* k_in, const uint16_t* v_in,

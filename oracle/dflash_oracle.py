@@ -32,6 +32,11 @@ Readings where the pages are silent (each listed in the design doc):
     fusing a committed position later overwrites its cell ([#1426]
     "Speculative decode integration": rejected cells need no rollback).
   * Drafts are the argmax of rows 1..B-1 (lowest id on ties).
+  * Attention window W > 0 ([#1426] "Additional constraints": the drafter
+    attention window defaults to 32768 cells; [#3322] keeps 32768 resident
+    cells for a 262144-token context in physical rings): the block at p
+    attends over positions [max(0, p + B - W), p + B), and the state keeps
+    position pos in cell pos mod capacity.
   * Accept length n = longest prefix with draft_j == target_j; the bonus
     token is target_n.
 
@@ -203,42 +208,63 @@ class Model:
 class State:
     """Per-layer, position-addressed FP16 context K/V of one sequence
     ([#1426] "Owned DFlash K/V state": five independent per-layer states,
-    FP16 K/V).  K[l], V[l]: float16 [n_kv, capacity, d].  ``valid`` tracks
-    which cells have been written; attention refuses to read an unwritten
-    cell (the pages' parity harness fails hard on invalid cells, [#1426]
-    "Parity validation")."""
+    FP16 K/V).  K[l], V[l]: float16 [n_kv, capacity, d].  ``held[l][c]`` is
+    the position cell c holds (-1: never written); attention refuses to read
+    a position whose cell does not hold it (the pages' parity harness fails
+    hard on invalid cells, [#1426] "Parity validation").  Without an
+    attention window position pos is cell pos (pos < capacity); with one
+    (cfg.attn_window > 0) the cells are a ring and pos is cell pos mod
+    capacity, so a later position overwrites the cell of an earlier one."""
 
     def __init__(self, cfg, capacity: int):
         self.cfg = cfg
         self.capacity = capacity
+        self.window = int(getattr(cfg, "attn_window", 0) or 0)
+        if self.window > capacity:
+            raise ValueError("the attention window does not fit the state's cells")
         shape = (cfg.n_kv_heads, capacity, cfg.head_dim)
         self.K = [np.zeros(shape, dtype=np.float16) for _ in range(cfg.n_layers)]
         self.V = [np.zeros(shape, dtype=np.float16) for _ in range(cfg.n_layers)]
-        self.valid = [np.zeros(capacity, dtype=bool) for _ in range(cfg.n_layers)]
+        self.held = [np.full(capacity, -1, dtype=np.int64) for _ in range(cfg.n_layers)]
+
+    def cells(self, pos) -> np.ndarray:
+        """Cell index of each position."""
+        pos = np.asarray(pos, dtype=np.int64)
+        if pos.size and pos.min() < 0:
+            raise IndexError("negative position")
+        if self.window > 0:
+            return pos % self.capacity
+        if pos.size and pos.max() >= self.capacity:
+            raise IndexError("position outside the state's capacity")
+        return pos
 
     def fill(self, kv_pairs, n_pos: int) -> None:
-        """Set cells [0, n_pos) from float16 arrays [n_kv, n_pos, d]."""
+        """Set positions [0, n_pos) from float16 arrays [n_kv, n_pos, d]."""
+        if n_pos > self.capacity:
+            raise IndexError("more positions than cells")
         for l, (k, v) in enumerate(kv_pairs):
             self.K[l][:, :n_pos, :] = k
             self.V[l][:, :n_pos, :] = v
-            self.valid[l][:n_pos] = True
+            self.held[l][:n_pos] = np.arange(n_pos)
 
     def write(self, l: int, pos, k, v) -> None:
         """Round k, v ([n, n_kv, d]) to FP16 and store them at positions pos."""
         pos = np.asarray(pos, dtype=np.int64)
-        if pos.size and (pos.min() < 0 or pos.max() >= self.capacity):
-            raise IndexError("position outside the state's capacity")
-        self.K[l][:, pos, :] = round_f16(k).transpose(1, 0, 2)
-        self.V[l][:, pos, :] = round_f16(v).transpose(1, 0, 2)
-        self.valid[l][pos] = True
+        c = self.cells(pos)
+        self.K[l][:, c, :] = round_f16(k).transpose(1, 0, 2)
+        self.V[l][:, c, :] = round_f16(v).transpose(1, 0, 2)
+        self.held[l][c] = pos
 
-    def keys(self, l: int, n: int):
-        """float64 K, V for cells [0, n), as [n, n_kv, d]."""
-        if not self.valid[l][:n].all():
-            bad = int(np.argmin(self.valid[l][:n]))
-            raise ValueError(f"layer {l}: K/V cell {bad} read before it was written")
-        k = self.K[l][:, :n, :].astype(np.float64).transpose(1, 0, 2)
-        v = self.V[l][:, :n, :].astype(np.float64).transpose(1, 0, 2)
+    def keys(self, l: int, hi: int, lo: int = 0):
+        """float64 K, V of positions [lo, hi), as [hi - lo, n_kv, d]."""
+        pos = np.arange(lo, hi, dtype=np.int64)
+        c = self.cells(pos)
+        held = self.held[l][c]
+        if not np.array_equal(held, pos):
+            bad = int(pos[np.argmax(held != pos)])
+            raise ValueError(f"layer {l}: K/V of position {bad} read before it was written")
+        k = self.K[l][:, c, :].astype(np.float64).transpose(1, 0, 2)
+        v = self.V[l][:, c, :].astype(np.float64).transpose(1, 0, 2)
         return k, v
 
 
@@ -301,7 +327,8 @@ def draft_block(model: Model, state: State, anchor_tok: int, anchor_pos: int,
 
     Per layer, in the stage order of [#1426] "Parity validation":
       xn = rmsnorm(x); q, k, v = W xn; q, k per-head normed; RoPE at p + i;
-      block K/V written to cells [p, p+B); attention over cells [0, p+B);
+      block K/V written to positions [p, p+B); attention over positions
+      [lo, p+B), lo = 0 or, with an attention window W, max(0, p + B - W);
       x += W_o attn; x += W_down(silu(W_gate xn2) * W_up xn2).
     Then the final norm, the LM head on rows 1..B-1 and their argmax.
     """
@@ -309,8 +336,9 @@ def draft_block(model: Model, state: State, anchor_tok: int, anchor_pos: int,
     B, p = int(block_len), int(anchor_pos)
     if not (2 <= B):
         raise ValueError("block_len must be >= 2")
-    if p + B > state.capacity:
+    if state.window == 0 and p + B > state.capacity:
         raise IndexError("anchor_pos + block_len exceeds the state's capacity")
+    lo = max(0, p + B - state.window) if state.window > 0 else 0
     d, nq, nkv = cfg.head_dim, cfg.n_q_heads, cfg.n_kv_heads
     toks = np.full(B, cfg.mask_token_id, dtype=np.int64)
     toks[0] = anchor_tok
@@ -325,7 +353,7 @@ def draft_block(model: Model, state: State, anchor_tok: int, anchor_pos: int,
         q = rope_neox(q, pos[:, None], cfg.rope_theta)
         k, v = project_kv(model, l, xn, pos)
         state.write(l, pos, k, v)
-        kc, vc = state.keys(l, p + B)
+        kc, vc = state.keys(l, p + B, lo)
         a = attention(q, kc, vc, 1.0 / math.sqrt(d))
         x = x + a.reshape(B, nq * d) @ model.mat(pre + "wo").T
         if trace:

@@ -422,7 +422,7 @@ def test_context_keys_rotated_at_their_position():
         u1 = O.rope_neox(st1.K[l][:, S:].astype(np.float64), -(S + p)[None, :], cfg.rope_theta)
         assert np.allclose(u0, u1, atol=4e-3)
         assert np.array_equal(st0.V[l], st1.V[l][:, S:])
-        assert st1.valid[l][S:].all() and not st1.valid[l][:S].any()
+        assert np.array_equal(st1.held[l][S:], S + p) and (st1.held[l][:S] == -1).all()
 
 
 def test_pass_position_shift_invariance():
@@ -445,7 +445,7 @@ def test_pass_position_shift_invariance():
     view = O.State(cfg, n + 8)
     view.K = [k[:, S:] for k in st1.K]
     view.V = [v[:, S:] for v in st1.V]
-    view.valid = [vv[S:] for vv in st1.valid]
+    view.held = [hh[S:] - S for hh in st1.held]
     orig = O.rope_neox
     O.rope_neox = lambda x, pos, theta: orig(x, np.asarray(pos) + S, theta)
     try:
@@ -457,3 +457,87 @@ def test_pass_position_shift_invariance():
     sure = r0.top2_gap > 1e-2
     assert sure.any()
     assert np.array_equal(r0.drafts[sure], r1.drafts[sure])
+
+
+# ---------------------------------------------------------------------------
+# attention window and ring-addressed cells
+# ---------------------------------------------------------------------------
+
+def _window_setup(seed, n, W, capacity, positions=None):
+    cfg = _tiny(attn_window=W)
+    ck = synth.make_checkpoint(cfg, seed=seed)
+    m = O.Model(cfg, ck)
+    taps = synth.make_taps(cfg, n, seed=seed)
+    st = O.State(cfg, capacity)
+    O.fuse_context(m, st, taps, np.arange(n) if positions is None else positions)
+    return cfg, m, st, taps
+
+
+def test_window_that_covers_the_context_changes_nothing():
+    """A window at least as long as p + B attends to exactly the positions of
+    the plain pass: results bit-identical to no window."""
+    n, B = 40, 4
+    cfg0 = _tiny()
+    ck = synth.make_checkpoint(cfg0, seed=31)
+    taps = synth.make_taps(cfg0, n, seed=31)
+    res = []
+    for W in (0, n + B, 128):
+        cfg = cfg0.with_(attn_window=W)
+        m = O.Model(cfg, ck)
+        st = O.State(cfg, 128)
+        O.fuse_context(m, st, taps, np.arange(n))
+        res.append(O.draft_block(m, st, 5, n, B))
+    for r in res[1:]:
+        assert np.array_equal(r.final_hidden, res[0].final_hidden)
+        assert np.array_equal(r.drafts, res[0].drafts)
+
+
+def test_window_reads_exactly_the_last_w_positions():
+    """With W < p + B the pass depends on positions [p + B - W, p + B) only:
+    replacing every K/V cell of an older position by large noise leaves the
+    result bit-identical, while replacing the one position just inside the
+    window changes it (so the boundary is exact, not off by one)."""
+    n, B, W = 48, 4, 20
+    cfg, m, st, _ = _window_setup(32, n, W, 64)
+    ref = O.draft_block(m, st, 5, n, B)
+    lo = n + B - W
+    rng = np.random.default_rng(32)
+    noisy = O.State(cfg, 64)
+    noisy.K = [k.copy() for k in st.K]
+    noisy.V = [v.copy() for v in st.V]
+    noisy.held = [h.copy() for h in st.held]
+    for l in range(cfg.n_layers):
+        noisy.K[l][:, :lo, :] = rng.normal(0, 50, noisy.K[l][:, :lo, :].shape).astype(np.float16)
+        noisy.V[l][:, :lo, :] = rng.normal(0, 50, noisy.V[l][:, :lo, :].shape).astype(np.float16)
+    out = O.draft_block(m, noisy, 5, n, B)
+    assert np.array_equal(out.final_hidden, ref.final_hidden)
+    inside = O.State(cfg, 64)
+    inside.K = [k.copy() for k in st.K]
+    inside.V = [v.copy() for v in st.V]
+    inside.held = [h.copy() for h in st.held]
+    for l in range(cfg.n_layers):
+        inside.V[l][:, lo, :] = rng.normal(0, 50, inside.V[l][:, lo, :].shape).astype(np.float16)
+    assert not np.array_equal(O.draft_block(m, inside, 5, n, B).final_hidden, ref.final_hidden)
+
+
+def test_ring_cells_match_position_addressed_cells():
+    """Fusing positions past the capacity of a ring state overwrites the
+    cells of older positions (pos mod capacity); as long as the window fits
+    the ring, the pass equals the same windowed pass over a state large
+    enough to keep every position in its own cell."""
+    n, B, W, C = 200, 4, 96, 128
+    cfg, m, ring, taps = _window_setup(33, n, W, C)
+    big = O.State(cfg.with_(attn_window=0), 256)
+    big.window = W  # the same window over position-addressed cells
+    O.fuse_context(m, big, taps, np.arange(n))
+    r_ring = O.draft_block(m, ring, 7, n, B)
+    r_big = O.draft_block(m, big, 7, n, B)
+    assert np.array_equal(r_ring.final_hidden, r_big.final_hidden)
+    assert np.array_equal(r_ring.drafts, r_big.drafts)
+    # position 0 was evicted by position C: reading it fails hard
+    with pytest.raises(ValueError):
+        ring.keys(0, 1, 0)
+    # cell n % C - 1 holds the last fused position, cell n % C the block's
+    # anchor position written by the pass, cell (n + B) % C an older position
+    assert ring.held[0][n % C - 1] == n - 1 and ring.held[0][n % C] == n
+    assert ring.held[0][(n + B) % C] == n + B - C
