@@ -330,6 +330,7 @@ int dflash_config_check(const dflash_config* c) {
   if ((c->n_kv_heads * c->head_dim) % 64) return DFLASH_ERR_UNSUPPORTED;
   if (c->n_taps < 1 || c->n_taps > 64) return DFLASH_ERR_UNSUPPORTED;
   if (c->vocab < 2) return DFLASH_ERR_UNSUPPORTED;
+  if (c->attn_window < 0) return DFLASH_ERR_INVALID_ARG;
   if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return DFLASH_ERR_INVALID_ARG;
   if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta)) return DFLASH_ERR_INVALID_ARG;
   if (!(c->norm_eps >= 0.f) || !std::isfinite(c->norm_eps)) return DFLASH_ERR_INVALID_ARG;
@@ -465,6 +466,9 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate;
   const long long arena_rows = static_cast<long long>(L) * n_slots * nkv * capacity;
   if (arena_rows > 0x7fffffffLL) return DFLASH_ERR_CAPACITY;
+  // a ring of cells (attention window) must hold the window and keep every
+  // 128-position super-tile of the attention in one contiguous run of cells
+  if (m->cfg.attn_window > 0 && (capacity < m->cfg.attn_window || capacity % 128)) return DFLASH_ERR_UNSUPPORTED;
   dflash_state* s = new (std::nothrow) dflash_state();
   if (!s) return DFLASH_ERR_OUT_OF_MEMORY;
   auto fail = [&](int rc) {
@@ -490,7 +494,9 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
     // holds 225 KB of shared memory and 512 TMEM columns); buffers sized for
     // up to 4 CTAs' worth of chunks per SM (and at most 512 chunks, the merge
     // kernel's limit)
-    const long long tiles = (capacity + 127) / 128;
+    // positions one block attends to: the window (plus alignment), else the whole state
+    const long long span = m->cfg.attn_window > 0 ? static_cast<long long>(m->cfg.attn_window) + 128 : capacity;
+    const long long tiles = (span + 127) / 128;
     const long long per = static_cast<long long>(n_slots) * nkv;
     long long cmax = (4LL * m->sm_count) / per;
     cmax = cmax < 1 ? 1 : (cmax > 512 ? 512 : cmax);
@@ -633,6 +639,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       e.Vst = s->V;
       e.n_slots = s->n_slots;
       e.cap = s->capacity;
+      e.ring = c.attn_window > 0;
       e.slot = slot;
       e.positions = positions + base;
       e.n_valid = rows;
@@ -674,7 +681,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   };
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
-                 s->capacity, status, nullptr, nullptr, nullptr, 0};
+                 s->capacity, c.attn_window > 0, status, nullptr, nullptr, nullptr, 0};
     if (packed) {
       ea.xn = s->xn;
       ea.ku = ku_of(wt);
@@ -722,6 +729,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       e.layer = l;
       e.n_slots = s->n_slots;
       e.cap = s->capacity;
+      e.ring = c.attn_window > 0;
       e.n_seq = n_seq;
       e.anchor_pos = anchor_pos;
       e.block_len = block_len;
@@ -841,16 +849,17 @@ int dflash_state_read_kv(const dflash_state* s, int32_t slot, int32_t layer, int
                          float* v_out, dflash_stream_t stream) {
   if (!s) return DFLASH_ERR_INVALID_ARG;
   const dflash_config& c = s->model->cfg;
-  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 ||
-      static_cast<long long>(pos0) + n > s->capacity)
+  const bool ring = c.attn_window > 0;
+  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || n > s->capacity ||
+      (!ring && static_cast<long long>(pos0) + n > s->capacity))
     return DFLASH_ERR_INVALID_ARG;
   const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (k_out)
-    TRY(check_gemv(launch_kv_copy(false, s->K + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, k_out, nullptr, st),
+    TRY(check_gemv(launch_kv_copy(false, s->K + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, k_out, nullptr, st),
                    "read k"));
   if (v_out)
-    TRY(check_gemv(launch_kv_copy(false, s->V + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, v_out, nullptr, st),
+    TRY(check_gemv(launch_kv_copy(false, s->V + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, v_out, nullptr, st),
                    "read v"));
   return DFLASH_OK;
 }
@@ -859,16 +868,17 @@ int dflash_state_write_kv(dflash_state* s, int32_t slot, int32_t layer, int32_t 
                           const uint16_t* v_in, dflash_stream_t stream) {
   if (!s) return DFLASH_ERR_INVALID_ARG;
   const dflash_config& c = s->model->cfg;
-  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 ||
-      static_cast<long long>(pos0) + n > s->capacity)
+  const bool ring = c.attn_window > 0;
+  if (slot < 0 || slot >= s->n_slots || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || n > s->capacity ||
+      (!ring && static_cast<long long>(pos0) + n > s->capacity))
     return DFLASH_ERR_INVALID_ARG;
   const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (k_in)
-    TRY(check_gemv(launch_kv_copy(true, s->K + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, nullptr, k_in, st),
+    TRY(check_gemv(launch_kv_copy(true, s->K + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, nullptr, k_in, st),
                    "write k"));
   if (v_in)
-    TRY(check_gemv(launch_kv_copy(true, s->V + off, s->capacity, c.head_dim, c.n_kv_heads, pos0, n, nullptr, v_in, st),
+    TRY(check_gemv(launch_kv_copy(true, s->V + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, nullptr, v_in, st),
                    "write v"));
   return DFLASH_OK;
 }

@@ -30,6 +30,8 @@ struct AttnArgs {
   int out_f16;            // 1: one FP16 plane; 0: BF16 hi and lo planes
   int out_rows, out_ku;   // chunked layout: rows R of the pass and inputs per unit
   int layer, n_slots, n_kv, n_q, gq, cap, C, n_seq;
+  int window;             // 0: keys [0, p + B), cell = position; W > 0: keys
+                          // [max(0, p + B - W), p + B) in a ring, cell = position mod cap
   int32_t* status;
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
@@ -180,13 +182,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   if (tid == 0) DFLASH_ATTN_STAMP(0);
 
-  // key range of this chunk, in super-tiles
+  // key positions [lo, T), in super-tiles of kTcKS positions from `kbase`
+  // (lo rounded down to a super-tile); with a window the cells are a ring and
+  // a super-tile (cap % kTcKS == 0) is one contiguous run of cells
   const int p = a.anchor_pos[s];
   int B = a.block_len[s];
   B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
   int T = p + B;
-  T = T < 0 ? 0 : (T > a.cap ? a.cap : T);
-  const int nst_all = (T + kTcKS - 1) / kTcKS;
+  int lo = 0;
+  if (a.window > 0) {
+    T = T < 0 ? 0 : T;
+    lo = T - a.window < 0 ? 0 : T - a.window;
+  } else {
+    T = T < 0 ? 0 : (T > a.cap ? a.cap : T);
+  }
+  const int kbase = lo - lo % kTcKS;
+  const int nst_all = (T - kbase + kTcKS - 1) / kTcKS;
   const int spc = (nst_all + a.C - 1) / a.C;
   const int st0 = c * spc;
   const int st1 = min(nst_all, st0 + spc);
@@ -224,23 +235,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       prefetch_tensormap(&a.qmap);
       prefetch_tensormap(&a.kmap);
       prefetch_tensormap(&a.vmap);
+      auto tile_row = [&](int j) {
+        const int pos = kbase + (st0 + j) * kTcKS;
+        return row0 + (a.window > 0 ? pos % a.cap : pos);
+      };
       auto issue_k = [&](int j) {
-        const int y = row0 + (st0 + j) * kTcKS;
+        const int y = tile_row(j);
         mbar_arrive_expect_tx(kfull, 2 * Geo::TILE_BYTES);
         for (int t = 0; t < 2; ++t)
           for (int b = 0; b < Geo::BOXES; ++b)
             tma_load_2d(sk + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.kmap, b * 64, y + t * kTcKT, kfull);
       };
       auto issue_v = [&](int j) {
-        const int y = row0 + (st0 + j) * kTcKS;
+        const int y = tile_row(j);
         mbar_arrive_expect_tx(vfull, 2 * Geo::TILE_BYTES);
         for (int t = 0; t < 2; ++t)
           for (int b = 0; b < Geo::BOXES; ++b)
             tma_load_2d(sv + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.vmap, b * 64, y + t * kTcKT, vfull);
       };
-      // A first super-tile wholly inside the fused context [0, p) does not
-      // depend on the previous kernel (which writes the block cells).
-      const bool early = (st0 + 1) * kTcKS <= p;
+      // A first super-tile wholly before the block's positions does not
+      // depend on the previous kernel (which writes the block cells; in a
+      // ring they cannot be the cells of a position inside the window).
+      const bool early = kbase + (st0 + 1) * kTcKS <= p;
       if (early) {
         issue_k(0);
         issue_v(0);
@@ -342,17 +358,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b]);
-      // keys of this slice before T (the last super-tile's tail takes no weight)
-      const int nk = min(T - (st0 + j) * kTcKS, kTcKS) - cs * 32;
+      // keys e of this slice with lo <= position < T take weight (the last
+      // super-tile's tail and, with a window, the first one's head take none)
+      const int spos = kbase + (st0 + j) * kTcKS + cs * 32;
+      const int khi = min(T - spos, 32), klo = max(lo - spos, 0);
+      const bool full_slice = klo == 0 && khi >= 32;
       float mx = -INFINITY;
       if (live) {
-        if (nk >= 32) {
+        if (full_slice) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (e < nk) mx = fmaxf(mx, __uint_as_float(r[e]));
+            if (e >= klo && e < khi) mx = fmaxf(mx, __uint_as_float(r[e]));
         }
       }
       if (tid == 64 && j == 0) DFLASH_ATTN_STAMP(2);
@@ -378,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       float ls = 0.f;
       if (live) {
         uint32_t pk[16];
-        if (nk >= 32) {
+        if (full_slice) {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), LOG2E, -base));
@@ -389,8 +408,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         } else {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = e < nk ? ex2_approx(fmaf(__uint_as_float(r[e]), LOG2E, -base)) : 0.f;
-            const float p1 = e + 1 < nk ? ex2_approx(fmaf(__uint_as_float(r[e + 1]), LOG2E, -base)) : 0.f;
+            const float p0 =
+                (e >= klo && e < khi) ? ex2_approx(fmaf(__uint_as_float(r[e]), LOG2E, -base)) : 0.f;
+            const float p1 =
+                (e + 1 >= klo && e + 1 < khi) ? ex2_approx(fmaf(__uint_as_float(r[e + 1]), LOG2E, -base)) : 0.f;
             ls += p0 + p1;
             pk[e >> 1] = pack_f16x2(p0, p1);
           }
@@ -690,6 +711,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.n_q = c.n_q_heads;
   a.gq = c.n_q_heads / c.n_kv_heads;
   a.cap = st.capacity;
+  a.window = c.attn_window;
   a.C = st.attn_chunks;
   a.n_seq = n_seq;
   a.status = status;

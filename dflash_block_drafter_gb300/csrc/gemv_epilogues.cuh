@@ -226,6 +226,7 @@ struct EpiHeads {
   __half* Kst;
   __half* Vst;
   int layer, n_slots, cap;
+  int ring;              // cells form a ring (attention window): position pos in cell pos mod cap
   int n_seq;             // mode 0: slots in this pass
   const int32_t* anchor_pos;
   const int32_t* block_len;
@@ -316,7 +317,7 @@ struct EpiHeads {
               int B = block_len[sl[q]];
               B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
               pos[q] = anchor_pos[sl[q]] + i;
-              write_state[q] = (i < B) && pos[q] >= 0 && pos[q] < cap;
+              write_state[q] = (i < B) && pos[q] >= 0 && (ring || pos[q] < cap);
             }
           } else {
             sl[q] = slot;
@@ -324,7 +325,7 @@ struct EpiHeads {
               use[q] = false;
             } else {
               pos[q] = positions[n];
-              write_state[q] = pos[q] >= 0 && pos[q] < cap;
+              write_state[q] = pos[q] >= 0 && (ring || pos[q] < cap);
               if (!write_state[q] && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
             }
           }
@@ -339,7 +340,8 @@ struct EpiHeads {
       for (int q = 0; q < 2; ++q) {
         if (!use[q]) continue;
         const int n = n0 + 4 * q;
-        const size_t cell = ((static_cast<size_t>((l * n_slots + sl[q]) * n_kv + kvh) * cap) + pos[q]) * d;
+        const size_t cell =
+            ((static_cast<size_t>((l * n_slots + sl[q]) * n_kv + kvh) * cap) + (ring ? pos[q] % cap : pos[q])) * d;
         if (kind == 2) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)

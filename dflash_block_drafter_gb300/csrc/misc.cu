@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
       if (B < DFLASH_MIN_BLOCK || B > DFLASH_MAX_BLOCK) set_status(a.status, DFLASH_DEV_BAD_BLOCK);
       const int Bc = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
       const int p = a.anchor_pos[s];
-      if (p < 0 || static_cast<long long>(p) + Bc > a.cap) set_status(a.status, DFLASH_DEV_CAPACITY);
+      if (p < 0 || (!a.ring && static_cast<long long>(p) + Bc > a.cap)) set_status(a.status, DFLASH_DEV_CAPACITY);
     }
   }
   const uint16_t* er = a.embed + static_cast<size_t>(tok) * a.H;
@@ -331,7 +331,12 @@ cudaError_t launch_accept(const int32_t* drafts, const int32_t* tgt, const int32
 }
 
 // ------------------------------------------------------- K/V import/export
-__global__ void kv_read_kernel(const __half* __restrict__ cells, int cap, int d, int n_kv, int pos0, int n,
+// Cell of position pos: pos itself, or pos mod cap in a ring of cells.
+__device__ __forceinline__ size_t kv_cell(int pos, int cap, int ring) {
+  return static_cast<size_t>(ring ? pos % cap : pos);
+}
+
+__global__ void kv_read_kernel(const __half* __restrict__ cells, int cap, int ring, int d, int n_kv, int pos0, int n,
                                float* __restrict__ out) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(n_kv) * n * d;
@@ -339,10 +344,10 @@ __global__ void kv_read_kernel(const __half* __restrict__ cells, int cap, int d,
   const int h = static_cast<int>(idx / (static_cast<long long>(n) * d));
   const long long rem = idx - static_cast<long long>(h) * n * d;
   const int i = static_cast<int>(rem / d), k = static_cast<int>(rem % d);
-  out[idx] = __half2float(cells[(static_cast<size_t>(h) * cap + pos0 + i) * d + k]);
+  out[idx] = __half2float(cells[(static_cast<size_t>(h) * cap + kv_cell(pos0 + i, cap, ring)) * d + k]);
 }
 
-__global__ void kv_write_kernel(__half* __restrict__ cells, int cap, int d, int n_kv, int pos0, int n,
+__global__ void kv_write_kernel(__half* __restrict__ cells, int cap, int ring, int d, int n_kv, int pos0, int n,
                                 const uint16_t* __restrict__ in) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(n_kv) * n * d;
@@ -350,17 +355,17 @@ __global__ void kv_write_kernel(__half* __restrict__ cells, int cap, int d, int 
   const int h = static_cast<int>(idx / (static_cast<long long>(n) * d));
   const long long rem = idx - static_cast<long long>(h) * n * d;
   const int i = static_cast<int>(rem / d), k = static_cast<int>(rem % d);
-  cells[(static_cast<size_t>(h) * cap + pos0 + i) * d + k] = __ushort_as_half(in[idx]);
+  cells[(static_cast<size_t>(h) * cap + kv_cell(pos0 + i, cap, ring)) * d + k] = __ushort_as_half(in[idx]);
 }
 
-cudaError_t launch_kv_copy(bool write, __half* cells, int cap, int d, int n_kv, int pos0, int n, float* out,
+cudaError_t launch_kv_copy(bool write, __half* cells, int cap, bool ring, int d, int n_kv, int pos0, int n, float* out,
                            const uint16_t* in, cudaStream_t st) {
   const long long total = static_cast<long long>(n_kv) * n * d;
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
-  if (write) kv_write_kernel<<<blocks, threads, 0, st>>>(cells, cap, d, n_kv, pos0, n, in);
-  else kv_read_kernel<<<blocks, threads, 0, st>>>(cells, cap, d, n_kv, pos0, n, out);
+  if (write) kv_write_kernel<<<blocks, threads, 0, st>>>(cells, cap, ring, d, n_kv, pos0, n, in);
+  else kv_read_kernel<<<blocks, threads, 0, st>>>(cells, cap, ring, d, n_kv, pos0, n, out);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,12 @@ def test_config_check_rejects(lib):
     c = _cfg()
     c.weight_type = 7
     assert D.dflash_config_check(c) == D.DFLASH_ERR_UNSUPPORTED
+    c = _cfg()
+    c.attn_window = -1
+    assert D.dflash_config_check(c) == D.DFLASH_ERR_INVALID_ARG
+    c = _cfg()
+    c.attn_window = 32768  # the pages' default drafter window is a valid model setting
+    assert D.dflash_config_check(c) == D.DFLASH_OK
     assert lib.dflash_config_check(None) == D.DFLASH_ERR_INVALID_ARG
 
 
