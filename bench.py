@@ -70,7 +70,9 @@ def algorithmic_bytes(cfg, ctx: int, B: int, n_fuse: int) -> dict:
     layer_params = sum(a * b for n, (a, b) in shapes.items() if n != "fc")
     kv_params = sum(a * b for n, (a, b) in shapes.items() if n.endswith((".wk", ".wv")))
     head = cfg.vocab * H * 2
-    kv_read = L * 2 * nkv * (ctx + B) * d * 2
+    window = getattr(cfg, "attn_window", 0)
+    attended = min(ctx + B, window) if window > 0 else ctx + B
+    kv_read = L * 2 * nkv * attended * d * 2
     kv_write_block = L * 2 * nkv * B * d * 2
     draft = layer_params * bpw + head + kv_read + kv_write_block + B * H * 2
     fuse = (shapes["fc"][0] * shapes["fc"][1] + kv_params) * bpw + n_fuse * cfg.tap_width * 2 \
@@ -214,12 +216,37 @@ def run_reference(args, rank: int):
 
 
 def config_block(cfg):
-    return {"workload": "DFlash draft cycle: fuse 8 committed positions + draft an 8-row block at p = 8192 "
-                        "+ greedy accept; 5 layers, hidden 2560, 24Q/2KV x 256, MLP 7680, vocab 151936, "
-                        f"{cfg.weight_type.upper()} backbone",
-            "ctx": cfg.ctx, "block": cfg.block, "fuse_per_step": FUSE_PER_STEP, "weight_type": cfg.weight_type,
-            "sequences_per_gpu": 1,
-            "l2": "inputs larger than L2: every step streams ~1.9 GB of weights and K/V (L2 is 129 MB)"}
+    window = getattr(cfg, "attn_window", 0)
+    win = (f", attention window {window} over a ring of {state_capacity(cfg)} cells" if window > 0 else "")
+    block = {"workload": f"DFlash draft cycle: fuse 8 committed positions + draft an 8-row block at p = {cfg.ctx} "
+                         "+ greedy accept; 5 layers, hidden 2560, 24Q/2KV x 256, MLP 7680, vocab 151936, "
+                         f"{cfg.weight_type.upper()} backbone{win}",
+             "ctx": cfg.ctx, "block": cfg.block, "fuse_per_step": FUSE_PER_STEP, "weight_type": cfg.weight_type,
+             "sequences_per_gpu": 1,
+             "l2": "inputs larger than L2: every step streams over 1 GB of weights and K/V (L2 is 129 MB)"}
+    if window > 0:
+        block["attn_window"] = window
+    return block
+
+
+def workload_config(args):
+    cfg = synth.CONFIGS[WORKLOAD]
+    if args.weight_type:
+        cfg = cfg.with_(weight_type=args.weight_type)
+    if args.ctx:
+        cfg = cfg.with_(ctx=args.ctx)
+    if args.window:
+        cfg = cfg.with_(attn_window=args.window)
+    return cfg
+
+
+def state_capacity(cfg) -> int:
+    """Cells of the bench's state: the context and one block, or with an
+    attention window a ring of the window rounded up to 128 cells."""
+    window = getattr(cfg, "attn_window", 0)
+    if window > 0:
+        return (window + 127) // 128 * 128
+    return cfg.ctx + cfg.block
 
 
 # --------------------------------------------------------------------------
@@ -235,19 +262,24 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     D.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    cfg = synth.CONFIGS[WORKLOAD]
-    if args.weight_type:
-        cfg = cfg.with_(weight_type=args.weight_type)
+    cfg = workload_config(args)
     ctx, B = cfg.ctx, cfg.block
     t_setup = time.perf_counter()
     ckpt = synth.make_checkpoint(cfg, seed=0)
     model = DraftModel(cfg, ckpt, device=dev)
-    st = DraftState(model, n_slots=1, capacity=ctx + B)
-    # build the 8192-position context by fusion (128-position tiles)
+    st = DraftState(model, n_slots=1, capacity=state_capacity(cfg))
+    # build the context by fusion (128-position tiles); long contexts reuse one
+    # block of taps (its values do not change the work)
+    shared = None
     for base in range(0, ctx, 1024):
-        taps = synth.make_taps(cfg, 1024, seed=5, stream=base)
-        st.fuse(0, torch.as_tensor(taps.view(np.int16), device=dev),
-                torch.arange(base, base + 1024, dtype=torch.int32, device=dev))
+        n = min(1024, ctx - base)
+        if ctx <= 16384:
+            taps = torch.as_tensor(synth.make_taps(cfg, n, seed=5, stream=base).view(np.int16), device=dev)
+        else:
+            if shared is None:
+                shared = torch.as_tensor(synth.make_taps(cfg, 1024, seed=5).view(np.int16), device=dev)
+            taps = shared[:n]
+        st.fuse(0, taps, torch.arange(base, base + n, dtype=torch.int32, device=dev))
     torch.cuda.synchronize(dev)
     setup_s = time.perf_counter() - t_setup
 
@@ -413,6 +445,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--weight-type", default=None, choices=[None, "bf16", "q8_0", "q5_0", "q4_0"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ctx", type=int, default=0, help="anchor position p (default: the workload's 8192)")
+    ap.add_argument("--window", type=int, default=0, help="drafter attention window over a ring of cells (0: none)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
