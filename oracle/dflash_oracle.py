@@ -39,6 +39,11 @@ Readings where the pages are silent (each listed in the design doc):
     position pos in cell pos mod capacity.
   * Accept length n = longest prefix with draft_j == target_j; the bonus
     token is target_n.
+  * Confidence gate (--spec-min-p floor, [#3322] "Long-prompt diagnosis and
+    fix": floor 0.5 by default, 0.7 in the 256K run): a draft's confidence
+    is the drafter's softmax probability of the drafted token, and the block
+    offers the drafts before the first one whose confidence is below the
+    floor (floor 0 offers all).
 
 parity status: every function below is pinned by tests/test_oracle_pins.py
 (closed forms, hand-packed blocks, invariants, brute force, the pages' own
@@ -315,6 +320,7 @@ class DraftResult:
     logits: np.ndarray        # float64 [B-1, V]
     top2_gap: np.ndarray      # float64 [B-1]: top-1 minus top-2 logit
     stages: Optional[Dict[str, np.ndarray]] = None
+    probs: Optional[np.ndarray] = None  # float64 [B-1]: softmax probability of each draft
 
 
 def draft_block(model: Model, state: State, anchor_tok: int, anchor_pos: int,
@@ -373,7 +379,26 @@ def draft_block(model: Model, state: State, anchor_tok: int, anchor_pos: int,
     drafts = np.argmax(logits, axis=-1).astype(np.int32)
     part = np.partition(logits, -2, axis=-1)
     gap = part[:, -1] - part[:, -2]
-    return DraftResult(drafts, hf, logits, gap, stages if trace else None)
+    return DraftResult(drafts, hf, logits, gap, stages if trace else None, draft_probs(logits))
+
+
+def draft_probs(logits) -> np.ndarray:
+    """Softmax probability of each row's argmax: exp(max) / sum_v exp(l_v)
+    = 1 / sum_v exp(l_v - max), float64."""
+    logits = np.asarray(logits, dtype=np.float64)
+    mx = logits.max(axis=-1, keepdims=True)
+    return 1.0 / np.exp(logits - mx).sum(axis=-1)
+
+
+def gate(drafts, probs, floor: float) -> np.ndarray:
+    """The drafts a block offers under the confidence floor: the prefix
+    before the first draft with probability < floor; the rest become -1
+    (not offered, so acceptance stops there)."""
+    out = np.array(drafts, dtype=np.int32, copy=True)
+    low = np.nonzero(np.asarray(probs) < floor)[0]
+    if low.size:
+        out[low[0]:] = -1
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -541,3 +541,48 @@ def test_ring_cells_match_position_addressed_cells():
     # anchor position written by the pass, cell (n + B) % C an older position
     assert ring.held[0][n % C - 1] == n - 1 and ring.held[0][n % C] == n
     assert ring.held[0][(n + B) % C] == n + B - C
+
+
+# ---------------------------------------------------------------------------
+# confidence gate (spec-min-p)
+# ---------------------------------------------------------------------------
+
+def test_draft_probs_closed_forms():
+    """Uniform logits give 1/V; one logit ahead of V - 1 equal ones by delta
+    gives 1 / (1 + (V - 1) e^-delta); a shift of every logit changes nothing;
+    large logits (1e4) do not overflow."""
+    V = 1000
+    assert np.allclose(O.draft_probs(np.zeros((1, V))), 1.0 / V)
+    for delta in (0.0, 0.5, 3.0, 40.0):
+        row = np.zeros(V)
+        row[17] = delta
+        want = 1.0 / (1.0 + (V - 1) * math.exp(-delta))
+        assert math.isclose(O.draft_probs(row[None])[0], want, rel_tol=1e-12)
+    rng = np.random.default_rng(51)
+    lg = rng.normal(0, 3, (4, V))
+    assert np.allclose(O.draft_probs(lg), O.draft_probs(lg + 1e4), rtol=1e-9)
+
+
+def test_draft_probs_brute_force():
+    """Against exp(max) / sum of exp over a tiny vocabulary, element by element
+    with math.exp, and in (0, 1] always."""
+    rng = np.random.default_rng(52)
+    lg = rng.normal(0, 2, (6, 7))
+    for r in range(6):
+        tot = sum(math.exp(v) for v in lg[r])
+        assert math.isclose(O.draft_probs(lg[r:r + 1])[0], math.exp(lg[r].max()) / tot, rel_tol=1e-12)
+    p = O.draft_probs(rng.normal(0, 5, (50, 64)))
+    assert np.all(p > 0) and np.all(p <= 1)
+
+
+def test_gate_prefix_rule():
+    d = np.array([5, 9, 2, 7])
+    p = np.array([0.9, 0.6, 0.4, 0.95])
+    assert np.array_equal(O.gate(d, p, 0.0), d)          # floor 0 offers every draft
+    assert np.array_equal(O.gate(d, p, 0.5), [5, 9, -1, -1])  # cut at the first low one, later ones too
+    assert np.array_equal(O.gate(d, p, 0.6), [5, 9, -1, -1])  # equal to the floor is offered
+    assert np.array_equal(O.gate(d, p, 0.95), [-1, -1, -1, -1])
+    assert np.array_equal(O.gate(d, p, 1.5), [-1, -1, -1, -1])
+    # an offered prefix of length n accepts at most n proposals
+    n, _ = O.accept(O.gate(d, p, 0.5), [5, 9, 2, 7, 1], 5)
+    assert n == 2
