@@ -108,6 +108,8 @@ _SIGS = {
     "dflash_state_set_head_events": (ctypes.c_int, [_P, _P, _P]),
     "dflash_state_set_profile_events": (ctypes.c_int, [_P, ctypes.POINTER(_P), _I]),
     "dflash_state_set_attn_chunks": (ctypes.c_int, [_P, _I, ctypes.POINTER(_I)]),
+    "dflash_state_set_spec_min_p": (ctypes.c_int, [_P, ctypes.c_float]),
+    "dflash_state_read_draft_probs": (ctypes.c_int, [_P, _P, _P]),
     "dflash_head_argmax_static": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
 }
 
@@ -283,6 +285,15 @@ def dflash_state_set_profile_events(state: int, events) -> None:
     arr = (_P * max(1, len(events)))(*events) if events else None
     _check(load_library().dflash_state_set_profile_events(state, arr, len(events)),
            "dflash_state_set_profile_events")
+
+
+def dflash_state_set_spec_min_p(state: int, floor: float) -> None:
+    _check(load_library().dflash_state_set_spec_min_p(state, floor), "dflash_state_set_spec_min_p")
+
+
+def dflash_state_read_draft_probs(state: int, out: int, stream: int = 0) -> None:
+    """Copy the last pass's [n_slots, 7] float draft confidences to out (device)."""
+    _check(load_library().dflash_state_read_draft_probs(state, out, stream or None), "dflash_state_read_draft_probs")
 
 
 def dflash_state_set_attn_chunks(state: int, chunks: int = 0) -> int:

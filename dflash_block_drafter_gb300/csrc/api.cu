@@ -191,7 +191,7 @@ void free_state(State* s) {
   if (!s) return;
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
-  f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->nonfinite);
+  f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
   f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->status);
 }
 
@@ -540,6 +540,8 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   if (cudaMemset(s->counters, 0, size_t(CNT_REGIONS) * s->counter_stride * 4) != cudaSuccess)
     return fail(cuda_fail(cudaGetLastError(), "cudaMemset counters"));
   STRY(dev_alloc(&s->argmax_slots, size_t(s->max_grid) * rmax * 8, &total));
+  STRY(dev_alloc(&s->argmax_ms, size_t(s->max_grid) * rmax * 8, &total));
+  STRY(dev_alloc(&s->draft_probs, size_t(n_slots) * (DFLASH_MAX_BLOCK - 1) * 4, &total));
   STRY(dev_alloc(&s->nonfinite, 16, &total));
   s->fuse_rows = 128;
   STRY(dev_alloc(&s->h_raw, size_t(s->fuse_rows) * H * 4, &total));
@@ -806,6 +808,9 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.block_len = block_len;
     p.drafts = drafts;
     p.slots = s->argmax_slots;
+    p.ms = s->argmax_ms;
+    p.probs = s->draft_probs;
+    p.min_p = s->spec_min_p;
     p.grid_cnt = s->counters + static_cast<size_t>(CNT_ARGMAX) * s->counter_stride;
     p.final_hidden = final_hidden;
     a.rs_early = final_hidden != nullptr;
@@ -943,6 +948,19 @@ int dflash_state_set_attn_chunks(dflash_state* s, int32_t chunks, int32_t* max_c
   if (chunks == 0) return DFLASH_OK;
   if (chunks < 1 || chunks > s->attn_chunks_max) return DFLASH_ERR_INVALID_ARG;
   s->attn_chunks = chunks;
+  return DFLASH_OK;
+}
+
+int dflash_state_set_spec_min_p(dflash_state* s, float floor) {
+  if (!s || !(floor >= 0.f && floor <= 1.f)) return DFLASH_ERR_INVALID_ARG;
+  s->spec_min_p = floor;
+  return DFLASH_OK;
+}
+
+int dflash_state_read_draft_probs(const dflash_state* s, float* out, dflash_stream_t stream) {
+  if (!s || !out) return DFLASH_ERR_INVALID_ARG;
+  CK(cudaMemcpyAsync(out, s->draft_probs, size_t(s->n_slots) * (DFLASH_MAX_BLOCK - 1) * 4, cudaMemcpyDeviceToDevice,
+                     reinterpret_cast<cudaStream_t>(stream)));
   return DFLASH_OK;
 }
 

@@ -18,6 +18,9 @@ struct ArgmaxParams {
   const int32_t* block_len;
   int32_t* drafts;
   unsigned long long* slots;
+  float2* ms;      // [grid, R] per-CTA (max logit, sum of exp) for the draft probabilities
+  float* probs;    // [n_seq, 7] out, or null
+  float min_p;     // confidence floor (0: every draft offered)
   int* grid_cnt;
   float* final_hidden;
   const float* x;
@@ -138,7 +141,8 @@ cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const Launc
 // LM head + argmax over the borrowed row-major BF16 head.
 inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc) {
   DFLASH_NT_SWITCH(
-      nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.grid_cnt, p.final_hidden, p.x,
+      nt, EpiArgmax<NT> e{p.vocab, p.n_seq, p.block_len, p.drafts, p.slots, p.ms, p.probs, p.min_p, p.grid_cnt,
+                          p.final_hidden, p.x,
                           p.norm_w, p.H, p.status};
       if constexpr (NT == 1) {
         if (fused_norm(nt)) return launch_gemv<WT_HEAD, NT, X_NORM>(a, e, lc);

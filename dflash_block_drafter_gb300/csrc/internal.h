@@ -94,6 +94,9 @@ struct State {
   int* counters = nullptr;     // [CNT_REGIONS][counter_stride]
   int counter_stride = 0;
   unsigned long long* argmax_slots = nullptr;  // [max_grid, R]
+  float2* argmax_ms = nullptr;  // [max_grid, R]: per-CTA (max logit, sum of exp) of the LM head
+  float* draft_probs = nullptr; // [n_slots, 7]: softmax probability of each draft of the last pass
+  float spec_min_p = 0.f;       // confidence floor of the drafts (0: every draft offered)
   int* nonfinite = nullptr;    // [1] scratch flag
   // fusion workspace (tiles of up to fuse_rows positions)
   int fuse_rows = 0;

@@ -13,7 +13,8 @@ import torch
 from . import (DFLASH_MAX_BLOCK, dflash_accept, dflash_draft_block, dflash_fuse_context, dflash_model_create,
                dflash_model_dequantize, dflash_model_destroy, dflash_model_device_bytes, dflash_state_create,
                dflash_state_destroy, dflash_state_device_bytes, dflash_state_read_kv, dflash_state_status,
-               dflash_state_write_kv, load_library, make_config, make_weights)
+               dflash_state_read_draft_probs, dflash_state_set_spec_min_p, dflash_state_write_kv, load_library,
+               make_config, make_weights)
 
 
 def _stream(stream: Optional[torch.cuda.Stream] = None) -> int:
@@ -124,6 +125,16 @@ class DraftState:
         """k16, v16: float16 / int16 tensors [n_kv, n, d] on the device."""
         n = k16.shape[1]
         dflash_state_write_kv(self.handle, slot, layer, pos0, n, k16.data_ptr(), v16.data_ptr(), _stream())
+
+    def set_spec_min_p(self, floor: float) -> None:
+        """Confidence floor of the offered drafts (0: all)."""
+        dflash_state_set_spec_min_p(self.handle, floor)
+
+    def draft_probs(self) -> torch.Tensor:
+        """[n_slots, 7] float confidences of the last pass's drafts (-1: none)."""
+        out = torch.empty((self.n_slots, DFLASH_MAX_BLOCK - 1), dtype=torch.float32, device=self.model.device)
+        dflash_state_read_draft_probs(self.handle, out.data_ptr(), _stream())
+        return out
 
     def take_status(self) -> int:
         torch.cuda.synchronize(self.model.device)

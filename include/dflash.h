@@ -313,6 +313,22 @@ int dflash_state_set_profile_events(dflash_state* state, void* const* events, in
  * non-NULL; pass chunks = 0 to only query).  Applies to later calls. */
 int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* max_chunks);
 
+/* Confidence gate of the proposals ("--spec-min-p", "#3322 ...", "Long-prompt
+ * diagnosis and fix": floor 0.5 by default there, 0.7 in its 256K run).  A
+ * draft's confidence is the drafter's softmax probability of the drafted
+ * token (its LM-head logits, all V of them).  After this call every
+ * dflash_draft_block on the state writes -1 (not offered) for the first
+ * draft of a block whose confidence is below `floor` and for every later
+ * draft of that block, so acceptance stops there.  floor in [0, 1] (else
+ * DFLASH_ERR_INVALID_ARG); 0, the default, offers every draft. */
+int dflash_state_set_spec_min_p(dflash_state* state, float floor);
+
+/* Copy the confidences of the last dflash_draft_block into out, a caller
+ * device buffer of [n_slots, 7] float, on the stream: entry [s][j] is the
+ * confidence of draft j of slot s (whether or not the gate offered it), or
+ * -1 where the block has no draft j (j >= B - 1, or non-finite logits). */
+int dflash_state_read_draft_probs(const dflash_state* state, float* out, dflash_stream_t stream);
+
 /* Greedy ids over the target's LM head for n_rows (1..8) rows of final
  * hidden states, for callers that cannot allocate device memory: code that
  * runs while a CUDA graph is being captured, engines that own all device
