@@ -405,7 +405,8 @@ struct EpiArgmax {
   unsigned long long* slots;     // [gridDim.x, R]
   float2* ms;                    // [gridDim.x, R]: each CTA's (max logit, sum of exp(logit - max))
   float* probs;                  // [n_seq, 7] out: softmax probability of each draft (-1 where none)
-  float min_p;                   // confidence floor: drafts from the first one below it are not offered
+  float min_p;                   // confidence floor: drafts from the first one below it are not offered;
+                                 // 0: no confidences are computed (probs are -1) and every draft is offered
   int* grid_cnt;
   float* final_hidden;           // optional [n_seq, 8, H] (X_NORM prologue)
   const float* x;                // residual rows for final_hidden
@@ -444,14 +445,19 @@ struct EpiArgmax {
           const int h = e & 1;
           if (!isfinite(v)) {
             L.bad = 1;
-          } else if (v > L.v[t][h]) {
-            // a new maximum: rescale the running sum to it (0 from -inf)
-            L.s[t][h] = L.s[t][h] * ex2_approx((L.v[t][h] - v) * LOG2E) + 1.f;
+          } else if (min_p > 0.f) {
+            if (v > L.v[t][h]) {
+              // a new maximum: rescale the running sum to it (0 from -inf)
+              L.s[t][h] = L.s[t][h] * ex2_approx((L.v[t][h] - v) * LOG2E) + 1.f;
+              L.v[t][h] = v;
+              L.id[t][h] = m;
+            } else {
+              L.s[t][h] += ex2_approx((v - L.v[t][h]) * LOG2E);
+              if (v == L.v[t][h] && m < L.id[t][h]) L.id[t][h] = m;
+            }
+          } else if (v > L.v[t][h] || (v == L.v[t][h] && m < L.id[t][h])) {
             L.v[t][h] = v;
             L.id[t][h] = m;
-          } else {
-            L.s[t][h] += ex2_approx((v - L.v[t][h]) * LOG2E);
-            if (v == L.v[t][h] && m < L.id[t][h]) L.id[t][h] = m;
           }
         }
       }
@@ -540,25 +546,28 @@ struct EpiArgmax {
         kc = k2 > kc ? k2 : kc;
       }
     }
+    const bool sums = min_p > 0.f;  // uniform: confidences wanted
     named_bar_sync(1, 128);
-    if (tid < R) sf[tid] = kc ? float_from_order_key(static_cast<uint32_t>(kc >> 32)) : -INFINITY;
-    named_bar_sync(1, 128);
+    if (sums) {
+      if (tid < R) sf[tid] = kc ? float_from_order_key(static_cast<uint32_t>(kc >> 32)) : -INFINITY;
+      named_bar_sync(1, 128);
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
+      for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float mrow = sf[t * 8 + (lane & 3) * 2 + h];
-        float c = L.s[t][h] > 0.f ? L.s[t][h] * ex2_approx((L.v[t][h] - mrow) * LOG2E) : 0.f;
+        for (int h = 0; h < 2; ++h) {
+          const float mrow = sf[t * 8 + (lane & 3) * 2 + h];
+          float c = L.s[t][h] > 0.f ? L.s[t][h] * ex2_approx((L.v[t][h] - mrow) * LOG2E) : 0.f;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        if (lane < 4) sf[R + w * R + t * 8 + lane * 2 + h] = c;
+          for (int o = 4; o < 32; o <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+          if (lane < 4) sf[R + w * R + t * 8 + lane * 2 + h] = c;
+        }
+      named_bar_sync(1, 128);
+      if (tid < R) {
+        const float S = (sf[R + tid] + sf[2 * R + tid]) + (sf[3 * R + tid] + sf[4 * R + tid]);
+        __stcg(ms + static_cast<size_t>(blockIdx.x) * R + tid, make_float2(sf[tid], S));
       }
-    named_bar_sync(1, 128);
-    if (tid < R) {
-      const float S = (sf[R + tid] + sf[2 * R + tid]) + (sf[3 * R + tid] + sf[4 * R + tid]);
-      __stcg(ms + static_cast<size_t>(blockIdx.x) * R + tid, make_float2(sf[tid], S));
-      __stcg(slots + static_cast<size_t>(blockIdx.x) * R + tid, kc);
     }
+    if (tid < R) __stcg(slots + static_cast<size_t>(blockIdx.x) * R + tid, kc);
     named_bar_sync(1, 128);
     if (tid == 0) {
       const int old = atomic_add_acq_rel(grid_cnt, 1);
@@ -568,44 +577,46 @@ struct EpiArgmax {
     if (!sflag[2]) return;
     const unsigned long long k = grid_max<R>(tid, w, lane, sstage);
     named_bar_sync(1, 128);
-    if (tid < R) sf[tid] = k ? float_from_order_key(static_cast<uint32_t>(k >> 32)) : -INFINITY;
-    named_bar_sync(1, 128);
-    {
-      // sum over every CTA of its sum rescaled to the row's overall maximum:
-      // thread t takes row t % R over CTAs t / R, t / R + 128 / R, ...
-      constexpr int NS = 128 / R;
-      const int G = static_cast<int>(gridDim.x);
-      const int r = tid % R, st = tid / R;
-      const float mg = sf[r];
-      float acc = 0.f;
-      for (int c0 = st; c0 < G; c0 += 8 * NS) {
-        float2 v[8];
+    if (sums) {
+      if (tid < R) sf[tid] = k ? float_from_order_key(static_cast<uint32_t>(k >> 32)) : -INFINITY;
+      named_bar_sync(1, 128);
+      {
+        // sum over every CTA of its sum rescaled to the row's overall maximum:
+        // thread t takes row t % R over CTAs t / R, t / R + 128 / R, ...
+        constexpr int NS = 128 / R;
+        const int G = static_cast<int>(gridDim.x);
+        const int r = tid % R, st = tid / R;
+        const float mg = sf[r];
+        float acc = 0.f;
+        for (int c0 = st; c0 < G; c0 += 8 * NS) {
+          float2 v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = c0 + q * NS;
-          v[q] = c < G ? __ldcg(ms + static_cast<size_t>(c) * R + r) : make_float2(-INFINITY, 0.f);
+          for (int q = 0; q < 8; ++q) {
+            const int c = c0 + q * NS;
+            v[q] = c < G ? __ldcg(ms + static_cast<size_t>(c) * R + r) : make_float2(-INFINITY, 0.f);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (v[q].y > 0.f) acc += v[q].y * ex2_approx((v[q].x - mg) * LOG2E);
         }
+        if constexpr (R < 32) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (v[q].y > 0.f) acc += v[q].y * ex2_approx((v[q].x - mg) * LOG2E);
+          for (int o = R; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          if (lane < R) sf[R + w * R + lane] = acc;
+        } else {
+          sf[R + tid] = acc;  // stripe st of row r at R + st * R + r
+        }
       }
-      if constexpr (R < 32) {
+      named_bar_sync(1, 128);
+      if (tid < R) {
+        constexpr int E = R < 32 ? 4 : 128 / R;
+        float S = 0.f;
 #pragma unroll
-        for (int o = R; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane < R) sf[R + w * R + lane] = acc;
-      } else {
-        sf[R + tid] = acc;  // stripe st of row r at R + st * R + r
+        for (int e = 0; e < E; ++e) S += sf[R + e * R + tid];
+        sf[5 * R + tid] = S > 0.f ? 1.f / S : 0.f;
       }
+      named_bar_sync(1, 128);
     }
-    named_bar_sync(1, 128);
-    if (tid < R) {
-      constexpr int E = R < 32 ? 4 : 128 / R;
-      float S = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) S += sf[R + e * R + tid];
-      sf[5 * R + tid] = S > 0.f ? 1.f / S : 0.f;
-    }
-    named_bar_sync(1, 128);
     if (tid < R) {
       const int s = tid >> 3, i = tid & 7;
       if (s < n_seq && i >= 1) {
@@ -618,10 +629,12 @@ struct EpiArgmax {
             set_status(status, DFLASH_DEV_NONFINITE);
           } else {
             out = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
-            prob = sf[5 * R + tid];
-            // offered only if no draft of the block up to this one is below the floor
-            for (int i2 = 1; i2 <= i; ++i2)
-              if (sf[5 * R + s * 8 + i2] < min_p) out = -1;
+            if (sums) {
+              prob = sf[5 * R + tid];
+              // offered only if no draft of the block up to this one is below the floor
+              for (int i2 = 1; i2 <= i; ++i2)
+                if (sf[5 * R + s * 8 + i2] < min_p) out = -1;
+            }
           }
         }
         drafts[s * (DFLASH_MAX_BLOCK - 1) + (i - 1)] = out;

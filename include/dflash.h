@@ -320,13 +320,15 @@ int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* m
  * dflash_draft_block on the state writes -1 (not offered) for the first
  * draft of a block whose confidence is below `floor` and for every later
  * draft of that block, so acceptance stops there.  floor in [0, 1] (else
- * DFLASH_ERR_INVALID_ARG); 0, the default, offers every draft. */
+ * DFLASH_ERR_INVALID_ARG); 0, the default, offers every draft and skips the
+ * confidences altogether (the LM head then runs a plain argmax). */
 int dflash_state_set_spec_min_p(dflash_state* state, float floor);
 
 /* Copy the confidences of the last dflash_draft_block into out, a caller
  * device buffer of [n_slots, 7] float, on the stream: entry [s][j] is the
  * confidence of draft j of slot s (whether or not the gate offered it), or
- * -1 where the block has no draft j (j >= B - 1, or non-finite logits). */
+ * -1 where the block has no draft j (j >= B - 1, or non-finite logits) and
+ * everywhere when that pass ran with floor 0. */
 int dflash_state_read_draft_probs(const dflash_state* state, float* out, dflash_stream_t stream);
 
 /* Greedy ids over the target's LM head for n_rows (1..8) rows of final

@@ -54,7 +54,8 @@ def _setup_slots(wtype, ctxs, Bs, seed):
 def test_gate_parity(wtype, ctxs, Bs):
     st, om, osts, toks = _setup_slots(wtype, ctxs, Bs, seed=61)
     res = [O.draft_block(om, osts[s], int(toks[s]), ctxs[s], Bs[s]) for s in range(len(ctxs))]
-    # confidences with the gate off: every draft offered
+    # confidences under a floor no draft is below: every draft offered
+    st.set_spec_min_p(1e-12)
     st.draft(len(ctxs))
     probs = st.draft_probs().cpu().numpy()
     for s, r in enumerate(res):
@@ -77,7 +78,13 @@ def test_gate_parity(wtype, ctxs, Bs):
         assert np.array_equal(got[:upto] == -1, want[:upto] == -1), f"slot {s}: {got} vs {want} (floor {floor})"
         sure = (want[:upto] != -1) & (r.top2_gap[:upto] > 1e-2)
         assert np.array_equal(got[:upto][sure], want[:upto][sure]), f"slot {s}: {got} vs {want}"
+    # floor 0 (the default) skips the confidences and offers every draft
     st.set_spec_min_p(0.0)
+    st.draft(len(ctxs))
+    torch.cuda.synchronize()
+    assert np.all(st.draft_probs().cpu().numpy() == -1)
+    for s, r in enumerate(res):
+        check_drafts(st.drafts[s].cpu().numpy(), r, Bs[s], f"slot {s}, floor 0")
     assert st.take_status() == 0
 
 
