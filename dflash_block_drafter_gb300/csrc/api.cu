@@ -705,8 +705,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         NormArgs na{s->x, m->attn_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
                     ku_of(wt)};
         prof_mark(s, stream);
-        prof_mark(s, stream);
-      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "attn norm"));
+        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "attn norm"));
         a.X = s->xnorm;
         a.ldx = H;
       }
@@ -763,8 +762,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         NormArgs na{s->x, m->mlp_norm + size_t(l) * H, s->xnorm, f16, H, R, c.norm_eps, nullptr, 0,
                     ku_of(wt)};
         prof_mark(s, stream);
-        prof_mark(s, stream);
-      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "mlp norm"));
+        TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "mlp norm"));
         a.X = s->xnorm;
         a.ldx = H;
       }
