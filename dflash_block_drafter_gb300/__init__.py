@@ -99,6 +99,7 @@ _SIGS = {
     "dflash_fuse_context": (ctypes.c_int, [_P, _P, _I, _P, _P, _I, _P, _P]),
     "dflash_draft_block": (ctypes.c_int, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_accept": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P, _P, _P]),
+    "dflash_commit_positions": (ctypes.c_int, [_P, _P, _I, _P, _P]),
     "dflash_state_read_kv": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dflash_state_write_kv": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dflash_state_status": (ctypes.c_int, [_P, ctypes.POINTER(_I), _P]),
@@ -208,6 +209,11 @@ def dflash_accept(drafts: int, target_ids: int, block_len: int, n_seq: int, max_
                   accept_len: int, next_anchor: int, anchor_pos_inout: int = 0, stream: int = 0) -> None:
     _check(load_library().dflash_accept(drafts, target_ids, block_len, n_seq, max_block_len, accept_len,
                                         next_anchor, anchor_pos_inout or None, stream or None), "dflash_accept")
+
+
+def dflash_commit_positions(anchor_pos: int, accept_len: int, n_seq: int, positions: int, stream: int = 0) -> None:
+    _check(load_library().dflash_commit_positions(anchor_pos, accept_len, n_seq, positions, stream or None),
+           "dflash_commit_positions")
 
 
 def dflash_state_read_kv(state: int, slot: int, layer: int, pos0: int, n: int, k_out: int, v_out: int,

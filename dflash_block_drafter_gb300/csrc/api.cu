@@ -848,6 +848,15 @@ int dflash_accept(const int32_t* drafts, const int32_t* target_ids, const int32_
   return DFLASH_OK;
 }
 
+int dflash_commit_positions(const int32_t* anchor_pos, const int32_t* accept_len, int32_t n_seq,
+                            int32_t* positions, dflash_stream_t stream) {
+  if (!anchor_pos || !accept_len || !positions || n_seq < 1) return DFLASH_ERR_INVALID_ARG;
+  TRY(check_gemv(launch_commit_positions(anchor_pos, accept_len, n_seq, positions,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                 "commit positions"));
+  return DFLASH_OK;
+}
+
 int dflash_state_read_kv(const dflash_state* s, int32_t slot, int32_t layer, int32_t pos0, int32_t n, float* k_out,
                          float* v_out, dflash_stream_t stream) {
   if (!s) return DFLASH_ERR_INVALID_ARG;

@@ -325,8 +325,9 @@ struct EpiHeads {
               use[q] = false;
             } else {
               pos[q] = positions[n];
+              // a negative position is a row to skip (no cell, no error)
               write_state[q] = pos[q] >= 0 && (ring || pos[q] < cap);
-              if (!write_state[q] && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
+              if (pos[q] >= 0 && !write_state[q] && lane == 0 && hh == 0) set_status(status, DFLASH_DEV_CAPACITY);
             }
           }
           if (kind != 0 && !write_state[q]) use[q] = false;

@@ -50,6 +50,8 @@ cudaError_t launch_embed(const EmbedArgs& a, int nt, cudaStream_t st);
 cudaError_t launch_rmsnorm_rows(const NormArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* tgt, const int32_t* block_len, int n_seq, int maxB,
                           int32_t* accept_len, int32_t* next_anchor, int32_t* anchor_pos, cudaStream_t st);
+cudaError_t launch_commit_positions(const int32_t* anchor_pos, const int32_t* accept_len, int n_seq, int32_t* out,
+                                    cudaStream_t st);
 cudaError_t launch_kv_copy(bool write, __half* cells, int cap, bool ring, int d, int n_kv, int pos0, int n, float* out,
                            const uint16_t* in, cudaStream_t st);
 cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,

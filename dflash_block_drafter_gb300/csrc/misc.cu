@@ -322,6 +322,25 @@ __global__ void accept_kernel(const int32_t* __restrict__ drafts, const int32_t*
   if (anchor_pos) anchor_pos[s] += n + 1;
 }
 
+// Positions committed by the last acceptance, for the next fusion: with the
+// anchor already advanced to p + n + 1, the committed rows are p .. p + n
+// (the anchor and the n accepted candidates); the rest of the 8 are -1.
+__global__ void commit_positions_kernel(const int32_t* __restrict__ anchor_pos, const int32_t* __restrict__ accept_len,
+                                        int n_seq, int32_t* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_seq * DFLASH_MAX_BLOCK) return;
+  const int s = i / DFLASH_MAX_BLOCK, j = i - s * DFLASH_MAX_BLOCK;
+  const int n = accept_len[s];
+  out[i] = j <= n ? anchor_pos[s] - n - 1 + j : -1;
+}
+
+cudaError_t launch_commit_positions(const int32_t* anchor_pos, const int32_t* accept_len, int n_seq, int32_t* out,
+                                    cudaStream_t st) {
+  const int total = n_seq * DFLASH_MAX_BLOCK;
+  commit_positions_kernel<<<(total + 127) / 128, 128, 0, st>>>(anchor_pos, accept_len, n_seq, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* tgt, const int32_t* block_len, int n_seq, int maxB,
                           int32_t* accept_len, int32_t* next_anchor, int32_t* anchor_pos, cudaStream_t st) {
   const int threads = 128;

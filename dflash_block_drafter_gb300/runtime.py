@@ -10,8 +10,8 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-from . import (DFLASH_MAX_BLOCK, dflash_accept, dflash_draft_block, dflash_fuse_context, dflash_model_create,
-               dflash_model_dequantize, dflash_model_destroy, dflash_model_device_bytes, dflash_state_create,
+from . import (DFLASH_MAX_BLOCK, dflash_accept, dflash_commit_positions, dflash_draft_block, dflash_fuse_context,
+               dflash_model_create, dflash_model_dequantize, dflash_model_destroy, dflash_model_device_bytes, dflash_state_create,
                dflash_state_destroy, dflash_state_device_bytes, dflash_state_read_kv, dflash_state_status,
                dflash_state_read_draft_probs, dflash_state_set_spec_min_p, dflash_state_write_kv, load_library,
                make_config, make_weights)
@@ -160,3 +160,10 @@ def accept(drafts: torch.Tensor, target_ids: torch.Tensor, block_len: torch.Tens
     dflash_accept(drafts.data_ptr(), target_ids.data_ptr(), block_len.data_ptr(), n_seq, max_b,
                   accept_len.data_ptr(), next_anchor.data_ptr(), anchor_pos.data_ptr() if anchor_pos is not None
                   else 0, _stream(stream))
+
+
+def commit_positions(anchor_pos: torch.Tensor, accept_len: torch.Tensor, positions: torch.Tensor,
+                     stream=None) -> None:
+    """positions [n_seq, 8] <- the rows the next fusion commits (-1: none)."""
+    dflash_commit_positions(anchor_pos.data_ptr(), accept_len.data_ptr(), accept_len.numel(),
+                            positions.data_ptr(), _stream(stream))

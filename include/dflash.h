@@ -205,7 +205,9 @@ size_t dflash_state_device_bytes(const dflash_state* state);
  *   taps:      [n, n_taps*H] BF16 (uint16 bits), the five taps of a position
  *              concatenated in tap order.
  *   positions: [n] int32, distinct, each in [0, capacity) (ring states: >= 0,
- *              and distinct modulo capacity).
+ *              and distinct modulo capacity); a negative position skips its
+ *              row (nothing written, no error), so a fixed-size call can fuse
+ *              a device-determined number of positions (dflash_commit_positions).
  * For every position and layer l: k = RoPE(rmsnorm_head(W_k,l h), pos) and
  * v = W_v,l h are rounded to FP16 and written to the slot's cells,
  * overwriting what was there ("Position-addressed context/KV cells are
@@ -251,6 +253,19 @@ int dflash_draft_block(const dflash_model* model, dflash_state* state, int32_t n
  *   anchor_pos_inout: optional [n_seq] int32: p += n + 1 (the next anchor's
  *               position) when non-NULL.
  * 2 <= max_block_len <= 8. */
+/* The positions the next fusion commits after dflash_accept advanced
+ * anchor_pos: the verify window's anchor and its n accepted candidates sit at
+ * p .. p + n (p = anchor_pos - n - 1, with n = accept_len), so
+ * positions[s][j] = p + j for j <= n and -1 for n < j < 8 ("#1426 ...",
+ * "Speculative decode integration": the committed prefix is fused, the
+ * bonus token anchors the next block).  With the target's taps of those rows
+ * this lets fuse -> draft -> accept -> commit run on the device with no host
+ * round trip (a fixed 8-row dflash_fuse_context skips the -1 rows).
+ *   anchor_pos, accept_len: [n_seq] int32 device, as left by dflash_accept.
+ *   positions: [n_seq, 8] int32 device out. */
+int dflash_commit_positions(const int32_t* anchor_pos, const int32_t* accept_len, int32_t n_seq,
+                            int32_t* positions, dflash_stream_t stream);
+
 int dflash_accept(const int32_t* drafts, const int32_t* target_ids, const int32_t* block_len,
                   int32_t n_seq, int32_t max_block_len, int32_t* accept_len,
                   int32_t* next_anchor, int32_t* anchor_pos_inout, dflash_stream_t stream);

@@ -300,13 +300,24 @@ def fuse_hidden(model: Model, taps_bits) -> np.ndarray:
 def fuse_context(model: Model, state: State, taps_bits, positions) -> np.ndarray:
     """Fuse newly committed positions: project h_ctx into every layer's own
     K/V and write it by position, overwriting the cell ([#1426] "Drafter
-    runtime" and "Speculative decode integration").  Returns h_ctx."""
+    runtime" and "Speculative decode integration").  A negative position
+    marks a row that is not committed: it is skipped.  Returns h_ctx."""
     pos = np.asarray(positions, dtype=np.int64)
     h = fuse_hidden(model, taps_bits)
+    keep = pos >= 0
     for l in range(model.cfg.n_layers):
-        k, v = project_kv(model, l, h, pos)
-        state.write(l, pos, k, v)
+        k, v = project_kv(model, l, h[keep], pos[keep])
+        state.write(l, pos[keep], k, v)
     return h
+
+
+def commit_positions(anchor_pos_after: int, n: int, rows: int = 8) -> np.ndarray:
+    """The positions a cycle commits for the next fusion, given the anchor
+    position after acceptance (p + n + 1) and the accept length n: the
+    window's anchor at p and its n accepted candidates, p .. p + n; the
+    remaining rows are -1 ([#1426] "Speculative decode integration")."""
+    p = int(anchor_pos_after) - int(n) - 1
+    return np.array([p + j if j <= n else -1 for j in range(rows)], dtype=np.int32)
 
 
 # ----------------------------------------------------------------------------

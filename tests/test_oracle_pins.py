@@ -586,3 +586,36 @@ def test_gate_prefix_rule():
     # an offered prefix of length n accepts at most n proposals
     n, _ = O.accept(O.gate(d, p, 0.5), [5, 9, 2, 7, 1], 5)
     assert n == 2
+
+
+# ---------------------------------------------------------------------------
+# the device-chained cycle: committed positions, skipped fusion rows
+# ---------------------------------------------------------------------------
+
+def test_commit_positions_rule():
+    """Anchor at p, n accepted: rows p .. p + n are committed, the bonus
+    token's position p + n + 1 is the next anchor (the pages' acceptance
+    cases: full, partial and first-candidate rejection)."""
+    p = 100
+    for n in (0, 3, 7):
+        after = p + n + 1
+        got = O.commit_positions(after, n)
+        assert list(got[: n + 1]) == list(range(p, p + n + 1))
+        assert (got[n + 1:] == -1).all() and len(got) == 8
+
+
+def test_fusion_skips_negative_positions():
+    """Fusing rows with some positions -1 writes exactly the other rows,
+    bit-identical to fusing only those rows."""
+    cfg = _tiny()
+    ck = synth.make_checkpoint(cfg, seed=71, with_target_tensors=False)
+    m = O.Model(cfg, ck)
+    taps = synth.make_taps(cfg, 8, seed=71)
+    pos = np.array([10, 11, 12, -1, -1, -1, -1, -1])
+    a = O.State(cfg, 32)
+    O.fuse_context(m, a, taps, pos)
+    b = O.State(cfg, 32)
+    O.fuse_context(m, b, taps[:3], pos[:3])
+    for l in range(cfg.n_layers):
+        assert np.array_equal(a.K[l], b.K[l]) and np.array_equal(a.V[l], b.V[l])
+        assert np.array_equal(a.held[l], b.held[l])
