@@ -76,8 +76,8 @@ enum dflash_status {
 enum dflash_device_error {
   DFLASH_DEV_NONFINITE = 1,   /* a logit or hidden value was NaN/Inf ("non-finite refusal") */
   DFLASH_DEV_BAD_TOKEN = 2,   /* anchor token id outside [0, vocab) */
-  DFLASH_DEV_CAPACITY = 4,    /* p + block_len > capacity, or a fuse position outside [0, capacity)
-                                 (ring states, attn_window > 0: a negative position) */
+  DFLASH_DEV_CAPACITY = 4,    /* p + block_len > capacity, or a fuse position >= capacity (negative
+                                 fuse positions are skipped rows; ring states accept any p >= 0) */
   DFLASH_DEV_BAD_BLOCK = 8,   /* a block_len outside [2, 8] (clamped) */
   DFLASH_DEV_TIMEOUT = 16     /* a pipeline wait exceeded its time limit (should never happen) */
 };

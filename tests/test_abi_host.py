@@ -93,6 +93,10 @@ def test_null_and_range_arguments_rejected(lib):
     for n_seq, maxb in ((0, 8), (1, 1), (1, 9)):
         assert lib.dflash_accept(fake, fake, fake, n_seq, maxb, fake, fake, None, None) == D.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_accept(None, fake, fake, 1, 8, fake, fake, None, None) == D.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_commit_positions(None, fake, 1, fake, None) == D.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_commit_positions(fake, fake, 0, fake, None) == D.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_state_set_spec_min_p(None, 0.5) == D.DFLASH_ERR_INVALID_ARG
+    assert lib.dflash_state_read_draft_probs(None, fake, None) == D.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_state_read_kv(None, 0, 0, 0, 1, None, None, None) == D.DFLASH_ERR_INVALID_ARG
     assert lib.dflash_state_write_kv(None, 0, 0, 0, 1, None, None, None) == D.DFLASH_ERR_INVALID_ARG
     st = ctypes.c_int32()
