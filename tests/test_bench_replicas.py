@@ -49,3 +49,23 @@ def test_single_rank_needs_no_collective():
     import bench
     assert bench.max_over_ranks([7.0, 1.5]) == [7.0, 1.5]
     assert bench.replica_throughput(1, 3000, 1500.0) == pytest.approx(2000.0)
+
+
+def test_window_options_size_the_state_and_bytes():
+    """--ctx / --window: a ring of the window rounded to 128 cells, and K/V
+    bytes for the attended positions only; the default workload unchanged."""
+    import argparse
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    base = bench.workload_config(argparse.Namespace(weight_type=None, ctx=0, window=0))
+    assert bench.state_capacity(base) == base.ctx + base.block
+    full = bench.algorithmic_bytes(base, base.ctx, base.block, 8)
+    assert full["step"] == 1884651520  # 1.792 GB draft + 92 MB fusion at 8192 positions, BF16
+    win = bench.workload_config(argparse.Namespace(weight_type="q8_0", ctx=262144, window=32768))
+    assert win.attn_window == 32768 and bench.state_capacity(win) == 32768
+    b = bench.algorithmic_bytes(win, win.ctx, win.block, 8)
+    nowin = bench.algorithmic_bytes(win.with_(attn_window=0), win.ctx, win.block, 8)
+    kv_per_pos = win.n_layers * 2 * win.n_kv_heads * win.head_dim * 2
+    assert nowin["draft"] - b["draft"] == kv_per_pos * (win.ctx + win.block - 32768)
+    assert bench.state_capacity(win.with_(attn_window=100)) == 128
