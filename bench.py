@@ -45,9 +45,9 @@ METRIC = "draft passes/s and drafted tok/s at 8K ctx, block 8; HBM GB/s vs roofl
 UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
-# DRAM bytes (read + write) of one LM-head launch at this workload, from the
-# ncu capture summarised in profiles/lm_head_argmax_full_bf16.md (6.195 TB/s x
-# 126.11 us).  Reset to None whenever the head kernel changes.
+# DRAM bytes (read + write) of one LM-head launch at this workload, from one
+# ncu capture of that kernel (6.195 TB/s x 126.11 us).  Reset to None whenever
+# the head kernel changes.
 HEAD_TRAFFIC_BYTES = 781.3e6
 
 

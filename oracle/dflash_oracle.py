@@ -21,7 +21,7 @@ Citations name the page (by its title) and the section:
           Qwen3.8-Flash-Next"
   [#3322] "#3322 [Engine] support the official Flash-Next DFlash2 checkpoint"
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent (the library header states the same ones):
   * RMSNorm is x / sqrt(mean(x^2) + eps) * w with eps = 1e-6.
   * per-head RMSNorm over head_dim on q and k ("q raw / q normed / q" stage
     names, [#1426] "Parity validation"), before RoPE, also on context k.
@@ -47,8 +47,12 @@ Readings where the pages are silent (each listed in the design doc):
 
 parity status: every function below is pinned by tests/test_oracle_pins.py
 (closed forms, hand-packed blocks, invariants, brute force, the pages' own
-geometry and acceptance cases); the composition of the full pass beyond those
-pins follows the stage order of [#1426] "Parity validation".
+geometry and acceptance cases).  The per-layer composition of the pass is
+pinned as well: the per-head q / k norms (scale invariance of W_q, W_k; the
+q_norm x k_norm product), which norm feeds which sub-layer (zero mlp_norm
+removes the MLP; zero attn_norm gives uniform attention over the values),
+the roles of gate and up (a one-unit SwiGLU closed form) and the value path
+(an identity W_v stores the unnormed, unrotated input).
 """
 from __future__ import annotations
 

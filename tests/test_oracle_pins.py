@@ -619,3 +619,149 @@ def test_fusion_skips_negative_positions():
     for l in range(cfg.n_layers):
         assert np.array_equal(a.K[l], b.K[l]) and np.array_equal(a.V[l], b.V[l])
         assert np.array_equal(a.held[l], b.held[l])
+
+
+# ---------------------------------------------------------------------------
+# per-layer composition of the pass: which norm feeds which projection, the
+# per-head q / k norms, the roles of gate and up, the value path
+# ---------------------------------------------------------------------------
+
+def _scaled(ck, name, c):
+    """A BF16 tensor of the checkpoint times c (a power of two: exact)."""
+    return synth.to_bf16_bits((O.decode_bf16(ck[name]) * c).astype(np.float32))
+
+
+def _run_pass(cfg, ck, seed, B=4, trace=False):
+    m = O.Model(cfg, ck)
+    st = O.State(cfg, 128)
+    O.fuse_context(m, st, synth.make_taps(cfg, cfg.ctx, seed=seed), np.arange(cfg.ctx))
+    return O.draft_block(m, st, 21, cfg.ctx, B, trace=trace), st
+
+
+@pytest.mark.parametrize("mat", ["wq", "wk"])
+def test_per_head_qk_norm_makes_projection_scale_irrelevant(mat):
+    """With eps = 0 the per-head RMSNorm of q (and of every k, context and
+    block) removes any positive scale of W_q (W_k): the whole pass is
+    unchanged.  Without the norm the attention logits would scale by 4."""
+    cfg = _tiny(norm_eps=0.0)
+    ck = synth.make_checkpoint(cfg, seed=31)
+    r0, _ = _run_pass(cfg, ck, 31)
+    ck2 = dict(ck)
+    for l in range(cfg.n_layers):
+        ck2[f"layers.{l}.{mat}"] = _scaled(ck, f"layers.{l}.{mat}", 4.0)
+    r1, _ = _run_pass(cfg, ck2, 31)
+    rms = float(np.sqrt(np.mean(r0.final_hidden ** 2)))
+    assert np.allclose(r0.final_hidden, r1.final_hidden, rtol=0, atol=1e-12 * rms)
+    assert np.array_equal(r0.drafts, r1.drafts)
+
+
+def test_qk_norm_weights_enter_the_logits_as_a_product():
+    """q_norm x 2 with k_norm x 1/2 leaves every logit q.k (hence the pass)
+    unchanged; q_norm x 2 alone sharpens the softmax and changes it.  This
+    separates the two weights: using k_norm for q, or ignoring q_norm, fails."""
+    cfg = _tiny()
+    ck = synth.make_checkpoint(cfg, seed=32)
+    r0, _ = _run_pass(cfg, ck, 32)
+    both, qonly = dict(ck), dict(ck)
+    for l in range(cfg.n_layers):
+        both[f"layers.{l}.q_norm"] = _scaled(ck, f"layers.{l}.q_norm", 2.0)
+        both[f"layers.{l}.k_norm"] = _scaled(ck, f"layers.{l}.k_norm", 0.5)
+        qonly[f"layers.{l}.q_norm"] = _scaled(ck, f"layers.{l}.q_norm", 2.0)
+    r1, _ = _run_pass(cfg, both, 32)
+    r2, _ = _run_pass(cfg, qonly, 32)
+    rms = float(np.sqrt(np.mean(r0.final_hidden ** 2)))
+    # k / 2 is stored in FP16 exactly (a power of two)
+    assert np.allclose(r0.final_hidden, r1.final_hidden, rtol=0, atol=1e-12 * rms)
+    assert not np.allclose(r0.final_hidden, r2.final_hidden, rtol=0, atol=1e-4 * rms)
+
+
+def test_zero_mlp_norm_makes_the_mlp_vanish():
+    """mlp_norm = 0 zeroes the MLP input, so silu(0) * 0 = 0 and every layer's
+    residual leaves the MLP unchanged (x_mlp == x_attn); the attention
+    sub-layers are untouched (its input norm is attn_norm, not mlp_norm)."""
+    cfg = _tiny()
+    ck = synth.make_checkpoint(cfg, seed=33)
+    r0, _ = _run_pass(cfg, ck, 33, trace=True)
+    ck2 = dict(ck)
+    for l in range(cfg.n_layers):
+        ck2[f"layers.{l}.mlp_norm"] = np.zeros_like(ck[f"layers.{l}.mlp_norm"])
+    r1, _ = _run_pass(cfg, ck2, 33, trace=True)
+    for l in range(cfg.n_layers):
+        assert np.array_equal(r1.stages[f"layers.{l}.x_mlp"], r1.stages[f"layers.{l}.x_attn"])
+        assert not np.allclose(r0.stages[f"layers.{l}.x_mlp"], r0.stages[f"layers.{l}.x_attn"])
+    # layer 0's attention sub-layer does not see mlp_norm at all
+    assert np.array_equal(r0.stages["layers.0.x_attn"], r1.stages["layers.0.x_attn"])
+
+
+def test_zero_attn_norm_gives_uniform_attention_over_values():
+    """attn_norm = 0 makes q = k = v = 0 for the block rows, so every score is
+    0 and each head's attention output is the plain mean of its kv head's
+    values over the context cells [0, p) and the B zero block rows."""
+    cfg = _tiny()
+    ck = synth.make_checkpoint(cfg, seed=34)
+    ck2 = dict(ck)
+    for l in range(cfg.n_layers):
+        ck2[f"layers.{l}.attn_norm"] = np.zeros_like(ck[f"layers.{l}.attn_norm"])
+    B = 4
+    r, st = _run_pass(cfg, ck2, 34, B=B, trace=True)
+    grp = cfg.n_q_heads // cfg.n_kv_heads
+    for l in range(cfg.n_layers):
+        v_ctx = st.V[l][:, :cfg.ctx, :].astype(np.float64)   # [n_kv, ctx, d]
+        mean = v_ctx.sum(axis=1) / (cfg.ctx + B)
+        a = r.stages[f"layers.{l}.attn"]                     # [B, n_q, d]
+        for h in range(cfg.n_q_heads):
+            assert np.allclose(a[:, h, :], mean[h // grp][None, :], rtol=0, atol=1e-12)
+        assert not np.any(st.V[l][:, cfg.ctx:cfg.ctx + B, :])
+
+
+def test_swiglu_gate_and_up_roles_closed_form():
+    """One MLP unit: W_gate = a e_i^T, W_up = b e_j^T (row 0), W_down = e_k e_0^T
+    gives x_mlp - x_attn = silu(a xn_i) * (b xn_j) at element k and 0
+    elsewhere, xn = rmsnorm(x_attn, mlp_norm).  With a != b and xn_i != xn_j,
+    silu on the up projection instead of the gate fails."""
+    cfg = _tiny(n_layers=1)
+    ck = synth.make_checkpoint(cfg, seed=35)
+    H, I = cfg.hidden, cfg.intermediate
+    i, j, k, a, b = 3, 17, 40, 1.5, -0.75
+    g = np.zeros((I, H), np.float32); g[0, i] = a
+    u = np.zeros((I, H), np.float32); u[0, j] = b
+    dn = np.zeros((H, I), np.float32); dn[k, 0] = 1.0
+    ck["layers.0.w_gate"] = synth.to_bf16_bits(g)
+    ck["layers.0.w_up"] = synth.to_bf16_bits(u)
+    ck["layers.0.w_down"] = synth.to_bf16_bits(dn)
+    r, _ = _run_pass(cfg, ck, 35, trace=True)
+    xa = r.stages["layers.0.x_attn"]
+    xn = xa / np.sqrt(np.mean(xa * xa, -1, keepdims=True) + cfg.norm_eps) * O.decode_bf16(ck["layers.0.mlp_norm"])
+    z = a * xn[:, i]
+    want = (z / (1.0 + np.exp(-z))) * (b * xn[:, j])
+    delta = r.stages["layers.0.x_mlp"] - xa
+    assert np.allclose(delta[:, k], want, rtol=0, atol=1e-13)
+    assert not np.any(np.delete(delta, k, axis=1))
+    swapped = ((b * xn[:, j]) / (1.0 + np.exp(-b * xn[:, j]))) * (a * xn[:, i])
+    assert not np.allclose(delta[:, k], swapped, rtol=0, atol=1e-6)
+
+
+def test_values_are_the_unnormed_unrotated_projection():
+    """W_v = [I 0] (selecting the first n_kv * d hidden elements): the fused
+    context's V cells are FP16(h_ctx[:, :n_kv d]) and the block's own V cells
+    are FP16(rmsnorm(embed, attn_norm)[:, :n_kv d]) -- no norm and no
+    rotation on values, and the value input of the draft pass is the
+    attn_norm output."""
+    cfg = _tiny(n_layers=1)
+    ck = synth.make_checkpoint(cfg, seed=36)
+    H, nv = cfg.hidden, cfg.n_kv_heads * cfg.head_dim
+    wv = np.zeros((nv, H), np.float32); wv[:, :nv] = np.eye(nv, dtype=np.float32)
+    ck["layers.0.wv"] = synth.to_bf16_bits(wv)
+    m = O.Model(cfg, ck)
+    st = O.State(cfg, 128)
+    taps = synth.make_taps(cfg, cfg.ctx, seed=36)
+    h = O.fuse_context(m, st, taps, np.arange(cfg.ctx))
+    want_ctx = O.round_f16(h[:, :nv]).reshape(cfg.ctx, cfg.n_kv_heads, cfg.head_dim).transpose(1, 0, 2)
+    assert np.array_equal(st.V[0][:, :cfg.ctx, :], want_ctx)
+    B = 4
+    O.draft_block(m, st, 21, cfg.ctx, B)
+    toks = [21] + [cfg.mask_token_id] * (B - 1)
+    e = O.decode_bf16(ck["embed"][toks])
+    xn = e / np.sqrt(np.mean(e * e, -1, keepdims=True) + cfg.norm_eps) * O.decode_bf16(ck["layers.0.attn_norm"])
+    want_blk = O.round_f16(xn[:, :nv]).reshape(B, cfg.n_kv_heads, cfg.head_dim).transpose(1, 0, 2)
+    assert np.array_equal(st.V[0][:, cfg.ctx:cfg.ctx + B, :], want_blk)
