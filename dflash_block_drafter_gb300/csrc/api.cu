@@ -29,7 +29,7 @@ cudaError_t gemv_argmax(int nt, const GemvArgs& a, const ArgmaxParams& p, const 
 unsigned long long* trace_slot(State& st) {
 #ifdef DFLASH_TRACE
   if (st.trace && st.trace_k < st.trace_launches)
-    return st.trace + static_cast<size_t>(st.trace_k++) * st.max_grid * 8;
+    return st.trace + static_cast<size_t>(st.trace_k++) * st.max_grid * kTraceSlots;
 #endif
   (void)st;
   return nullptr;
@@ -236,6 +236,25 @@ int grid_for(const Model& m, const GemvArgs& a) {
   int g = sm;
   if (g > a.U) g = a.U;
   return g < 1 ? 1 : g;
+}
+
+// Cluster finishing of an 8-row GEMV whose grid splits every 64-row group
+// into the same number of parts (grid_for with groups <= SMs): clusters of
+// parts x gph CTAs (gph = groups per attention head for the per-head
+// epilogue, else 1), at most 8.  Sets a.cl_parts / a.cl_gph and returns the
+// cluster size, or 1 (no clusters: the counter-based finishing) when the
+// shape does not allow it.
+int plan_cluster(GemvArgs& a, int grid, int gph) {
+  a.cl_parts = a.cl_gph = 0;
+  const int groups = a.UPG > 0 ? a.U / a.UPG : 0;
+  if (groups < 1 || grid % groups) return 1;
+  const int parts = grid / groups;
+  if (parts > a.UPG || groups % gph) return 1;
+  const int cs = parts * gph;
+  if (cs <= 1 || cs > 8 || gph > 4) return 1;
+  a.cl_parts = parts;
+  a.cl_gph = gph;
+  return cs;
 }
 
 int check_gemv(cudaError_t e, const char* what) {
@@ -602,6 +621,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       const bool fpacked = fused_norm(nt);
       EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt)}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
     }
@@ -648,6 +668,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       e.status = status;
       e.rows_ = nt * 8;
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "fuse kv"));
     }
@@ -737,6 +758,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       e.status = status;
       e.rows_ = R;
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "qkv"));
     }
@@ -749,6 +771,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.ldx = nq * d;
       EpiResid e{s->x, H, PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt)}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
     }
@@ -780,6 +803,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
                           l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm,
                           l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
     }

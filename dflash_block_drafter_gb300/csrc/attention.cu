@@ -40,7 +40,7 @@ struct AttnArgs {
 #define DFLASH_ATTN_STAMP(k)                                                                                  \
   do {                                                                                                        \
     if (a.trace)                                                                                              \
-      a.trace[(static_cast<size_t>(blockIdx.z) * gridDim.y * gridDim.x + blockIdx.y * gridDim.x + blockIdx.x) * 8 + \
+      a.trace[(static_cast<size_t>(blockIdx.z) * gridDim.y * gridDim.x + blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + \
               (k)] = globaltimer_ns();                                                                        \
   } while (0)
 #else

@@ -42,6 +42,13 @@ struct GemvArgs {
   const float* ssq;
   int n_ssq;
   int rs_early;                  // X_NORM: 1 / RMS needed before the first group (final hidden rows)
+  // Cluster finishing (8-row passes): when cl_parts * cl_gph > 1 the grid is
+  // launched in clusters of cl_parts * cl_gph CTAs covering cl_gph whole
+  // 64-row groups (one attention head for the per-head epilogue), each group
+  // split between cl_parts CTAs.  A group's partial sums go to its first CTA
+  // through distributed shared memory, and the groups of a head exchange
+  // their results there, instead of through global memory and counters.
+  int cl_parts, cl_gph;
   float* partials;               // [gridDim.x, 2, 64, R]
   int* counters;                 // [N / 64]
   int32_t* status;
@@ -51,7 +58,7 @@ struct GemvArgs {
 #ifdef DFLASH_TRACE
 #define DFLASH_STAMP(k)                                                                   \
   do {                                                                                    \
-    if (a.trace) a.trace[static_cast<size_t>(blockIdx.x) * 8 + (k)] = globaltimer_ns(); \
+    if (a.trace) a.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + (k)] = globaltimer_ns(); \
   } while (0)
 #else
 #define DFLASH_STAMP(k) \
@@ -87,8 +94,17 @@ struct GemvGeom {
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
   static constexpr int RING = STAGES * STAGE;
   static constexpr int THREADS = 128 * CWG + 32;
-  static constexpr int MISC = SBUF + 8 * (2 * STAGES + 1) + 64 + 4 * R * 8 + R * 4;
-  // smem: [ring][partial-sum double buffer][barriers][misc]
+  // cluster finishing buffers (8-row passes of the backbone formats): the
+  // group's partial sums from up to kClMaxParts - 1 other CTAs, and the
+  // kClMaxGph groups of a head (kClHeadSlot floats each: 8 x 64 values in mma
+  // fragment order, then per-warp partial sums of squares [4][8])
+  static constexpr int kClMaxParts = 8, kClMaxGph = 4, kClHeadSlot = 512 + 32;
+  static constexpr bool kClusterable = NT == 1 && WT != WT_HEAD;
+  static constexpr int CL_RED = kClusterable ? (kClMaxParts - 1) * 128 * 16 : 0;
+  static constexpr int CL_HEAD = kClusterable ? kClMaxGph * kClHeadSlot * 4 : 0;
+  static constexpr int CLBUF = CL_RED + CL_HEAD;
+  static constexpr int MISC = SBUF + CLBUF + 8 * (2 * STAGES + 3) + 64 + 4 * R * 8 + R * 4;
+  // smem: [ring][partial-sum double buffer][cluster buffers][barriers][misc]
   static __host__ __device__ constexpr int smem_bytes(int) { return 1024 + RING + MISC; }
 };
 
@@ -125,9 +141,13 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   float4* sbuf = reinterpret_cast<float4*>(ring + Geo::RING);          // [2][128][NT] (second warpgroup's sums)
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING + Geo::SBUF);
+  float4* cl_red = reinterpret_cast<float4*>(ring + Geo::RING + Geo::SBUF);             // [parts - 1][128]
+  float* cl_head = reinterpret_cast<float*>(ring + Geo::RING + Geo::SBUF + Geo::CL_RED);  // [gph][8][64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING + Geo::SBUF + Geo::CLBUF);
   uint64_t* empty = full + STAGES;
-  int* sflag = reinterpret_cast<int*>(empty + STAGES);                 // 16 ints
+  uint64_t* cl_red_bar = empty + STAGES;   // the other parts' sums have arrived
+  uint64_t* cl_head_bar = cl_red_bar + 1;  // the head's other groups have arrived
+  int* sflag = reinterpret_cast<int*>(cl_head_bar + 1);                // 16 ints
   float* srs = reinterpret_cast<float*>(sflag + 16);                  // [R] row scales
   unsigned long long* sstage = reinterpret_cast<unsigned long long*>(srs + R);  // [4][R]
 
@@ -139,10 +159,15 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
   const int n_units = u_end - u_begin;
 
+  const int cl_size = Geo::kClusterable ? a.cl_parts * a.cl_gph : 1;
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4 * Geo::CWG);
+    }
+    if (cl_size > 1) {
+      mbar_init(cl_red_bar, a.cl_parts > 1 ? a.cl_parts - 1 : 1);
+      mbar_init(cl_head_bar, a.cl_gph > 1 ? a.cl_gph - 1 : 1);
     }
     fence_barrier_init();
   }
@@ -159,6 +184,9 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
     }
   }
   __syncthreads();
+  // cluster peers may use this CTA's barriers once every CTA has signalled
+  // here (the finishing step waits for that before its first remote access)
+  if (cl_size > 1) cluster_arrive_relaxed();
 
   if (warp == 4 * Geo::CWG) {
     // ------------------------------------------------------------ producer
@@ -277,20 +305,50 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
     epi.prologue(a, tid, XMODE == X_NORM ? srs : nullptr);
     named_bar_sync(1, 128);
   }
-  if (tid == 0) DFLASH_STAMP(4);
 
   typename Epi::Local loc;
   epi.init(loc);
-  float acc[NT][4], acc2[NT][4];  // acc2: lo-plane products (a second, independent chain)
+  if constexpr (Geo::kClusterable && Epi::kCluster) {
+    // cluster finishing: every peer's barriers are initialised once all have
+    // signalled (waited for here, while the ring fills, by the threads that
+    // later access peers); the epilogue's per-CTA constants are loaded now
+    if (cl_size > 1 && kh == 0) {
+      cluster_wait();
+      epi.prepare_cluster(a, loc, u_begin / a.UPG, w, lane);
+    }
+  }
+  // Accumulator chains: for the BF16 formats one per k-step and activation
+  // plane (acc: hi plane, k-step 0; accb: hi, k-step 1; acc2 / acc2b: the lo
+  // plane), so consecutive MMAs never wait on each other; the quantised
+  // formats sum each 32-block in its own temporary and scale it into acc.
+  // (tiles of more than 16 rows keep one chain per plane: registers)
+  constexpr bool kChains = NT <= 2;
+  constexpr int NB = kChains ? NT : 1;
+  float acc[NT][4], acc2[NT][4], accb_s[NB][4], acc2b_s[NB][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t)
     for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NB; ++t)
+    for (int e = 0; e < 4; ++e) accb_s[t][e] = acc2b_s[t][e] = 0.f;
+  auto accb = [&](int t) -> float(&)[4] {
+    if constexpr (kChains) return accb_s[t];
+    else return acc[t];
+  };
+  auto acc2b = [&](int t) -> float(&)[4] {
+    if constexpr (kChains) return acc2b_s[t];
+    else return acc2[t];
+  };
 
   const int first_group = u_begin / a.UPG;
   const uint32_t ring_s = smem_u32(ring);
   const int xrow = lane >> 2;
   bool ok = true;
   int gcount = 0;  // group ends passed (the same sequence in both warpgroups)
+  // blocks of a unit handled together: all their shared-memory loads are
+  // issued before their MMAs (fewer at once for large tiles: registers)
+  constexpr int IB = NT <= 2 ? BPW : 1;
+  constexpr bool kPairs = (WT == WT_Q4_0 || WT == WT_Q5_0) && IB % 2 == 0;
 
   // After a timeout the loop keeps running (without waiting) so every warp
   // takes the same named barriers; the outputs are then unspecified.
@@ -306,40 +364,77 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
     const uint32_t ubase = ring_s + s * Geo::STAGE;
 
 #pragma unroll
-    for (int bq = 0; bq < BPW; ++bq) {
-      const int bl = kh * BPW + bq;
-      const BlockFrag f = decode_block<WT, kF16>(ubase, w, lane, bl);
+    for (int b0 = 0; b0 < BPW; b0 += IB) {
+      BlockFrag f[IB];
+      uint4 xf[IB][NT], xl[IB][NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        uint4 xf, xl;
-        const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
-        xf = lds128(xb);
-        if constexpr (kSplit) xl = lds128(xb + R * Geo::XS_STRIDE);
-        if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
-          mma_bf16_16816(acc[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
-          mma_bf16_16816(acc[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
-          if constexpr (kSplit) {
-            mma_bf16_16816(acc2[t], f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xl.x, xl.y);
-            mma_bf16_16816(acc2[t], f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xl.z, xl.w);
-          }
+      for (int i = 0; i < IB; ++i) {
+        const int bl = kh * BPW + b0 + i;
+        if constexpr (kPairs) {
+          if (i % 2 == 0) decode_pair<WT, kF16>(ubase, w, lane, bl >> 1, f[i], f[i + 1]);
         } else {
-          float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (kF16) {
-            mma_f16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
-            mma_f16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
-          } else {
-            mma_bf16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xf.x, xf.y);
-            mma_bf16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xf.z, xf.w);
+          f[i] = decode_block<WT, kF16>(ubase, w, lane, bl);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint32_t xb = ubase + F::UNIT + (t * 8 + xrow) * Geo::XS_STRIDE + bl * 64 + (lane & 3) * 16;
+          xf[i][t] = lds128(xb);
+          if constexpr (kSplit) xl[i][t] = lds128(xb + R * Geo::XS_STRIDE);
+        }
+      }
+      if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
+#pragma unroll
+        for (int i = 0; i < IB; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            mma_bf16_16816(acc[t], f[i].a[0][0], f[i].a[0][1], f[i].a[0][2], f[i].a[0][3], xf[i][t].x, xf[i][t].y);
+            mma_bf16_16816(accb(t), f[i].a[1][0], f[i].a[1][1], f[i].a[1][2], f[i].a[1][3], xf[i][t].z, xf[i][t].w);
             if constexpr (kSplit) {
-              mma_bf16_16816(tmp, f.a[0][0], f.a[0][1], f.a[0][2], f.a[0][3], xl.x, xl.y);
-              mma_bf16_16816(tmp, f.a[1][0], f.a[1][1], f.a[1][2], f.a[1][3], xl.z, xl.w);
+              mma_bf16_16816(acc2[t], f[i].a[0][0], f[i].a[0][1], f[i].a[0][2], f[i].a[0][3], xl[i][t].x,
+                             xl[i][t].y);
+              mma_bf16_16816(acc2b(t), f[i].a[1][0], f[i].a[1][1], f[i].a[1][2], f[i].a[1][3], xl[i][t].z,
+                             xl[i][t].w);
             }
           }
-          acc[t][0] = fmaf(f.d_r, tmp[0], acc[t][0]);
-          acc[t][1] = fmaf(f.d_r, tmp[1], acc[t][1]);
-          acc[t][2] = fmaf(f.d_r8, tmp[2], acc[t][2]);
-          acc[t][3] = fmaf(f.d_r8, tmp[3], acc[t][3]);
+      } else {
+        // one sum per block; its MMAs (k-steps, planes) in rounds over the
+        // blocks, so neighbouring MMAs belong to different blocks
+        float tmp[IB][NT][4];
+#pragma unroll
+        for (int i = 0; i < IB; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) tmp[i][t][0] = tmp[i][t][1] = tmp[i][t][2] = tmp[i][t][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+          for (int i = 0; i < IB; ++i)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const uint32_t b0r = ks ? xf[i][t].z : xf[i][t].x, b1r = ks ? xf[i][t].w : xf[i][t].y;
+              if constexpr (kF16)
+                mma_f16_16816(tmp[i][t], f[i].a[ks][0], f[i].a[ks][1], f[i].a[ks][2], f[i].a[ks][3], b0r, b1r);
+              else
+                mma_bf16_16816(tmp[i][t], f[i].a[ks][0], f[i].a[ks][1], f[i].a[ks][2], f[i].a[ks][3], b0r, b1r);
+            }
+          if constexpr (kSplit) {
+#pragma unroll
+            for (int i = 0; i < IB; ++i)
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                const uint32_t b0r = ks ? xl[i][t].z : xl[i][t].x, b1r = ks ? xl[i][t].w : xl[i][t].y;
+                mma_bf16_16816(tmp[i][t], f[i].a[ks][0], f[i].a[ks][1], f[i].a[ks][2], f[i].a[ks][3], b0r, b1r);
+              }
+          }
         }
+#pragma unroll
+        for (int i = 0; i < IB; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            acc[t][0] = fmaf(f[i].d_r, tmp[i][t][0], acc[t][0]);
+            acc[t][1] = fmaf(f[i].d_r, tmp[i][t][1], acc[t][1]);
+            acc[t][2] = fmaf(f[i].d_r8, tmp[i][t][2], acc[t][2]);
+            acc[t][3] = fmaf(f[i].d_r8, tmp[i][t][3], acc[t][3]);
+          }
       }
     }
     __syncwarp();
@@ -347,11 +442,16 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
     if (tid == 0 && it == n_units - 1) DFLASH_STAMP(6);
 
     if (j == a.UPG - 1 || u == u_end - 1) {
-      if constexpr (kSplit && (WT == WT_BF16 || WT == WT_HEAD)) {
+      if constexpr (WT == WT_BF16 || WT == WT_HEAD) {
 #pragma unroll
         for (int t = 0; t < NT; ++t)
           for (int e = 0; e < 4; ++e) {
-            acc[t][e] += acc2[t][e];
+            if constexpr (kChains) {
+              acc[t][e] = (acc[t][e] + accb_s[t][e]) + (acc2[t][e] + acc2b_s[t][e]);
+              accb_s[t][e] = acc2b_s[t][e] = 0.f;
+            } else {
+              acc[t][e] += acc2[t][e];
+            }
             acc2[t][e] = 0.f;
           }
       }
@@ -394,8 +494,51 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
           acc[t][3] *= srs[n + 1];
         }
       }
+      bool clustered = false;
+      if constexpr (Geo::kClusterable && Epi::kCluster) {
+        if (cl_size > 1) {
+          // ------------------------------------- cluster finishing (DSMEM)
+          // this CTA's range lies in one group: part `part` of local group gl
+          clustered = true;
+          if (tid == 0) DFLASH_STAMP(4);
+          const int rank = static_cast<int>(blockIdx.x) % cl_size;
+          const int part = rank % a.cl_parts, gl = rank / a.cl_parts;
+          const uint32_t leader = static_cast<uint32_t>(gl * a.cl_parts);
+          if (part != 0) {
+            st_cluster_v4(mapa_shared(smem_u32(cl_red + (part - 1) * 128 + tid), leader), acc[0][0], acc[0][1],
+                          acc[0][2], acc[0][3]);
+            named_bar_sync(1, 128);
+            if (tid == 0) mbar_remote_arrive(mapa_shared(smem_u32(cl_red_bar), leader));
+          } else {
+            float pre[NT][4];
+            float4 wpre = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (Epi::kPreload) epi.template preload<WT, NT>(g, w, lane, pre, wpre);
+            if (a.cl_parts > 1) {
+              if (ok && !mbar_wait_cluster(cl_red_bar, 0)) {
+                set_status(a.status, DFLASH_DEV_TIMEOUT);
+                ok = false;
+              }
+              // the other parts' sums in rank order (deterministic)
+              for (int p = 0; p < a.cl_parts - 1; ++p) {
+                const float4 q = cl_red[p * 128 + tid];
+                acc[0][0] += q.x;
+                acc[0][1] += q.y;
+                acc[0][2] += q.z;
+                acc[0][3] += q.w;
+              }
+            }
+            if constexpr (Epi::kPreload)
+              epi.template group_pre<WT, NT>(g, w, lane, acc, pre, wpre);
+            else
+              ok = epi.template group_cluster<WT>(a, loc, g, gl, a.cl_parts, w, lane, tid, acc, cl_head,
+                                                  cl_head_bar, ok);
+          }
+        }
+      }
       const bool complete = (g * a.UPG >= u_begin) && (j == a.UPG - 1);
-      if (complete) {
+      if (clustered) {
+        // finished above
+      } else if (complete) {
         epi.template group<WT, NT>(a, loc, g, w, lane, acc);
         if constexpr (Epi::kAfterGroup) {
           named_bar_sync(1, 128);

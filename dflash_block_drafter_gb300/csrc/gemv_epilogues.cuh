@@ -64,7 +64,7 @@ struct PackNext {
 };
 
 struct EpiStore {
-  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
+  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false, kCluster = true;
   using Local = NoLocal;
   float* out;
   int ldo;
@@ -84,6 +84,15 @@ struct EpiStore {
     }
     pack.template operator()<WT, NT>(g, w, lane, acc);
   }
+  // cluster finishing: the group's first CTA holds the complete sums
+  template <int WT>
+  __device__ bool group_cluster(const GemvArgs& a, const Local&, int g, int, int, int w, int lane, int,
+                                float (&acc)[1][4], float*, uint64_t*, bool ok) const {
+    Local loc;
+    group<WT, 1>(a, loc, g, w, lane, acc);
+    return ok;
+  }
+  __device__ void prepare_cluster(const GemvArgs&, Local&, int, int, int) const {}
   __device__ void after_group(const GemvArgs&, int, int, int*) const {}
   template <int NT>
   __device__ void finish(const GemvArgs&, Local&, int, int, int, unsigned long long*, int*) const {}
@@ -92,7 +101,7 @@ struct EpiStore {
 // Residual update x[R, ldx] += Y: attention output projection and MLP down
 // projection.  Every element has exactly one owner thread.
 struct EpiResid {
-  static constexpr bool kAfterGroup = false, kFinish = false;
+  static constexpr bool kAfterGroup = false, kFinish = false, kCluster = true;
   // a split group's finisher loads its residual values before it knows it
   // is the finisher, overlapping that load with the arrival counter
   static constexpr bool kPreload = true;
@@ -103,6 +112,7 @@ struct EpiResid {
 
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  __device__ void prepare_cluster(const GemvArgs&, Local&, int, int, int) const {}
 
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
@@ -168,7 +178,7 @@ struct EpiResid {
 // hi and lo planes).
 template <bool kF16>
 struct EpiSwiglu {
-  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false;
+  static constexpr bool kAfterGroup = false, kFinish = false, kPreload = false, kCluster = false;
   using Local = NoLocal;
   void* h;
   __device__ void init(Local&) const {}
@@ -211,8 +221,18 @@ struct EpiSwiglu {
 //   mode 1 (fusion K/V): per layer l, n_kv key heads then n_kv value heads;
 //     activation row n is committed position positions[n].
 struct EpiHeads {
-  static constexpr bool kAfterGroup = true, kFinish = false, kPreload = false;
-  using Local = NoLocal;
+  static constexpr bool kAfterGroup = true, kFinish = false, kPreload = false, kCluster = true;
+  // cluster finishing of an 8-row pass: what a thread needs for its rows
+  // (w, w + 4) and rotation pairs (lane + 32 j), prepared at kernel start
+  // Thread t of the first warpgroup writes row t / 16, head columns
+  // 64 gl + 4 (t % 16) + k (k < 4) of its group gl: each output is
+  // rs * (y_i * A[k] + y_p * B[k]) with p the column paired with i by the
+  // rotation, A = w_i cos * scale, B = -+ w_p sin * scale.
+  struct Local {
+    float A[4], B[4];
+    int pos;
+    int use;  // the row is written
+  };
   int mode;
   float* raw;       // [R, ldr]
   int ldr;
@@ -237,6 +257,68 @@ struct EpiHeads {
 
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+
+  // Row metadata of activation row n: position, whether its K/V cells are
+  // written, whether it is used at all (queries always are).
+  __device__ void row_info(int n, int kind, int& pos, bool& write_state, bool& use) const {
+    pos = 0;
+    write_state = false;
+    use = true;
+    if (mode == 0) {
+      const int sl = n >> 3, i = n & 7;
+      if (sl < n_seq) {
+        int B = block_len[sl];
+        B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+        pos = anchor_pos[sl] + i;
+        write_state = (i < B) && pos >= 0 && (ring || pos < cap);
+      }
+    } else {
+      if (n >= n_valid) {
+        use = false;
+      } else {
+        pos = positions[n];
+        // a negative position is a row to skip (no cell, no error)
+        write_state = pos >= 0 && (ring || pos < cap);
+      }
+    }
+    if (kind != 0 && !write_state) use = false;
+  }
+
+  // Cluster finishing, kernel start (8-row pass, this CTA = local group gl
+  // of head g / gph): this thread's row metadata and, for query and key
+  // heads, its columns' norm weights folded with their rotations at the
+  // row's position, so the finishing step after the weight stream has no
+  // global loads and no sin / cos left.
+  __device__ void prepare_cluster(const GemvArgs&, Local& L, int g, int w, int lane) const {
+    const int hh = g / gph, gl = g - hh * gph;
+    const int kind = head_kind(hh);
+    const int half = d / 2;
+    const int t = w * 32 + lane, n = t >> 4;
+    bool ws, use;
+    row_info(n, kind, L.pos, ws, use);
+    if (mode == 1 && L.pos >= 0 && !ws && n < n_valid && (t & 15) == 0 && hh == 0)
+      set_status(status, DFLASH_DEV_CAPACITY);
+    L.use = use;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      L.A[k] = 1.f;
+      L.B[k] = 0.f;
+    }
+    if (kind == 2) return;
+    const float* wn = (mode == 0) ? (kind == 0 ? q_norm : k_norm) : k_norm + static_cast<size_t>(hh / (2 * n_kv)) * d;
+    const float scale = kind == 0 ? q_scale : 1.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = gl * 64 + (t & 15) * 4 + k;
+      const bool lo = i < half;
+      const int f = lo ? i : i - half, p = lo ? i + half : i - half;
+      float sn, cs;
+      rope_sincos(__ldg(turns + f), L.pos, sn, cs);
+      L.A[k] = __ldg(wn + i) * cs * scale;
+      L.B[k] = (lo ? -1.f : 1.f) * __ldg(wn + p) * sn * scale;
+    }
+  }
+
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
@@ -264,12 +346,149 @@ struct EpiHeads {
     process_head(head, tid);
   }
 
+  // 0: query head, 1: key head, 2: value head
+  __device__ int head_kind(int hh) const {
+    if (mode == 0) return hh < n_q ? 0 : (hh < n_q + n_kv ? 1 : 2);
+    return (hh % (2 * n_kv)) < n_kv ? 1 : 2;
+  }
+
   __device__ void process_head(int hh, int tid) const {
+    const float* base = raw + static_cast<size_t>(hh) * d;
+    const int ld = ldr;
+    process_head_src(hh, tid, [base, ld](int n, int i) { return __ldcg(base + static_cast<size_t>(n) * ld + i); },
+                     0, d);
+  }
+
+  // Cluster finishing of the 8-row pass: this CTA holds the complete sums of
+  // local group gl of head g / gph.  Key and query heads need every group of
+  // the head (RMS over d, RoPE pairs (i, i + d/2)): each group's values go to
+  // slot gl of every group CTA's buffer ([gph][8 rows][64] floats, in
+  // distributed shared memory), and each CTA then writes its own 64 columns.
+  // Value heads write their columns straight away.
+  template <int WT>
+  __device__ bool group_cluster(const GemvArgs& ga, const Local& L, int g, int gl, int parts, int w, int lane,
+                                int tid, float (&acc)[1][4], float* hbuf, uint64_t* head_bar, bool ok) const {
+#ifdef DFLASH_TRACE
+    unsigned long long* a_trace = ga.trace;
+#else
+    (void)ga;
+#endif
+    constexpr int SLOT = 512 + 32;
+    const int hh = g / gph;
+    const int kind = head_kind(hh);
+    const bool exch = gph > 1 && kind != 2;
+    // this group's values in mma fragment order (thread t at 4 t) and, for
+    // the norm, each warp's sums of squares of rows 0..7 over its 16 columns
+    float* mine = hbuf + gl * SLOT;
+    const int t4 = tid * 4;
+    *reinterpret_cast<float4*>(mine + t4) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    float s0 = 0.f, s1 = 0.f;
+    if (kind != 2) {
+      s0 = acc[0][0] * acc[0][0] + acc[0][2] * acc[0][2];  // row 2 (lane % 4)
+      s1 = acc[0][1] * acc[0][1] + acc[0][3] * acc[0][3];  // row 2 (lane % 4) + 1
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      if (lane < 4) *reinterpret_cast<float2*>(mine + 512 + w * 8 + lane * 2) = make_float2(s0, s1);
+    }
+    if (exch) {
+      for (int l2 = 0; l2 < gph; ++l2) {
+        if (l2 == gl) continue;
+        const uint32_t r = static_cast<uint32_t>(l2 * parts);
+        st_cluster_v4(mapa_shared(smem_u32(mine + t4), r), acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        if (lane < 4) {
+          st_cluster_f32(mapa_shared(smem_u32(mine + 512 + w * 8 + lane * 2), r), s0);
+          st_cluster_f32(mapa_shared(smem_u32(mine + 512 + w * 8 + lane * 2 + 1), r), s1);
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+#ifdef DFLASH_TRACE
+    if (tid == 0 && a_trace) a_trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + 9] = globaltimer_ns();
+#endif
+    if (exch) {
+      if (tid == 0)
+        for (int l2 = 0; l2 < gph; ++l2)
+          if (l2 != gl) mbar_remote_arrive(mapa_shared(smem_u32(head_bar), static_cast<uint32_t>(l2 * parts)));
+      if (ok && !mbar_wait_cluster(head_bar, 0)) {
+        set_status(status, DFLASH_DEV_TIMEOUT);
+        ok = false;
+      }
+    }
+#ifdef DFLASH_TRACE
+    if (tid == 0 && a_trace) a_trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + 2] = globaltimer_ns();
+#endif
+    // ---- this thread's four outputs: row n, columns i0 .. i0 + 3
+    if (!L.use) return ok;
+    const int n = tid >> 4, c = (tid & 15) * 4, i0 = gl * 64 + c;
+    const int half = d / 2;
+    int kvh, l;
+    if (mode == 0) {
+      l = layer;
+      kvh = kind == 0 ? 0 : (kind == 1 ? hh - n_q : hh - n_q - n_kv);
+    } else {
+      l = hh / (2 * n_kv);
+      const int rem = hh - l * 2 * n_kv;
+      kvh = rem < n_kv ? rem : rem - n_kv;
+    }
+    float out[4];
+    if (kind == 2) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) out[k] = mine[frag_index(c + k, n)];
+    } else {
+      float ss = 0.f;
+      for (int g2 = 0; g2 < gph; ++g2)
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) ss += hbuf[g2 * SLOT + 512 + w2 * 8 + n];
+      const float rs = rsqrtf(ss / d + eps);
+      const int ip0 = i0 < half ? i0 + half : i0 - half;  // partner columns ip0 .. ip0 + 3
+      const float* ps = hbuf + (ip0 >> 6) * SLOT;
+      const int cp = ip0 & 63;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float yi = mine[frag_index(c + k, n)];
+        const float yp = ps[frag_index(cp + k, n)];
+        out[k] = rs * (yi * L.A[k] + yp * L.B[k]);
+      }
+    }
+    const int pos = L.pos;
+    __half* dst;
+    if (kind == 0) {
+      const int gq = n_q / n_kv;
+      dst = q_ready + ((static_cast<size_t>((n >> 3) * n_kv + hh / gq) * gq + hh % gq) * 8 + (n & 7)) * d + i0;
+    } else {
+      const size_t cell = ((static_cast<size_t>((l * n_slots + (mode == 0 ? (n >> 3) : slot)) * n_kv + kvh) * cap) +
+                           (ring ? pos % cap : pos)) * d;
+      dst = (kind == 1 ? Kst : Vst) + cell + i0;
+    }
+    const __half2 h01 = __floats2half2_rn(out[0], out[1]), h23 = __floats2half2_rn(out[2], out[3]);
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+    return ok;
+  }
+
+  // Element (row n, column c) of one group's values in mma fragment order
+  // (column c = 16 w' + r sits at thread w' * 32 + (r % 8) * 4 + n / 2,
+  // value (r / 8) * 2 + n % 2).
+  __device__ static int frag_index(int c, int n) {
+    const int r = c & 15;
+    return ((c >> 4) * 32 + (r & 7) * 4 + (n >> 1)) * 4 + (r >> 3) * 2 + (n & 1);
+  }
+
+  // Norm, rotation, FP16 rounding and cell / query writes of head hh for all
+  // rows; src(n, i) gives element i of row n's raw head values.  Only the
+  // outputs of columns [c_lo, c_hi) are written (their inputs may be read
+  // from any column of the head).
+  template <class Src>
+  __device__ void process_head_src(int hh, int tid, Src src, int c_lo, int c_hi) const {
     const int w = tid >> 5, lane = tid & 31;
     const int half = d / 2;
     const int R = n_rows();
     int kind, kvh, l;
     const float* wn;
+    const bool full = c_lo == 0 && c_hi >= d;  // every column written (no filtering)
     if (mode == 0) {
       l = layer;
       if (hh < n_q) { kind = 0; kvh = 0; wn = q_norm; }
@@ -332,10 +551,14 @@ struct EpiHeads {
           }
           if (kind != 0 && !write_state[q]) use[q] = false;
         }
-        // the row's d values, lane-strided: element lane + 32 j (d <= 256)
-        const float* y = raw + static_cast<size_t>(n) * ldr + static_cast<size_t>(hh) * d;
+        // the row's d values, lane-strided: element lane + 32 j (d <= 256);
+        // value heads read only the columns they write
 #pragma unroll
-        for (int j = 0; j < 8; ++j) yv[q][j] = (use[q] && lane + 32 * j < d) ? __ldcg(y + lane + 32 * j) : 0.f;
+        for (int j = 0; j < 8; ++j) {
+          const int i = lane + 32 * j;
+          const bool need = i < d && (kind != 2 || full || (i >= c_lo && i < c_hi));
+          yv[q][j] = (use[q] && need) ? src(n, i) : 0.f;
+        }
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -345,8 +568,10 @@ struct EpiHeads {
             ((static_cast<size_t>((l * n_slots + sl[q]) * n_kv + kvh) * cap) + (ring ? pos[q] % cap : pos[q])) * d;
         if (kind == 2) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (lane + 32 * j < d) Vst[cell + lane + 32 * j] = __float2half_rn(yv[q][j]);
+          for (int j = 0; j < 8; ++j) {
+            const int i = lane + 32 * j;
+            if (i < d && (full || (i >= c_lo && i < c_hi))) Vst[cell + i] = __float2half_rn(yv[q][j]);
+          }
           continue;
         }
         float ss = 0.f;
@@ -369,10 +594,14 @@ struct EpiHeads {
             // element i + d/2 (d = 64, 128 or 256), picked without a runtime register index
             const float yb = hj == 4 ? yv[q][(j + 4) & 7] : (hj == 2 ? yv[q][(j + 2) & 7] : yv[q][(j + 1) & 7]);
             const float b = yb * rs * wb[j];
-            float sn, cs;
-            rope_sincos(tn[j], pos[q], sn, cs);
-            dst[i] = __float2half_rn((a * cs - b * sn) * scale);
-            dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+            const bool w_lo = full || (i >= c_lo && i < c_hi);
+            const bool w_hi = full || (i + half >= c_lo && i + half < c_hi);
+            if (w_lo || w_hi) {
+              float sn, cs;
+              rope_sincos(tn[j], pos[q], sn, cs);
+              if (w_lo) dst[i] = __float2half_rn((a * cs - b * sn) * scale);
+              if (w_hi) dst[i + half] = __float2half_rn((b * cs + a * sn) * scale);
+            }
           }
         }
       }
@@ -392,7 +621,7 @@ struct EpiHeads {
 // the largest logit with ties going to the lowest id.
 template <int NT_>
 struct EpiArgmax {
-  static constexpr bool kAfterGroup = false, kFinish = true, kPreload = false;
+  static constexpr bool kAfterGroup = false, kFinish = true, kPreload = false, kCluster = false;
   struct Local {
     float v[NT_][2];
     int id[NT_][2];

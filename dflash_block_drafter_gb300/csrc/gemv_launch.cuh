@@ -11,6 +11,7 @@ struct LaunchCfg {
   cudaStream_t stream;
   int grid;
   bool pdl;
+  int cluster = 1;  // CTAs per cluster (GemvArgs::cl_parts * cl_gph; 1: no clusters)
 };
 
 struct ArgmaxParams {
@@ -75,11 +76,23 @@ inline cudaError_t launch_gemv(const GemvArgs& a, const Epi& epi, const LaunchCf
   cfg.blockDim = dim3(GemvGeom<WT, NT, XMODE>::THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (lc.cluster > 1) {
+    if (!GemvGeom<WT, NT, XMODE>::kClusterable || !Epi::kCluster || lc.grid % lc.cluster ||
+        a.cl_parts * a.cl_gph != lc.cluster)
+      return cudaErrorInvalidValue;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(lc.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  } else if (a.cl_parts * a.cl_gph > 1) {
+    return cudaErrorInvalidValue;
+  }
   return cudaLaunchKernelEx(&cfg, kern, a, epi);
 }
 

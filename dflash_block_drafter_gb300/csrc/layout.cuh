@@ -223,4 +223,41 @@ __device__ __forceinline__ BlockFrag decode_block(uint32_t ubase, int w, int lan
   return f;
 }
 
+// Both 32-blocks of sub-chunk `pair` of a Q4_0 / Q5_0 unit (blocks 2 pair and
+// 2 pair + 1), with one load of the shared codes and scales.
+template <int WT, bool F16 = Fmt<WT>::kF16>
+__device__ __forceinline__ void decode_pair(uint32_t ubase, int w, int lane, int pair, BlockFrag& f0,
+                                            BlockFrag& f1) {
+  static_assert(WT == WT_Q4_0 || WT == WT_Q5_0, "two blocks per sub-chunk");
+  constexpr int CHUNK = Fmt<WT>::CHUNK;
+  const uint32_t base = ubase + (pair * 4 + w) * CHUNK;
+  const uint4 q = lds128(base + lane * 16);
+  constexpr int SC_OFF = (WT == WT_Q4_0) ? 512 : 640;
+  const uint2 sc = lds64(base + SC_OFF + (lane >> 2) * 8);
+  uint32_t hb = 0;
+  if constexpr (WT == WT_Q5_0) hb = lds32(base + 512 + lane * 4);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    BlockFrag& f = b ? f1 : f0;
+    const uint32_t wr = b ? q.y : q.x;
+    const uint32_t wr8 = b ? q.w : q.z;
+    const uint32_t scb = b ? sc.y : sc.x;
+    const __half2 d = *reinterpret_cast<const __half2*>(&scb);
+    f.d_r = __low2float(d);
+    f.d_r8 = __high2float(d);
+    if constexpr (WT == WT_Q4_0) {
+      f.a[0][0] = q4_pair<F16>(wr, 0); f.a[0][1] = q4_pair<F16>(wr8, 0);
+      f.a[0][2] = q4_pair<F16>(wr, 1); f.a[0][3] = q4_pair<F16>(wr8, 1);
+      f.a[1][0] = q4_pair<F16>(wr, 2); f.a[1][1] = q4_pair<F16>(wr8, 2);
+      f.a[1][2] = q4_pair<F16>(wr, 3); f.a[1][3] = q4_pair<F16>(wr8, 3);
+    } else {
+      const int o_r = b * 4, o_r8 = 8 + b * 4;
+      f.a[0][0] = q5_pair<F16>(wr, hb, 0, o_r); f.a[0][1] = q5_pair<F16>(wr8, hb, 0, o_r8);
+      f.a[0][2] = q5_pair<F16>(wr, hb, 1, o_r); f.a[0][3] = q5_pair<F16>(wr8, hb, 1, o_r8);
+      f.a[1][0] = q5_pair<F16>(wr, hb, 2, o_r); f.a[1][1] = q5_pair<F16>(wr8, hb, 2, o_r8);
+      f.a[1][2] = q5_pair<F16>(wr, hb, 3, o_r); f.a[1][3] = q5_pair<F16>(wr8, hb, 3, o_r8);
+    }
+  }
+}
+
 }  // namespace dflash
