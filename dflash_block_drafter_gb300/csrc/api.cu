@@ -619,7 +619,7 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
                           static_cast<uint32_t>(ku_of(wt)), static_cast<uint32_t>(rows)));
       // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
       const bool fpacked = fused_norm(nt);
-      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt)}};
+      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt), wt != WT_BF16}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
@@ -704,10 +704,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   };
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
-                 s->capacity, c.attn_window > 0, status, nullptr, nullptr, nullptr, 0};
+                 s->capacity, c.attn_window > 0, status, nullptr, nullptr, nullptr, 0, 0};
     if (packed) {
       ea.xn = s->xn;
       ea.ku = ku_of(wt);
+      ea.f16 = wt != WT_BF16;
       ea.ssq = s->ssq;
       ea.w_next = m->attn_norm;
     }
@@ -753,6 +754,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       e.cap = s->capacity;
       e.ring = c.attn_window > 0;
       e.n_seq = n_seq;
+      e.window = c.attn_window;
+      e.prefetch_kv = 1;
       e.anchor_pos = anchor_pos;
       e.block_len = block_len;
       e.status = status;
@@ -769,7 +772,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.n_valid_rows = R;
       a.X = s->attn_out;
       a.ldx = nq * d;
-      EpiResid e{s->x, H, PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt)}};
+      EpiResid e{s->x, H,
+                 PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt), wt != WT_BF16}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
@@ -801,7 +805,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       EpiResid e{s->x, H,
                  PackNext{packed ? s->xn : nullptr, s->ssq,
                           l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm,
-                          l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB}};
+                          l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB, l + 1 < L && wt != WT_BF16}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);

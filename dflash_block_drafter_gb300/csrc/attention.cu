@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         issue_v(0);
       }
       pdl_wait();
+      DFLASH_ATTN_STAMP(8);
       mbar_arrive_expect_tx(qfull, M * D * 2);
       for (int b = 0; b < Geo::BOXES; ++b) tma_load_2d(sq + b * (M * 128), &a.qmap, b * 64, (s * a.n_kv + g) * M, qfull);
       if (!early) {
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // S[j % 2] = Q K_j^T; the K buffer is released when it completes
       auto issue_qk = [&](int j) -> bool {
         if (!mbar_wait(kfull, j & 1)) return false;
+        if (j == 0) DFLASH_ATTN_STAMP(10);
         if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -311,7 +313,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       };
       // QK^T of super-tile j + 1 is issued before the PV of super-tile j, so it
       // runs while the softmax warps work on S[j % 2].
-      if (!mbar_wait(qfull, 0) || !issue_qk(0)) ok = false;
+      const bool qok = mbar_wait(qfull, 0);
+      DFLASH_ATTN_STAMP(9);
+      if (!qok || !issue_qk(0)) ok = false;
+      DFLASH_ATTN_STAMP(11);
       for (int j = 0; j < nst && ok; ++j) {
         if (j + 1 < nst && !issue_qk(j + 1)) { ok = false; break; }
         if (!mbar_wait(pfull, j & 1) || !mbar_wait(vfull, j & 1)) { ok = false; break; }
@@ -503,7 +508,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (tid == 64) {
           for (int h = 0; h < D / 64; ++h) tma_store_2d(&a.pmap, h * 64, static_cast<int>(pbase), sk + h * (M * 128));
           bulk_commit_group();
-          bulk_wait_group_0();
+          DFLASH_ATTN_STAMP(12);
+          bulk_wait_group_read_0();  // the staging buffer may be released; the writes land with the grid
+          DFLASH_ATTN_STAMP(13);
         }
       }
       if (cs == 0 && m < M) __stcg(a.ml + pbase + m, make_float2(m_run, l_run));

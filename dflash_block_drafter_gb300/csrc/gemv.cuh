@@ -74,8 +74,9 @@ struct GemvGeom {
   static constexpr int XSE = KU + 32;                   // streamed X row stride (elements, padded)
   static constexpr int XS_STRIDE = XSE * 2;             // ... in bytes
   static constexpr bool kStream = true;
-  // activation type fed to the MMA: FP16 for quantised weights unless X is BF16
-  static constexpr bool kF16 = F::kF16 && XMODE == X_STREAM;
+  // activation type fed to the MMA: FP16 for quantised weights unless X is
+  // the caller's BF16 taps
+  static constexpr bool kF16 = F::kF16 && (XMODE == X_STREAM || XMODE == X_NORM);
   // BF16 activations computed in fp32 are carried as two BF16 planes, hi and
   // lo = x - hi (about 16 significant bits), each multiplied on the tensor
   // cores; the caller's BF16 taps (X_STREAM_BF16) are exact and need no lo.
@@ -87,8 +88,10 @@ struct GemvGeom {
   // scheduler runs two consumer warps, hiding the MMA and shared-memory
   // latencies of one behind the other.  At each group end the second
   // warpgroup hands its partial sums to the first through a double buffer.
-  static constexpr int CWG = NT <= 4 ? 2 : 1;  // larger tiles keep 160 threads (register budget)
-  static constexpr int SBUF = CWG > 1 ? 2 * 128 * NT * 16 : 0;  // [2][128 threads][NT][4] floats
+  // Larger tiles keep fewer threads (register budget).
+  static constexpr int CWG = NT <= 4 ? 2 : 1;
+  // [2][CWG - 1 warpgroups][128 threads][NT][4] floats
+  static constexpr int SBUF = CWG > 1 ? 2 * (CWG - 1) * 128 * NT * 16 : 0;
   static constexpr int RING_BUDGET = 200000 - SBUF;
   static constexpr int STAGES_FIT = RING_BUDGET / STAGE;
   static constexpr int STAGES = STAGES_FIT < 2 ? 2 : (STAGES_FIT < F::STAGES ? STAGES_FIT : F::STAGES);
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  float4* sbuf = reinterpret_cast<float4*>(ring + Geo::RING);          // [2][128][NT] (second warpgroup's sums)
+  float4* sbuf = reinterpret_cast<float4*>(ring + Geo::RING);  // [2][CWG - 1][128][NT] (other warpgroups' sums)
   float4* cl_red = reinterpret_cast<float4*>(ring + Geo::RING + Geo::SBUF);             // [parts - 1][128]
   float* cl_head = reinterpret_cast<float*>(ring + Geo::RING + Geo::SBUF + Geo::CL_RED);  // [gph][8][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + Geo::RING + Geo::SBUF + Geo::CLBUF);
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
       }
       pdl_wait();  // activations below come from the previous kernel
       DFLASH_STAMP(1);
+      epi.producer_start(a, blockIdx.x, G);
       if constexpr (kStream)
         for (int it = 0; it < n_pre; ++it) issue_x(it, u_begin + it);
       int issued = n_pre;
@@ -456,30 +460,37 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
           }
       }
       if constexpr (Geo::CWG > 1) {
-        // second warpgroup: hand the K-half sums to the first and go on
+        // the other warpgroups hand their K-part sums to the first and go on
         // (barrier 2 + b: buffer b filled; barrier 4 + b: buffer b free again)
-        float4* sb = sbuf + (static_cast<size_t>(gcount & 1) * 128 + (w * 32 + lane)) * NT;
-        if (kh == 1) {
-          if (gcount >= 2) named_bar_sync(4 + (gcount & 1), 256);
+        constexpr int NB = 128 * Geo::CWG;
+        float4* sbb = sbuf + static_cast<size_t>(gcount & 1) * (Geo::CWG - 1) * 128 * NT;
+        if (kh >= 1) {
+          float4* sb = sbb + (static_cast<size_t>(kh - 1) * 128 + (w * 32 + lane)) * NT;
+          if (gcount >= 2) named_bar_sync(4 + (gcount & 1), NB);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             sb[t] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
             acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
           }
-          named_bar_arrive(2 + (gcount & 1), 256);
+          named_bar_arrive(2 + (gcount & 1), NB);
           ++gcount;
           continue;
         }
-        named_bar_sync(2 + (gcount & 1), 256);
+        named_bar_sync(2 + (gcount & 1), NB);
+        // fixed order over the warpgroups (deterministic)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const float4 q = sb[t];
-          acc[t][0] += q.x;
-          acc[t][1] += q.y;
-          acc[t][2] += q.z;
-          acc[t][3] += q.w;
+        for (int k2 = 0; k2 < Geo::CWG - 1; ++k2) {
+          const float4* sb = sbb + (static_cast<size_t>(k2) * 128 + (w * 32 + lane)) * NT;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const float4 q = sb[t];
+            acc[t][0] += q.x;
+            acc[t][1] += q.y;
+            acc[t][2] += q.z;
+            acc[t][3] += q.w;
+          }
         }
-        named_bar_arrive(4 + (gcount & 1), 256);
+        named_bar_arrive(4 + (gcount & 1), NB);
         ++gcount;
       }
       if constexpr (XMODE == X_NORM) {
@@ -622,9 +633,9 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   }
   if constexpr (Geo::CWG > 1) {
     // the first warpgroup's last two buffer releases have no later fill to pair with
-    if (kh == 1)
-      for (int gc = (gcount > 2 ? gcount - 2 : 0); gc < gcount; ++gc) named_bar_sync(4 + (gc & 1), 256);
-    if (kh == 1) return;
+    if (kh >= 1)
+      for (int gc = (gcount > 2 ? gcount - 2 : 0); gc < gcount; ++gc) named_bar_sync(4 + (gc & 1), 128 * Geo::CWG);
+    if (kh >= 1) return;
   }
   if constexpr (Epi::kFinish) epi.template finish<NT>(a, loc, w, lane, tid, sstage, sflag);
   if (tid == 0) DFLASH_STAMP(7);

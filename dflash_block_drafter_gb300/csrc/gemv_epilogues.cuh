@@ -15,15 +15,17 @@ struct NoLocal {};
 // Y stored as fp32 [R, ldo] (activation row major).  Feature fusion: fc.
 // Optional output of an epilogue that produces the rows x of a pass with 8
 // rows: the next RMSNorm-fed GEMV's input.  For each finished 64-column
-// group g: x[n][m] * w_next[m] split into BF16 hi and lo = bf16(v - hi), in
-// the chunked layout of 8 rows and `ku` inputs per unit (planes 0 and 1, see
-// xchunk_index), and ssq[g * 8 + n] = sum of x[n][m]^2 over the group.  The
-// GEMV divides its outputs by the row's RMS.  Null xn: none.
+// group g: x[n][m] * w_next[m] in the chunked layout of 8 rows and `ku`
+// inputs per unit (see xchunk_index) -- one FP16 plane when the consumer has
+// GGUF weights (f16), else BF16 hi and lo = bf16(v - hi) planes -- and
+// ssq[g * 8 + n] = sum of x[n][m]^2 over the group.  The GEMV divides its
+// outputs by the row's RMS.  Null xn: none.
 struct PackNext {
-  __nv_bfloat16* xn;
+  void* xn;
   float* ssq;
   const float* w_next;
   int ku;
+  int f16;
 
   // the four norm weights thread (w, lane) applies in group g (a load with no
   // dependence on the GEMV, so a finisher can issue it early)
@@ -49,11 +51,17 @@ struct PackNext {
       tile[n + 1][r1] = v[0][3];
       named_bar_sync(1, 128);
       const float4 xv = *reinterpret_cast<const float4*>(&tile[row][4 * q]);
-      uint2 hi, lo;
-      split_bf16x2(xv.x * wv.x, xv.y * wv.y, hi.x, lo.x);
-      split_bf16x2(xv.z * wv.z, xv.w * wv.w, hi.y, lo.y);
-      *reinterpret_cast<uint2*>(xn + xchunk_index(m, row, 0, 8, ku, 2)) = hi;
-      *reinterpret_cast<uint2*>(xn + xchunk_index(m, row, 1, 8, ku, 2)) = lo;
+      if (f16) {
+        *reinterpret_cast<uint2*>(static_cast<__half*>(xn) + xchunk_index(m, row, 0, 8, ku, 1)) =
+            make_uint2(pack_f16x2(xv.x * wv.x, xv.y * wv.y), pack_f16x2(xv.z * wv.z, xv.w * wv.w));
+      } else {
+        uint2 hi, lo;
+        split_bf16x2(xv.x * wv.x, xv.y * wv.y, hi.x, lo.x);
+        split_bf16x2(xv.z * wv.z, xv.w * wv.w, hi.y, lo.y);
+        __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(xn);
+        *reinterpret_cast<uint2*>(xb + xchunk_index(m, row, 0, 8, ku, 2)) = hi;
+        *reinterpret_cast<uint2*>(xb + xchunk_index(m, row, 1, 8, ku, 2)) = lo;
+      }
       float ss = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
 #pragma unroll
       for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -71,6 +79,7 @@ struct EpiStore {
   PackNext pack;  // optional (the fusion's fc output feeds the context K/V GEMV)
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  __device__ void producer_start(const GemvArgs&, int, int) const {}
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
@@ -112,6 +121,7 @@ struct EpiResid {
 
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  __device__ void producer_start(const GemvArgs&, int, int) const {}
   __device__ void prepare_cluster(const GemvArgs&, Local&, int, int, int) const {}
 
   template <int WT, int NT>
@@ -183,6 +193,7 @@ struct EpiSwiglu {
   void* h;
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+  __device__ void producer_start(const GemvArgs&, int, int) const {}
   __device__ static float silu(float v) { return v / (1.f + __expf(-v)); }
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
@@ -248,6 +259,8 @@ struct EpiHeads {
   int layer, n_slots, cap;
   int ring;              // cells form a ring (attention window): position pos in cell pos mod cap
   int n_seq;             // mode 0: slots in this pass
+  int window;            // attention window (ring), else 0
+  int prefetch_kv;       // mode 0: prefetch the layer's context K/V into L2 for the attention
   const int32_t* anchor_pos;
   const int32_t* block_len;
   int slot;              // mode 1
@@ -257,6 +270,47 @@ struct EpiHeads {
 
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
+
+  // Draft QKV (mode 0), producer lane after the dependent-launch wait: CTA
+  // cta of G asks L2 for its share of this layer's context K and V cells
+  // (positions [lo, p) of every slot and kv head, the cells the attention
+  // reads next; evict-last, so the weight stream does not displace them).
+  __device__ void producer_start(const GemvArgs&, int cta, int G) const {
+    if (mode != 0 || !prefetch_kv) return;
+    const uint64_t pol = l2_policy_evict_last();
+    const long long row_bytes = static_cast<long long>(d) * 2;
+    // total bytes over (slot, K/V, kv head) ranges, in cells
+    for (int s = 0; s < n_seq; ++s) {
+      const int p = anchor_pos[s];
+      int lo = 0;
+      if (ring) lo = p - (window - DFLASH_MAX_BLOCK) > 0 ? p - (window - DFLASH_MAX_BLOCK) : 0;
+      if (p <= lo) continue;
+      const long long n_pos = p - lo;
+      const long long per_cta = (n_pos + G - 1) / G;
+      const long long a0 = lo + per_cta * cta, a1 = a0 + per_cta < p ? a0 + per_cta : p;
+      if (a0 >= a1) continue;
+      for (int kvh = 0; kvh < n_kv; ++kvh)
+        for (int kv = 0; kv < 2; ++kv) {
+          const __half* base = (kv ? Vst : Kst) + static_cast<size_t>((layer * n_slots + s) * n_kv + kvh) * cap * d;
+          // a ring wraps at cap: at most two runs of cells
+          long long c0 = ring ? a0 % cap : a0;
+          long long left = a1 - a0;
+          while (left > 0) {
+            const long long run = (c0 + left <= cap) ? left : cap - c0;
+            const char* src = reinterpret_cast<const char*>(base + c0 * d);
+            long long bytes = run * row_bytes;
+            while (bytes > 0) {
+              const uint32_t b = static_cast<uint32_t>(bytes < (1 << 20) ? bytes : (1 << 20));
+              bulk_prefetch_l2(src, b, pol);
+              src += b;
+              bytes -= b;
+            }
+            left -= run;
+            c0 = 0;
+          }
+        }
+    }
+  }
 
   // Row metadata of activation row n: position, whether its K/V cells are
   // written, whether it is used at all (queries always are).
@@ -654,6 +708,7 @@ struct EpiArgmax {
       }
     L.bad = 0;
   }
+  __device__ void producer_start(const GemvArgs&, int, int) const {}
   __device__ void prologue(const GemvArgs&, int tid, const float* srs) const {
     if (final_hidden == nullptr || blockIdx.x != 0 || srs == nullptr) return;
     for (int i = tid; i < n_seq * 8 * H; i += 128) {

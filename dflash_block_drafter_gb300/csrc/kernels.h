@@ -20,12 +20,14 @@ struct EmbedArgs {
   int ring;  // cells form a ring (attention window): any position >= 0 fits
   int32_t* status;
   // optional (one slot): the first QKV GEMV's input, as PackNext writes it
-  // (BF16 hi/lo planes of x * w_next in the chunked layout of 8 rows and ku
-  // inputs per unit, per-64-column sums of squares)
-  __nv_bfloat16* xn;
+  // (x * w_next in the chunked layout of 8 rows and ku inputs per unit: one
+  // FP16 plane when f16, else BF16 hi/lo planes; per-64-column sums of
+  // squares)
+  void* xn;
   float* ssq;
   const float* w_next;
   int ku;
+  int f16;
 };
 
 // out = RMSNorm(x) * w in the chunked streamed-X layout (layout.cuh) of a

@@ -135,6 +135,18 @@ __device__ __forceinline__ uint32_t q8_pair(uint32_t word, uint32_t sel) {
     return pack_bf16x2(f.x, f.y);
   }
 }
+// The four nibble pairs of a Q4 word -> FP16 (e - 8) pairs, exact: pairs 0
+// and 2 as 0x6400 | n = 1024 + n minus 1032; pairs 1 and 3 taken in place
+// (bits 4..7 / 20..23) as 0x6400 | 16 n = 1024 + 16 n, times 1/16 minus 72
+// in one fused multiply-add (every intermediate is an exact FP16 integer).
+__device__ __forceinline__ void q4_word_f16(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  const uint32_t w8 = w >> 8;
+  p0 = hsub2_u32((w & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+  p1 = hfma2_u32((w & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+  p2 = hsub2_u32((w8 & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+  p3 = hfma2_u32((w8 & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+}
+
 // Nibble pair j of a Q4 word -> (e2j - 8, e2j+1 - 8), exact.  0x6400 | n is
 // the FP16 1024 + n; 0x4300 | n is the BF16 128 + n (n < 128).
 template <bool F16>
@@ -206,7 +218,10 @@ __device__ __forceinline__ BlockFrag decode_block(uint32_t ubase, int w, int lan
     const __half2 d = *reinterpret_cast<const __half2*>(&scb);
     f.d_r = __low2float(d);
     f.d_r8 = __high2float(d);
-    if constexpr (WT == WT_Q4_0) {
+    if constexpr (WT == WT_Q4_0 && F16) {
+      q4_word_f16(wr, f.a[0][0], f.a[0][2], f.a[1][0], f.a[1][2]);
+      q4_word_f16(wr8, f.a[0][1], f.a[0][3], f.a[1][1], f.a[1][3]);
+    } else if constexpr (WT == WT_Q4_0) {
       f.a[0][0] = q4_pair<F16>(wr, 0); f.a[0][1] = q4_pair<F16>(wr8, 0);
       f.a[0][2] = q4_pair<F16>(wr, 1); f.a[0][3] = q4_pair<F16>(wr8, 1);
       f.a[1][0] = q4_pair<F16>(wr, 2); f.a[1][1] = q4_pair<F16>(wr8, 2);
@@ -245,7 +260,10 @@ __device__ __forceinline__ void decode_pair(uint32_t ubase, int w, int lane, int
     const __half2 d = *reinterpret_cast<const __half2*>(&scb);
     f.d_r = __low2float(d);
     f.d_r8 = __high2float(d);
-    if constexpr (WT == WT_Q4_0) {
+    if constexpr (WT == WT_Q4_0 && F16) {
+      q4_word_f16(wr, f.a[0][0], f.a[0][2], f.a[1][0], f.a[1][2]);
+      q4_word_f16(wr8, f.a[0][1], f.a[0][3], f.a[1][1], f.a[1][3]);
+    } else if constexpr (WT == WT_Q4_0) {
       f.a[0][0] = q4_pair<F16>(wr, 0); f.a[0][1] = q4_pair<F16>(wr8, 0);
       f.a[0][2] = q4_pair<F16>(wr, 1); f.a[0][3] = q4_pair<F16>(wr8, 1);
       f.a[1][0] = q4_pair<F16>(wr, 2); f.a[1][1] = q4_pair<F16>(wr8, 2);

@@ -225,11 +225,17 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
                                    __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xffff0000u));
       reinterpret_cast<float4*>(xr)[c] = v;
       const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w_next) + c);
-      uint2 hi, lo;
-      split_bf16x2(v.x * wv.x, v.y * wv.y, hi.x, lo.x);
-      split_bf16x2(v.z * wv.z, v.w * wv.w, hi.y, lo.y);
-      *reinterpret_cast<uint2*>(a.xn + xchunk_index(4 * c, n, 0, 8, a.ku, 2)) = hi;
-      *reinterpret_cast<uint2*>(a.xn + xchunk_index(4 * c, n, 1, 8, a.ku, 2)) = lo;
+      if (a.f16) {
+        *reinterpret_cast<uint2*>(static_cast<__half*>(a.xn) + xchunk_index(4 * c, n, 0, 8, a.ku, 1)) =
+            make_uint2(pack_f16x2(v.x * wv.x, v.y * wv.y), pack_f16x2(v.z * wv.z, v.w * wv.w));
+      } else {
+        uint2 hi, lo;
+        split_bf16x2(v.x * wv.x, v.y * wv.y, hi.x, lo.x);
+        split_bf16x2(v.z * wv.z, v.w * wv.w, hi.y, lo.y);
+        __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(a.xn);
+        *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 0, 8, a.ku, 2)) = hi;
+        *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 1, 8, a.ku, 2)) = lo;
+      }
       ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
 #pragma unroll
