@@ -38,8 +38,6 @@ unsigned long long* trace_slot(State& st) {
 
 using namespace dflash;
 
-struct dflash_model : public Model {};
-struct dflash_state : public State {};
 
 namespace {
 

@@ -141,8 +141,6 @@ struct EpiArgmaxRows : public EpiArgmax<1> {
 
 using namespace dflash;
 
-struct dflash_model : public Model {};
-
 extern "C" int dflash_head_argmax_static(const dflash_model* m, const float* hidden, int32_t n_rows, int32_t* ids,
                                          int32_t* dev_status, dflash_stream_t stream_) {
   if (!m || !hidden || !ids) return DFLASH_ERR_INVALID_ARG;
@@ -151,6 +149,11 @@ extern "C" int dflash_head_argmax_static(const dflash_model* m, const float* hid
   // sizes beyond the fixed scratch array are refused, never truncated
   if (n_rows > kStaticMaxRows || c.hidden > kStaticMaxHidden || c.vocab > kStaticMaxVocab)
     return DFLASH_ERR_CAPACITY;
+  // the model's tensors (and the scratch array used below) belong to the
+  // device that was current at model creation: it must be current now
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (dev != m->device) return DFLASH_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return DFLASH_ERR_CUDA;

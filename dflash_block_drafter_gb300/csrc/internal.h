@@ -121,3 +121,8 @@ struct State {
 };
 
 }  // namespace dflash
+
+// The opaque handles of the C ABI (include/dflash.h) are the library's model
+// and state; defined once here for every translation unit that uses them.
+struct dflash_model : public dflash::Model {};
+struct dflash_state : public dflash::State {};

@@ -358,10 +358,12 @@ int dflash_state_read_draft_probs(const dflash_state* state, float* out, dflash_
  *   ids:    [n_rows] int32 out: argmax over the vocabulary of head . row
  *           (ties to the lowest id), computed exactly as the draft pass does.
  * Returns DFLASH_ERR_CAPACITY when n_rows > 8, hidden > 8192 or vocab >
- * 262144 (the fixed scratch's limits).  The first call on each device looks
- * up the scratch array's device address; make it before any stream capture.
- * All calls share the one scratch array: calls that overlap on the GPU race
- * (order them on one stream).  Each call clears the counters it relies on. */
+ * 262144 (the fixed scratch's limits), and DFLASH_ERR_INVALID_ARG when the
+ * current device is not the one the model was created on.  ids[n_rows..7]
+ * are not written.  The first call on each device looks up the scratch
+ * array's device address; make it before any stream capture.  All calls
+ * share the one scratch array: calls that overlap on the GPU race (order
+ * them on one stream).  Each call clears the counters it relies on. */
 int dflash_head_argmax_static(const dflash_model* model, const float* hidden, int32_t n_rows, int32_t* ids,
                               int32_t* dev_status, dflash_stream_t stream);
 
