@@ -46,9 +46,11 @@ UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
 # DRAM bytes (read + write) of one LM-head launch at this workload, from one
-# ncu capture of that kernel (6.195 TB/s x 126.11 us).  Reset to None whenever
-# the head kernel changes.
-HEAD_TRAFFIC_BYTES = 781.3e6
+# ncu capture of that kernel (dram__bytes_read.sum 778097920 +
+# dram__bytes_write.sum 2913280).  Reset to None whenever the head kernel
+# changes.
+HEAD_TRAFFIC_BYTES = 781011200
+HEAD_TRAFFIC_SOURCE = "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one LM-head launch, commit 0abd8a6"
 
 
 def load_peaks():
@@ -78,6 +80,42 @@ def algorithmic_bytes(cfg, ctx: int, B: int, n_fuse: int) -> dict:
     fuse = (shapes["fc"][0] * shapes["fc"][1] + kv_params) * bpw + n_fuse * cfg.tap_width * 2 \
         + L * 2 * nkv * n_fuse * d * 2
     return {"draft": int(draft), "fuse": int(fuse), "head": int(head), "step": int(draft + fuse)}
+
+
+def draft_bytes(cfg, ctx: int, B: int) -> int:
+    """Algorithmic bytes of one draft pass of one sequence (weights, LM head,
+    context K/V read, block K/V written, embedding rows)."""
+    return algorithmic_bytes(cfg, ctx, B, 0)["draft"]
+
+
+def cpu_model() -> str:
+    """The host CPU's name as the kernel reports it (x86 'model name', or the
+    Arm implementer / part codes)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "CPU implementer" in fields:
+        return f"Arm implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
+def replay_stats(event_pairs, per_replay: int) -> dict:
+    """Median / min / max per step from (start, end) CUDA-event pairs around
+    graph replays of `per_replay` steps each."""
+    ms = sorted(a.elapsed_time(b) / per_replay for a, b in event_pairs)
+    return {"median_ms": statistics.median(ms), "min_ms": ms[0], "max_ms": ms[-1], "replays": len(ms),
+            "steps_per_replay": per_replay}
 
 
 class ClockSampler:
@@ -196,6 +234,24 @@ def oracle_baseline(ckpt, cfg, budget_s: float = 12.0, max_steps: int = 1000):
             "seconds": dt}
 
 
+def oracle_one_thread(budget_s: float = 10.0) -> dict:
+    """The same oracle cycle with every BLAS / OpenMP pool limited to one
+    thread, in a child process (the pools size themselves at import)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, dflash_synth as synth; "
+            "cfg = synth.CONFIGS[bench.WORKLOAD]; ck = synth.make_checkpoint(cfg, seed=0, threads=1); "
+            "r = bench.oracle_baseline(ck, cfg, budget_s=%r, max_steps=1000); r['cores'] = 1; "
+            "print(json.dumps(r))") % (ROOT, budget_s)
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=budget_s * 6 + 120)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, never fatal
+        return {"error": str(e)[:200]}
+
+
 def run_reference(args, rank: int):
     if rank != 0:
         return
@@ -252,6 +308,127 @@ def state_capacity(cfg) -> int:
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
+def _fill_context_random(st, cfg, slot, n, dev, seed):
+    """Seeded N(0, 1) FP16 K/V for positions [0, n) of one slot (the draft
+    pass's work does not depend on the values)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    for l in range(cfg.n_layers):
+        k = torch.randn(cfg.n_kv_heads, n, cfg.head_dim, device=dev, generator=g).half()
+        v = torch.randn(cfg.n_kv_heads, n, cfg.head_dim, device=dev, generator=g).half()
+        st.write_kv(slot, l, 0, k, v)
+
+
+def _time_graph(fn, stream, G: int, n_rep: int) -> dict:
+    """Capture G calls of fn in one CUDA graph and time n_rep replays with an
+    event pair around each (median / min / max per call)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(G):
+            fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+    with torch.cuda.stream(stream):
+        graph.replay()
+        for a, b in ev:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    stream.synchronize()
+    r = replay_stats(ev, G)
+    r["mean_ms"] = ev[0][0].elapsed_time(ev[-1][1]) / (G * n_rep)
+    return r
+
+
+def time_weight_type(wt: str, dev, peak: float, n_rep: int = 20) -> dict:
+    """Device-timed draft pass and draft cycle of the full geometry at an
+    8192-position context with the given backbone type (graph replays)."""
+    import torch
+    from dflash_block_drafter_gb300.runtime import DraftModel, DraftState, accept
+    cfg = synth.CONFIGS["full_bf16"].with_(weight_type=wt)
+    ctx, B = cfg.ctx, cfg.block
+    ck = synth.make_checkpoint(cfg, seed=0)
+    model = DraftModel(cfg, ck, device=dev)
+    del ck
+    st = DraftState(model, 1, ctx + B)
+    _fill_context_random(st, cfg, 0, ctx, dev, seed=1)
+    st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = 17, ctx, B
+    taps = torch.as_tensor(synth.make_taps(cfg, FUSE_PER_STEP, seed=2).view(np.int16), device=dev)
+    fpos = torch.arange(ctx - FUSE_PER_STEP, ctx, dtype=torch.int32, device=dev)
+    tgt = torch.zeros((1, B), dtype=torch.int32, device=dev)
+    acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def draft():
+        st.draft(1, want_hidden=False, stream=stream)
+
+    def cycle():
+        st.fuse(0, taps, fpos, stream=stream)
+        draft()
+        accept(st.drafts, tgt, st.block_len, acc, nxt, stream=stream)
+
+    d = _time_graph(draft, stream, 10, n_rep)
+    c = _time_graph(cycle, stream, 10, n_rep)
+    status = st.take_status()
+    ab = algorithmic_bytes(cfg, ctx, B, FUSE_PER_STEP)
+    gbs = ab["draft"] / (d["median_ms"] * 1e-3) / 1e9
+    out = {"draft_passes_per_s": 1e3 / d["median_ms"], "draft_us": d["median_ms"] * 1e3,
+           "draft_us_min_max": [d["min_ms"] * 1e3, d["max_ms"] * 1e3],
+           "drafted_tok_per_s": (B - 1) * 1e3 / d["median_ms"],
+           "draft_bytes": ab["draft"], "achieved_gbs": gbs, "frac": gbs / peak,
+           "cycles_per_s": 1e3 / c["median_ms"], "cycle_us": c["median_ms"] * 1e3,
+           "cycle_frac": ab["step"] / (c["median_ms"] * 1e-3) / 1e9 / peak, "device_status": status,
+           "timing": f"median of {n_rep} CUDA-graph replays of 10 calls"}
+    st.close()
+    model.close()
+    del st, model
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_batched_mix(dev, peak: float, n_rep: int = 10) -> dict:
+    """The batched serving mix: 16 sequences, Q4_0 backbone, contexts
+    U[2048, 32768], blocks U{2..8} (seeded), one dflash_draft_block call per
+    step over all 16 slots."""
+    import torch
+    from dflash_block_drafter_gb300.runtime import DraftModel, DraftState
+    cfg = synth.CONFIGS["batched_q4_0"]
+    ctxs, Bs = synth.batched_mix(cfg, seed=34)
+    ck = synth.make_checkpoint(cfg, seed=0)
+    model = DraftModel(cfg, ck, device=dev)
+    del ck
+    cap = int(ctxs.max()) + 8
+    st = DraftState(model, cfg.n_seq, cap)
+    for s in range(cfg.n_seq):
+        _fill_context_random(st, cfg, s, int(ctxs[s]), dev, seed=100 + s)
+    st.anchor_tok[:] = torch.as_tensor(synth.make_token_ids(cfg, cfg.n_seq, seed=34), device=dev)
+    st.anchor_pos[:] = torch.as_tensor(ctxs, device=dev)
+    st.block_len[:] = torch.as_tensor(Bs, device=dev)
+    stream = torch.cuda.Stream(dev)
+    d = _time_graph(lambda: st.draft(cfg.n_seq, want_hidden=False, stream=stream), stream, 5, n_rep)
+    status = st.take_status()
+    one = algorithmic_bytes(cfg, 0, 0, 0)  # weights and head once per pass
+    kv = sum(cfg.n_layers * 2 * cfg.n_kv_heads * (int(c) + int(b)) * cfg.head_dim * 2 for c, b in zip(ctxs, Bs))
+    byts = one["draft"] + kv
+    gbs = byts / (d["median_ms"] * 1e-3) / 1e9
+    out = {"workload": "16 sequences, Q4_0 backbone, contexts U[2048, 32768], blocks U{2..8} (seed 34), "
+                       "context K/V pre-filled", "pass_us": d["median_ms"] * 1e3,
+           "sequence_passes_per_s": cfg.n_seq * 1e3 / d["median_ms"],
+           "drafted_tok_per_s": float(np.sum(Bs - 1)) * 1e3 / d["median_ms"],
+           "bytes_per_pass": int(byts), "achieved_gbs": gbs, "frac": gbs / peak, "device_status": status,
+           "timing": f"median of {n_rep} CUDA-graph replays of 5 passes"}
+    st.close()
+    model.close()
+    del st, model
+    torch.cuda.empty_cache()
+    return out
+
 def run_gpu(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -332,12 +509,16 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    n_rep = args.steps // G
+    rep_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
     with ClockSampler(local_rank) as clocks:
         time.sleep(0.15)
         with torch.cuda.stream(stream):
             t_beg.record(stream)
-            for _ in range(args.steps // G):
+            for a, b in rep_ev:
+                a.record(stream)
                 graph.replay()
+                b.record(stream)
             t_end.record(stream)
         torch.cuda.synchronize(dev)
         time.sleep(0.15)
@@ -354,15 +535,16 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     with torch.cuda.graph(dgraph, stream=stream):
         st.draft(1, want_hidden=False, stream=stream)
     with torch.cuda.stream(stream):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_draft = max(20, args.steps // 4)
         dgraph.replay()
-        e0.record(stream)
-        for _ in range(n_draft):
+        d_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_draft)]
+        for a, b in d_ev:
+            a.record(stream)
             dgraph.replay()
-        e1.record(stream)
+            b.record(stream)
     torch.cuda.synchronize(dev)
-    draft_only_ms = e0.elapsed_time(e1) / n_draft
+    draft_stats = replay_stats(d_ev, 1)
+    draft_only_ms = d_ev[0][0].elapsed_time(d_ev[-1][1]) / n_draft
     one = torch.cuda.CUDAGraph()  # one cycle, for the end-to-end loop
     with torch.cuda.graph(one, stream=stream):
         step()
@@ -416,13 +598,16 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "DFlash geometry, N(0,1) taps)",
         "config": config_block(cfg),
         "drafted_tok_per_s": value * (B - 1),
+        "draft_passes_per_s": 1e3 / draft_stats["median_ms"],
         "draft_only_ms": draft_only_ms,
+        "draft_stats": draft_stats,
+        "step_stats": replay_stats(rep_ev, G),
         "achieved_gbs_step": step_gbs,
         "algorithmic_bytes_per_step": ab["step"],
         "roofline": {"bound": "hbm", "kernel": "lm_head_argmax (gemv_kernel<WT_HEAD>)",
                      "achieved": head_gbs, "peak": peak, "unit": "GB/s", "frac": head_gbs / peak,
-                     "peak_kind": peak_kind, "traffic": HEAD_TRAFFIC_BYTES, "bytes_per_launch": ab["head"],
-                     "avg_launch_ms": head_avg_ms},
+                     "peak_kind": peak_kind, "traffic": HEAD_TRAFFIC_BYTES, "traffic_source": HEAD_TRAFFIC_SOURCE,
+                     "bytes_per_launch": ab["head"], "avg_launch_ms": head_avg_ms},
         "step_roofline": {"achieved": step_gbs, "peak": peak, "frac": step_gbs / peak, "unit": "GB/s"},
         "e2e": {"value": replica_throughput(world, n_e2e, e2e_s * 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e},
@@ -432,8 +617,32 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "clocks": clocks.summary(),
         "setup_s": setup_s,
     }
+    if not args.no_extras:
+        draft_ab = algorithmic_bytes(cfg, ctx, B, FUSE_PER_STEP)
+        per = {cfg.weight_type: {
+            "draft_passes_per_s": 1e3 / draft_stats["median_ms"], "draft_us": draft_stats["median_ms"] * 1e3,
+            "draft_us_min_max": [draft_stats["min_ms"] * 1e3, draft_stats["max_ms"] * 1e3],
+            "drafted_tok_per_s": (B - 1) * 1e3 / draft_stats["median_ms"], "draft_bytes": draft_ab["draft"],
+            "achieved_gbs": draft_ab["draft"] / (draft_stats["median_ms"] * 1e-3) / 1e9,
+            "frac": draft_ab["draft"] / (draft_stats["median_ms"] * 1e-3) / 1e9 / peak,
+            "cycles_per_s": value, "cycle_us": ms_per_step * 1e3, "cycle_frac": step_gbs / peak,
+            "timing": "the headline run above"}}
+        del graph, dgraph, one
+        st.close()
+        model.close()
+        torch.cuda.empty_cache()
+        if cfg.ctx == 8192 and getattr(cfg, "attn_window", 0) == 0:
+            for wt in ("q8_0", "q5_0", "q4_0"):
+                if wt != cfg.weight_type:
+                    per[wt] = time_weight_type(wt, dev, peak)
+        line["per_weight_type"] = per
+        line["batched_mix"] = time_batched_mix(dev, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in oracle_baseline(ckpt, cfg).items() if k != "seconds"}
+        line["cpu_baseline"]["cpu_model"] = cpu_model()
+        one_t = oracle_one_thread()
+        line["cpu_baseline"]["one_thread"] = {k: v for k, v in one_t.items() if k in ("value", "unit", "cores",
+                                                                                     "sample", "error")}
     print(json.dumps(line), flush=True)
 
 
@@ -445,6 +654,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--weight-type", default=None, choices=[None, "bf16", "q8_0", "q5_0", "q4_0"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-weight-type and batched-mix timings that follow the headline run")
     ap.add_argument("--ctx", type=int, default=0, help="anchor position p (default: the workload's 8192)")
     ap.add_argument("--window", type=int, default=0, help="drafter attention window over a ring of cells (0: none)")
     args = ap.parse_args()
