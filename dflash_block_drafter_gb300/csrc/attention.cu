@@ -34,6 +34,8 @@ struct AttnArgs {
                           // [max(0, p + B - W), p + B) in a ring, cell = position mod cap
   int32_t* status;
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
+  const __half* kbase_ptr;    // the K / V arenas (rows of d halves) the maps address
+  const __half* vbase_ptr;
 };
 
 #ifdef DFLASH_TRACE
@@ -246,6 +248,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           for (int b = 0; b < Geo::BOXES; ++b)
             tma_load_2d(sk + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.kmap, b * 64, y + t * kTcKT, kfull);
       };
+      // tiles kLookAhead super-tiles ahead are asked of L2, so that long
+      // chunks find their next K / V there instead of waiting on HBM
+      constexpr int kLookAhead = 2;
+      auto prefetch_tile = [&](int j) {
+        if (j >= nst) return;
+        const int row = tile_row(j);
+        // the super-tile's cells that exist in this (layer, slot, kv head) slab
+        const int n_rows = min(kTcKS, row0 + a.cap - row);
+        if (n_rows <= 0) return;
+        const uint32_t bytes = static_cast<uint32_t>(n_rows * D * 2);
+        bulk_prefetch_l2_plain(a.kbase_ptr + static_cast<size_t>(row) * D, bytes);
+        bulk_prefetch_l2_plain(a.vbase_ptr + static_cast<size_t>(row) * D, bytes);
+      };
       auto issue_v = [&](int j) {
         const int y = tile_row(j);
         mbar_arrive_expect_tx(vfull, 2 * Geo::TILE_BYTES);
@@ -269,8 +284,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         issue_k(0);
         issue_v(0);
       }
+      for (int j = 1; j <= kLookAhead; ++j) prefetch_tile(j);
       int nk = 1, nv = 1;  // super-tiles issued
       for (int j = 1; j < nst; ++j) {
+        prefetch_tile(j + kLookAhead);
         if (!mbar_wait(kfree, (j - 1) & 1)) { ok = false; break; }
         issue_k(j);
         ++nk;
@@ -311,15 +328,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         umma_commit(kfree);
         return true;
       };
-      // QK^T of super-tile j + 1 is issued before the PV of super-tile j, so it
-      // runs while the softmax warps work on S[j % 2].
+      // QK^T of super-tile j + 1 runs while the softmax warps work on S[j % 2]:
+      // it is issued as soon as its K tile (and S buffer) is there, and the PV
+      // of super-tile j as soon as P_j and V_j are -- whichever is ready first
+      // goes first, so a late K tile never holds up the PV before it.
       const bool qok = mbar_wait(qfull, 0);
       DFLASH_ATTN_STAMP(9);
       if (!qok || !issue_qk(0)) ok = false;
       DFLASH_ATTN_STAMP(11);
       for (int j = 0; j < nst && ok; ++j) {
-        if (j + 1 < nst && !issue_qk(j + 1)) { ok = false; break; }
-        if (!mbar_wait(pfull, j & 1) || !mbar_wait(vfull, j & 1)) { ok = false; break; }
+        bool qk_next = j + 1 < nst;
+        {
+          const unsigned long long t0 = globaltimer_ns();
+          for (int spin = 0;; ++spin) {
+            if (qk_next && mbar_test(kfull, (j + 1) & 1) &&
+                (j + 1 < 2 || mbar_test(&sfree[(j + 1) & 1], (((j + 1) >> 1) - 1) & 1))) {
+              if (!issue_qk(j + 1)) { ok = false; break; }
+              qk_next = false;
+            }
+            if (mbar_test(pfull, j & 1) && mbar_test(vfull, j & 1)) break;
+            if ((spin & 63) == 63 && globaltimer_ns() - t0 > kWaitTimeoutNs) { ok = false; break; }
+          }
+          if (!ok) break;
+        }
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -330,6 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           }
         umma_commit(pfree);
         umma_commit(vfree);
+        if (qk_next && !issue_qk(j + 1)) { ok = false; break; }
       }
       // tensor memory may only be freed once every issued MMA has finished
       umma_commit(mdone);
@@ -724,6 +756,8 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.status = status;
   a.qmap = st.q_map;
   a.trace = trace_slot(st);
+  a.kbase_ptr = st.K;
+  a.vbase_ptr = st.V;
   cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.C, a.n_kv, n_seq), stream, true);
   if (e != cudaSuccess || a.C == 1) return e;
   if (st.prof_n > 0 && st.prof_k < st.prof_n)

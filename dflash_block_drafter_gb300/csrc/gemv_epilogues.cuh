@@ -279,6 +279,18 @@ struct EpiHeads {
     if (mode != 0 || !prefetch_kv) return;
     const uint64_t pol = l2_policy_evict_last();
     const long long row_bytes = static_cast<long long>(d) * 2;
+    {
+      // only a layer's K/V that L2 holds comfortably beside the weight
+      // stream (longer contexts stream their K/V in the attention itself)
+      long long total = 0;
+      for (int s = 0; s < n_seq; ++s) {
+        const int p = anchor_pos[s];
+        int lo = 0;
+        if (ring) lo = p - (window - DFLASH_MAX_BLOCK) > 0 ? p - (window - DFLASH_MAX_BLOCK) : 0;
+        if (p > lo) total += static_cast<long long>(p - lo) * n_kv * 2 * row_bytes;
+      }
+      if (total > (32ll << 20)) return;
+    }
     // total bytes over (slot, K/V, kv head) ranges, in cells
     for (int s = 0; s < n_seq; ++s) {
       const int p = anchor_pos[s];
