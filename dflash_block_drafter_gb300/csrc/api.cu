@@ -843,20 +843,46 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.status = status;
     if (packed) {
       set_packed(a);
-    } else {
-      NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8,
-                  32 * Fmt<WT_HEAD>::CB};
+      LaunchCfg lc{stream, grid_for(*m, a), true};
+      if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
       prof_mark(s, stream);
-      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "final norm"));
-      a.X = s->xnorm;
-      a.ldx = H;
-      p.final_hidden = nullptr;
+      TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
+      if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
+    } else {
+      // Up to 8 slots (64 rows) per head launch: a 128-row tile would spill
+      // the argmax epilogue's registers, so 16 slots take two launches, each
+      // over its own half of the rows (the head is streamed once per launch).
+      const int halves = nt > 8 ? nt / 8 : 1;
+      const int hnt = nt > 8 ? 8 : nt;
+      const int hr = hnt * 8;
+      const size_t half_elems = xchunk_elems(H, hr, 32 * Fmt<WT_HEAD>::CB, 2);
+      for (int h = 0; h < halves; ++h) {
+        const int rows_f32 = n_seq * 8 - h * hr;
+        NormArgs na{s->x + static_cast<size_t>(h) * hr * H, m->final_norm,
+                    static_cast<__nv_bfloat16*>(s->xnorm) + h * half_elems, 0, H, hr, c.norm_eps,
+                    final_hidden ? final_hidden + static_cast<size_t>(h) * hr * H : nullptr,
+                    rows_f32 < 0 ? 0 : (rows_f32 > hr ? hr : rows_f32), 32 * Fmt<WT_HEAD>::CB};
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_rmsnorm_rows(na, hr, stream), "final norm"));
+        GemvArgs ah = a;
+        ah.n_valid_rows = hr;
+        ah.X = static_cast<__nv_bfloat16*>(s->xnorm) + h * half_elems;
+        ah.ldx = H;
+        ArgmaxParams ph = p;
+        ph.final_hidden = nullptr;
+        ph.n_seq = n_seq - h * hnt > hnt ? hnt : n_seq - h * hnt;
+        ph.block_len = block_len + h * hnt;
+        ph.drafts = drafts + static_cast<size_t>(h) * hnt * (DFLASH_MAX_BLOCK - 1);
+        ph.probs = s->draft_probs + static_cast<size_t>(h) * hnt * (DFLASH_MAX_BLOCK - 1);
+        if (ph.n_seq <= 0) break;
+        LaunchCfg lc{stream, grid_for(*m, ah), true};
+        if (h == 0 && s->head_ev_begin)
+          CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
+        prof_mark(s, stream);
+        TRY(check_gemv(gemv_argmax(hnt, ah, ph, lc), "lm head"));
+      }
+      if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
     }
-    LaunchCfg lc{stream, grid_for(*m, a), true};
-    if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
-    prof_mark(s, stream);
-    TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
-    if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
   }
   prof_mark(s, stream);
   return DFLASH_OK;
@@ -960,9 +986,11 @@ int dflash_model_dequantize(const dflash_model* m, int32_t which, float* out, df
 int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   if (!s || n_seq < 1 || n_seq > s->n_slots) return -1;
   const int L = s->model->cfg.n_layers;
-  const bool streamed = !fused_norm(pow2ceil(n_seq));  // separate RMSNorm kernels
+  const int nt = pow2ceil(n_seq);
+  const bool streamed = !fused_norm(nt);  // separate RMSNorm kernels
   const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
-  return 1 + L * per_layer + 1 + (streamed ? 1 : 0);
+  const int head_launches = nt > 8 ? (n_seq + 7) / 8 : 1;  // 8 slots per head launch
+  return 1 + L * per_layer + head_launches * (streamed ? 2 : 1);
 }
 
 int32_t dflash_fuse_launches(const dflash_state* s, int32_t n) {
