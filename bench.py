@@ -358,6 +358,7 @@ def time_weight_type(wt: str, dev, peak: float, n_rep: int = 20) -> dict:
     del ck
     st = DraftState(model, 1, ctx + B)
     _fill_context_random(st, cfg, 0, ctx, dev, seed=1)
+    st.set_defer_kv(True)  # the committed rows' K/V ride in the next pass's QKV GEMVs
     st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = 17, ctx, B
     taps = torch.as_tensor(synth.make_taps(cfg, FUSE_PER_STEP, seed=2).view(np.int16), device=dev)
     fpos = torch.arange(ctx - FUSE_PER_STEP, ctx, dtype=torch.int32, device=dev)
@@ -463,6 +464,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     fuse_taps = torch.as_tensor(synth.make_taps(cfg, FUSE_PER_STEP, seed=2).view(np.int16), device=dev)
     fuse_pos = torch.arange(ctx - FUSE_PER_STEP, ctx, dtype=torch.int32, device=dev)
+    # each cycle's 8 committed rows: the fc projection in the fusion call, their
+    # K/V inside the next draft pass's QKV GEMVs (dflash_state_set_defer_kv)
+    st.set_defer_kv(not args.no_defer_kv)
     anchor = int(synth.make_token_ids(cfg, 1, seed=3)[0])
     st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = anchor, ctx, B
     tgt_np = synth.make_target_ids(np.zeros(B - 1, np.int32), cfg.vocab, seed=4, p_agree=0.0)[None]
@@ -597,7 +601,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.weight_type, "data": "synthetic (seeded; random-init weights of the "
         "DFlash geometry, N(0,1) taps)",
-        "config": config_block(cfg),
+        "config": dict(config_block(cfg), committed_kv=("separate launch in the fusion call" if args.no_defer_kv else
+                                                         "projected inside the next draft pass's QKV GEMVs")),
         "drafted_tok_per_s": value * (B - 1),
         "draft_passes_per_s": 1e3 / draft_stats["median_ms"],
         "draft_only_ms": draft_only_ms,
@@ -657,6 +662,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-weight-type and batched-mix timings that follow the headline run")
+    ap.add_argument("--no-defer-kv", action="store_true",
+                    help="project each cycle's committed rows' K/V in a separate launch of the fusion call")
+    ap.add_argument("--batched-mix-only", action="store_true",
+                    help="time only the 16-sequence batched mix and print its figures as one JSON line")
     ap.add_argument("--ctx", type=int, default=0, help="anchor position p (default: the workload's 8192)")
     ap.add_argument("--window", type=int, default=0, help="drafter attention window over a ring of cells (0: none)")
     args = ap.parse_args()
@@ -667,6 +676,14 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.batched_mix_only:
+        import torch
+        import dflash_block_drafter_gb300 as D
+        D.load_library()
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"batched_mix": time_batched_mix(dev, load_peaks()[0])}), flush=True)
         return
     if world > 1:
         import torch

@@ -110,6 +110,8 @@ _SIGS = {
     "dflash_state_set_profile_events": (ctypes.c_int, [_P, ctypes.POINTER(_P), _I]),
     "dflash_state_set_attn_chunks": (ctypes.c_int, [_P, _I, ctypes.POINTER(_I)]),
     "dflash_state_set_spec_min_p": (ctypes.c_int, [_P, ctypes.c_float]),
+    "dflash_state_set_defer_kv": (ctypes.c_int, [_P, _I]),
+    "dflash_state_flush": (ctypes.c_int, [_P, _P]),
     "dflash_state_read_draft_probs": (ctypes.c_int, [_P, _P, _P]),
     "dflash_head_argmax_static": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
 }
@@ -295,6 +297,14 @@ def dflash_state_set_profile_events(state: int, events) -> None:
 
 def dflash_state_set_spec_min_p(state: int, floor: float) -> None:
     _check(load_library().dflash_state_set_spec_min_p(state, floor), "dflash_state_set_spec_min_p")
+
+
+def dflash_state_set_defer_kv(state: int, on: bool) -> None:
+    _check(load_library().dflash_state_set_defer_kv(state, 1 if on else 0), "dflash_state_set_defer_kv")
+
+
+def dflash_state_flush(state: int, stream: int = 0) -> None:
+    _check(load_library().dflash_state_flush(state, stream or None), "dflash_state_flush")
 
 
 def dflash_state_read_draft_probs(state: int, out: int, stream: int = 0) -> None:

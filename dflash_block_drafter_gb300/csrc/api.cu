@@ -190,7 +190,7 @@ void free_state(State* s) {
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
   f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
-  f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->status);
+  f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
 }
 
 int pow2ceil(int v) {
@@ -564,6 +564,8 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->h_raw, size_t(s->fuse_rows) * H * 4, &total));
   STRY(dev_alloc(&s->kv_raw, size_t(s->fuse_rows) * L * 2 * nkv * d * 4, &total));
   STRY(dev_alloc(&s->fuse_xnorm, xchunk_elems(H, 128, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->fuse_xn, xchunk_elems(H, 8, 128, 2) * 2, &total));
+  STRY(dev_alloc(&s->fuse_ssq, size_t(H / 64) * 8 * 4, &total));
   STRY(dev_alloc(&s->status, 16, &total));
   if (cudaMemset(s->status, 0, 16) != cudaSuccess) return fail(cuda_fail(cudaGetLastError(), "cudaMemset"));
   STRY(make_map_2d(&s->q_map, s->q_ready, static_cast<uint64_t>(s->nt) * nkv * M, d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -589,6 +591,60 @@ int dflash_state_destroy(dflash_state* s) {
   return DFLASH_OK;
 }
 
+// K/V of every layer for `rows` fused rows (positions[rows] of `slot`) from
+// their x * hidden_norm: X in the chunked layout with the sums of squares ssq
+// (8-row tiles), or the rows already normalised (larger tiles, ssq null).
+static int launch_fuse_kv(const dflash_model* m, dflash_state* s, const void* X, const float* ssq, int rows,
+                          int nt, int32_t slot, const int32_t* positions, int32_t* status, cudaStream_t stream) {
+  const dflash_config& c = m->cfg;
+  const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers;
+  GemvArgs a = base_args(m->kv_all, *s, CNT_KV, status);
+  a.n_valid_rows = rows;
+  a.eps = c.norm_eps;
+  a.X = X;
+  a.ldx = H;
+  if (ssq) {
+    a.ssq = ssq;
+    a.n_ssq = H / 64;
+  }
+  EpiHeads e;
+  std::memset(&e, 0, sizeof(e));
+  e.mode = 1;
+  e.raw = s->kv_raw;
+  e.ldr = L * 2 * nkv * d;
+  e.d = d;
+  e.n_q = c.n_q_heads;
+  e.n_kv = nkv;
+  e.gph = d / 64;
+  e.head_cnt = s->counters + static_cast<size_t>(CNT_KV_HEADS) * s->counter_stride;
+  e.k_norm = m->k_norm;
+  e.turns = m->rope_turns;
+  e.eps = c.norm_eps;
+  e.q_scale = 1.f;
+  e.Kst = s->K;
+  e.Vst = s->V;
+  e.n_slots = s->n_slots;
+  e.cap = s->capacity;
+  e.ring = c.attn_window > 0;
+  e.slot = slot;
+  e.positions = positions;
+  e.n_valid = rows;
+  e.status = status;
+  e.rows_ = nt * 8;
+  LaunchCfg lc{stream, grid_for(*m, a), true};
+  if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
+  prof_mark(s, stream);
+  return check_gemv(gemv_heads_any(m->wtype, nt, a, e, lc), "fuse kv");
+}
+
+// Projects the K/V of a deferred 8-row fusion now (a separate GEMV).
+static int flush_deferred(const dflash_model* m, dflash_state* s, cudaStream_t stream) {
+  if (s->pend_n <= 0) return DFLASH_OK;
+  const int rows = s->pend_n;
+  s->pend_n = 0;
+  return launch_fuse_kv(m, s, s->fuse_xn, s->fuse_ssq, rows, 1, s->pend_slot, s->pend_pos, s->pend_status, stream);
+}
+
 int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, const uint16_t* taps,
                         const int32_t* positions, int32_t n, int32_t* dev_status, dflash_stream_t stream_) {
   if (!m || !s || s->model != m) return DFLASH_ERR_INVALID_ARG;
@@ -598,14 +654,20 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
   if (reinterpret_cast<uintptr_t>(taps) % 16) return DFLASH_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const dflash_config& c = m->cfg;
-  const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers;
+  const int H = c.hidden;
   const int wt = m->wtype;
   int32_t* status = dev_status ? dev_status : s->status;
   const int tw = c.n_taps * H;
   s->prof_k = 0;
+  // an earlier deferred fusion is projected first (its rows may be re-fused here)
+  TRY(flush_deferred(m, s, stream));
   for (int base = 0; base < n; base += s->fuse_rows) {
     const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
     const int nt = rows <= 8 ? 1 : 16;
+    // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
+    const bool fpacked = fused_norm(nt);
+    // a single 8-row tile of a deferring state leaves its K/V to the next draft pass
+    const bool defer = s->defer_kv && fpacked && n <= 8;
     // fc: h_raw = taps . W_fc^T
     {
       GemvArgs a = base_args(m->fc, *s, CNT_FC, status);
@@ -615,60 +677,30 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
       if (ku_of(wt) + 32 <= 256)
         TRY(make_rows_map(&a.xmap, a.X, static_cast<uint64_t>(rows), static_cast<uint64_t>(tw),
                           static_cast<uint32_t>(ku_of(wt)), static_cast<uint32_t>(rows)));
-      // with 8 rows the fc epilogue also packs h * hidden_norm for the K/V GEMV
-      const bool fpacked = fused_norm(nt);
-      EpiStore e{s->h_raw, H, PackNext{fpacked ? s->xn : nullptr, s->ssq, m->hidden_norm, ku_of(wt), wt != WT_BF16}};
+      EpiStore e{s->h_raw, H,
+                 PackNext{fpacked ? (defer ? s->fuse_xn : s->xn) : nullptr, defer ? s->fuse_ssq : s->ssq,
+                          m->hidden_norm, ku_of(wt), wt != WT_BF16}};
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
       prof_mark(s, stream);
       TRY(check_gemv(gemv_store_any(wt, nt, a, e, lc), "fuse fc"));
     }
+    if (defer) {
+      s->pend_n = rows;
+      s->pend_slot = slot;
+      s->pend_pos = positions + base;
+      s->pend_status = status;
+      continue;
+    }
     // K/V of every layer from rmsnorm(h_raw) * hidden_norm
-    {
-      GemvArgs a = base_args(m->kv_all, *s, CNT_KV, status);
-      a.n_valid_rows = rows;
-      a.eps = c.norm_eps;
-      if (fused_norm(nt)) {
-        a.X = s->xn;
-        a.ldx = H;
-        a.ssq = s->ssq;
-        a.n_ssq = H / 64;
-      } else {
-        NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0,
-                    ku_of(wt)};
-        prof_mark(s, stream);
-        TRY(check_gemv(launch_rmsnorm_rows(na, nt * 8, stream), "fuse norm"));
-        a.X = s->fuse_xnorm;
-        a.ldx = H;
-      }
-      EpiHeads e;
-      std::memset(&e, 0, sizeof(e));
-      e.mode = 1;
-      e.raw = s->kv_raw;
-      e.ldr = L * 2 * nkv * d;
-      e.d = d;
-      e.n_q = c.n_q_heads;
-      e.n_kv = nkv;
-      e.gph = d / 64;
-      e.head_cnt = s->counters + static_cast<size_t>(CNT_KV_HEADS) * s->counter_stride;
-      e.k_norm = m->k_norm;
-      e.turns = m->rope_turns;
-      e.eps = c.norm_eps;
-      e.q_scale = 1.f;
-      e.Kst = s->K;
-      e.Vst = s->V;
-      e.n_slots = s->n_slots;
-      e.cap = s->capacity;
-      e.ring = c.attn_window > 0;
-      e.slot = slot;
-      e.positions = positions + base;
-      e.n_valid = rows;
-      e.status = status;
-      e.rows_ = nt * 8;
-      LaunchCfg lc{stream, grid_for(*m, a), true};
-      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
+    if (fpacked) {
+      TRY(launch_fuse_kv(m, s, s->xn, s->ssq, rows, nt, slot, positions + base, status, stream));
+    } else {
+      NormArgs na{s->h_raw, m->hidden_norm, s->fuse_xnorm, wt != WT_BF16, H, rows, c.norm_eps, nullptr, 0,
+                  ku_of(wt)};
       prof_mark(s, stream);
-      TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "fuse kv"));
+      TRY(check_gemv(launch_rmsnorm_rows(na, nt * 8, stream), "fuse norm"));
+      TRY(launch_fuse_kv(m, s, s->fuse_xnorm, nullptr, rows, nt, slot, positions + base, status, stream));
     }
   }
   prof_mark(s, stream);
@@ -700,6 +732,19 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     a.ssq = s->ssq;
     a.n_ssq = H / 64;
   };
+  // A deferred fusion's rows ride in this pass's QKV GEMVs when every group
+  // of the widened GEMV gets CTAs of its own in clusters of one head:
+  // each layer's W_k / W_v groups are then read by two sets of CTAs at about
+  // the same time (block rows, committed rows) instead of once more in a
+  // separate launch.  Otherwise they are projected first, separately.
+  const int kv_groups = 2 * nkv * d / 64;
+  bool carry = false;
+  if (s->pend_n > 0 && packed) {
+    GemvArgs t = base_args(m->qkv[0], *s, CNT_QKV, status);
+    t.U += kv_groups * t.UPG;
+    carry = plan_cluster(t, grid_for(*m, t), d / 64) > 1 && (t.U / t.UPG) <= m->sm_count;
+  }
+  if (s->pend_n > 0 && !carry) TRY(flush_deferred(m, s, stream));
   {
     EmbedArgs ea{m->embed, anchor_tok, anchor_pos, block_len, s->x, H, c.vocab, c.mask_token_id, n_seq,
                  s->capacity, c.attn_window > 0, status, nullptr, nullptr, nullptr, 0, 0};
@@ -758,6 +803,20 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       e.block_len = block_len;
       e.status = status;
       e.rows_ = R;
+      if (carry) {
+        // the committed rows' K/V of this layer: W_k / W_v groups again, as
+        // extra groups over the deferred fusion's packed rows
+        a.U += kv_groups * a.UPG;
+        a.vgroups = kv_groups;
+        a.vwg0 = nq * d / 64;
+        a.X2 = s->fuse_xn;
+        a.ssq2 = s->fuse_ssq;
+        a.n_valid2 = s->pend_n;
+        e.n_heads0 = nq + 2 * nkv;
+        e.vpositions = s->pend_pos;
+        e.vn_valid = s->pend_n;
+        e.vslot = s->pend_slot;
+      }
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
       prof_mark(s, stream);
@@ -884,6 +943,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
     }
   }
+  if (carry) s->pend_n = 0;
   prof_mark(s, stream);
   return DFLASH_OK;
 }
@@ -919,6 +979,8 @@ int dflash_state_read_kv(const dflash_state* s, int32_t slot, int32_t layer, int
     return DFLASH_ERR_INVALID_ARG;
   const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // cells of a deferred fusion are projected before they are read
+  TRY(flush_deferred(static_cast<const dflash_model*>(s->model), const_cast<dflash_state*>(s), st));
   if (k_out)
     TRY(check_gemv(launch_kv_copy(false, s->K + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, k_out, nullptr, st),
                    "read k"));
@@ -938,6 +1000,8 @@ int dflash_state_write_kv(dflash_state* s, int32_t slot, int32_t layer, int32_t 
     return DFLASH_ERR_INVALID_ARG;
   const size_t off = static_cast<size_t>((layer * s->n_slots + slot) * c.n_kv_heads) * s->capacity * c.head_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // a deferred fusion's cells are written first, so later writes win as in call order
+  TRY(flush_deferred(static_cast<const dflash_model*>(s->model), s, st));
   if (k_in)
     TRY(check_gemv(launch_kv_copy(true, s->K + off, s->capacity, ring, c.head_dim, c.n_kv_heads, pos0, n, nullptr, k_in, st),
                    "write k"));
@@ -998,7 +1062,7 @@ int32_t dflash_fuse_launches(const dflash_state* s, int32_t n) {
   int k = 0;
   for (int base = 0; base < n; base += s->fuse_rows) {
     const int rows = (n - base) < s->fuse_rows ? (n - base) : s->fuse_rows;
-    k += fused_norm(rows <= 8 ? 1 : 16) ? 2 : 3;
+    k += fused_norm(rows <= 8 ? 1 : 16) ? ((s->defer_kv && n <= 8) ? 1 : 2) : 3;
   }
   return k;
 }
@@ -1010,6 +1074,18 @@ int dflash_state_set_attn_chunks(dflash_state* s, int32_t chunks, int32_t* max_c
   if (chunks < 1 || chunks > s->attn_chunks_max) return DFLASH_ERR_INVALID_ARG;
   s->attn_chunks = chunks;
   return DFLASH_OK;
+}
+
+int dflash_state_set_defer_kv(dflash_state* s, int32_t on) {
+  if (!s || (on != 0 && on != 1)) return DFLASH_ERR_INVALID_ARG;
+  if (!on && s->pend_n > 0) return DFLASH_ERR_INVALID_ARG;  // dflash_state_flush first
+  s->defer_kv = on;
+  return DFLASH_OK;
+}
+
+int dflash_state_flush(dflash_state* s, dflash_stream_t stream) {
+  if (!s) return DFLASH_ERR_INVALID_ARG;
+  return flush_deferred(static_cast<const dflash_model*>(s->model), s, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dflash_state_set_spec_min_p(dflash_state* s, float floor) {

@@ -42,6 +42,14 @@ struct GemvArgs {
   const float* ssq;
   int n_ssq;
   int rs_early;                  // X_NORM: 1 / RMS needed before the first group (final hidden rows)
+  // Extra groups (X_NORM, groups aligned to CTAs): the last vgroups of the
+  // U / UPG groups re-read weight groups [vwg0, vwg0 + vgroups) with their
+  // own activations X2, row sums of squares ssq2 and n_valid2 valid rows (an
+  // 8-row draft QKV GEMV that also projects the committed rows' K / V)
+  int vgroups, vwg0;
+  const void* X2;
+  const float* ssq2;
+  int n_valid2;
   // Cluster finishing (8-row passes): when cl_parts * cl_gph > 1 the grid is
   // launched in clusters of cl_parts * cl_gph CTAs covering cl_gph whole
   // 64-row groups (one attention head for the per-head epilogue), each group
@@ -161,6 +169,7 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   const int u_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.U) / G);
   const int u_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.U) / G);
   const int n_units = u_end - u_begin;
+  const int vu0 = a.U - a.vgroups * a.UPG;  // first unit of the extra groups (U: none)
 
   const int cl_size = Geo::kClusterable ? a.cl_parts * a.cl_gph : 1;
   if (tid == 0) {
@@ -209,7 +218,8 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
           tma_load_2d_hint(dst, &a.wmap, j * 128, g * 64, &full[it % STAGES], pol);
           tma_load_2d_hint(dst + 8192, &a.wmap, j * 128 + 64, g * 64, &full[it % STAGES], pol);
         } else {
-          bulk_g2s_hint(dst, a.W + static_cast<size_t>(u) * F::UNIT, F::UNIT, &full[it % STAGES], pol);
+          const int uw = u >= vu0 ? u - vu0 + a.vwg0 * a.UPG : u;
+          bulk_g2s_hint(dst, a.W + static_cast<size_t>(uw) * F::UNIT, F::UNIT, &full[it % STAGES], pol);
         }
       };
       auto issue_x = [&](int it, int u) {
@@ -217,8 +227,8 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
         if constexpr (XMODE == X_STREAM || XMODE == X_NORM) {
           // one contiguous chunk per plane
-          const uint8_t* src =
-              static_cast<const uint8_t*>(a.X) + static_cast<size_t>(j) * XPLANES * R * Geo::XS_STRIDE;
+          const uint8_t* src = static_cast<const uint8_t*>(u >= vu0 ? a.X2 : a.X) +
+                               static_cast<size_t>(j) * XPLANES * R * Geo::XS_STRIDE;
           bulk_g2s(dst, src, XPLANES * R * Geo::XS_STRIDE, &full[it % STAGES]);
         } else if constexpr (XMODE == X_STREAM_BF16) {
           if constexpr (kXBox) {
@@ -280,16 +290,20 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
   // holds groups lane and lane + 32; fixed summation order.
   float ssv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   bool rs_ready = XMODE != X_NORM;
+  // a CTA's units are all of the extra groups or none (groups aligned to CTAs)
+  const bool xcta = u_begin >= vu0;
+  const float* ssq = xcta ? a.ssq2 : a.ssq;
+  const int nvr = xcta ? a.n_valid2 : a.n_valid_rows;
   auto finish_rs = [&]() {
     if constexpr (XMODE == X_NORM) {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int r = w + 4 * rr;
         float ss = ssv[rr][0] + ssv[rr][1];
-        for (int g = lane + 64; g < a.n_ssq; g += 32) ss += __ldcg(a.ssq + g * 8 + r);
+        for (int g = lane + 64; g < a.n_ssq; g += 32) ss += __ldcg(ssq + g * 8 + r);
 #pragma unroll
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0 && r < R) srs[r] = (r < a.n_valid_rows) ? rsqrtf(ss / a.K + a.eps) : 0.f;
+        if (lane == 0 && r < R) srs[r] = (r < nvr) ? rsqrtf(ss / a.K + a.eps) : 0.f;
       }
       named_bar_sync(1, 128);
       rs_ready = true;
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r = w + 4 * rr, g = lane + 32 * h;
-          if (r < R && g < a.n_ssq) ssv[rr][h] = __ldcg(a.ssq + g * 8 + r);
+          if (r < R && g < a.n_ssq) ssv[rr][h] = __ldcg(ssq + g * 8 + r);
         }
       if (a.rs_early) finish_rs();
     }

@@ -266,7 +266,17 @@ struct EpiHeads {
   int slot;              // mode 1
   const int32_t* positions;  // mode 1: [n_valid] of this tile
   int n_valid;               // mode 1
+  // mode 0 with extra heads (n_heads0 > 0): heads hh >= n_heads0 are this
+  // layer's key heads then value heads again, over the committed rows
+  // (vpositions[vn_valid] of slot vslot), written like mode 1 (cluster
+  // finishing only)
+  int n_heads0;
+  const int32_t* vpositions;
+  int vn_valid;
+  int vslot;
   int32_t* status;
+
+  __device__ bool extra(int hh) const { return mode == 0 && n_heads0 > 0 && hh >= n_heads0; }
 
   __device__ void init(Local&) const {}
   __device__ void prologue(const GemvArgs&, int, const float*) const {}
@@ -326,11 +336,11 @@ struct EpiHeads {
 
   // Row metadata of activation row n: position, whether its K/V cells are
   // written, whether it is used at all (queries always are).
-  __device__ void row_info(int n, int kind, int& pos, bool& write_state, bool& use) const {
+  __device__ void row_info(int n, int kind, bool xh, int& pos, bool& write_state, bool& use) const {
     pos = 0;
     write_state = false;
     use = true;
-    if (mode == 0) {
+    if (mode == 0 && !xh) {
       const int sl = n >> 3, i = n & 7;
       if (sl < n_seq) {
         int B = block_len[sl];
@@ -339,10 +349,10 @@ struct EpiHeads {
         write_state = (i < B) && pos >= 0 && (ring || pos < cap);
       }
     } else {
-      if (n >= n_valid) {
+      if (n >= (xh ? vn_valid : n_valid)) {
         use = false;
       } else {
-        pos = positions[n];
+        pos = (xh ? vpositions : positions)[n];
         // a negative position is a row to skip (no cell, no error)
         write_state = pos >= 0 && (ring || pos < cap);
       }
@@ -358,11 +368,13 @@ struct EpiHeads {
   __device__ void prepare_cluster(const GemvArgs&, Local& L, int g, int w, int lane) const {
     const int hh = g / gph, gl = g - hh * gph;
     const int kind = head_kind(hh);
+    const bool xh = extra(hh);
     const int half = d / 2;
     const int t = w * 32 + lane, n = t >> 4;
     bool ws, use;
-    row_info(n, kind, L.pos, ws, use);
-    if (mode == 1 && L.pos >= 0 && !ws && n < n_valid && (t & 15) == 0 && hh == 0)
+    row_info(n, kind, xh, L.pos, ws, use);
+    if ((mode == 1 || xh) && L.pos >= 0 && !ws && n < (xh ? vn_valid : n_valid) && (t & 15) == 0 &&
+        hh == (xh ? n_heads0 : 0))
       set_status(status, DFLASH_DEV_CAPACITY);
     L.use = use;
 #pragma unroll
@@ -387,6 +399,7 @@ struct EpiHeads {
 
   template <int WT, int NT>
   __device__ void group(const GemvArgs&, Local&, int g, int w, int lane, float (&acc)[NT][4]) const {
+    if (extra(g / gph)) return;  // extra heads finish in clusters only
     const int m0 = g * 64 + frag_row<WT>(w, lane >> 2), m1 = g * 64 + frag_row<WT>(w, (lane >> 2) + 8);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -400,6 +413,7 @@ struct EpiHeads {
 
   __device__ void after_group(const GemvArgs& a, int g, int tid, int* sflag) const {
     const int head = g / gph;
+    if (extra(head)) return;
     if (gph > 1) {
       if (tid == 0) {
         const int old = atomic_add_acq_rel(&head_cnt[head], 1);
@@ -414,11 +428,13 @@ struct EpiHeads {
 
   // 0: query head, 1: key head, 2: value head
   __device__ int head_kind(int hh) const {
+    if (extra(hh)) return hh - n_heads0 < n_kv ? 1 : 2;
     if (mode == 0) return hh < n_q ? 0 : (hh < n_q + n_kv ? 1 : 2);
     return (hh % (2 * n_kv)) < n_kv ? 1 : 2;
   }
 
   __device__ void process_head(int hh, int tid) const {
+    if (extra(hh)) return;  // extra heads finish in clusters only
     const float* base = raw + static_cast<size_t>(hh) * d;
     const int ld = ldr;
     process_head_src(hh, tid, [base, ld](int n, int i) { return __ldcg(base + static_cast<size_t>(n) * ld + i); },
@@ -491,7 +507,12 @@ struct EpiHeads {
     const int n = tid >> 4, c = (tid & 15) * 4, i0 = gl * 64 + c;
     const int half = d / 2;
     int kvh, l;
-    if (mode == 0) {
+    const bool xh = extra(hh);
+    if (xh) {
+      l = layer;
+      const int rem = hh - n_heads0;
+      kvh = rem < n_kv ? rem : rem - n_kv;
+    } else if (mode == 0) {
       l = layer;
       kvh = kind == 0 ? 0 : (kind == 1 ? hh - n_q : hh - n_q - n_kv);
     } else {
@@ -525,7 +546,8 @@ struct EpiHeads {
       const int gq = n_q / n_kv;
       dst = q_ready + ((static_cast<size_t>((n >> 3) * n_kv + hh / gq) * gq + hh % gq) * 8 + (n & 7)) * d + i0;
     } else {
-      const size_t cell = ((static_cast<size_t>((l * n_slots + (mode == 0 ? (n >> 3) : slot)) * n_kv + kvh) * cap) +
+      const int sl = xh ? vslot : (mode == 0 ? (n >> 3) : slot);
+      const size_t cell = ((static_cast<size_t>((l * n_slots + sl) * n_kv + kvh) * cap) +
                            (ring ? pos % cap : pos)) * d;
       dst = (kind == 1 ? Kst : Vst) + cell + i0;
     }

@@ -103,6 +103,16 @@ struct State {
   float* h_raw = nullptr;      // [fuse_rows, H]
   float* kv_raw = nullptr;     // [fuse_rows, L * 2 * n_kv * d]
   void* fuse_xnorm = nullptr;  // [fuse_rows, H] activation type
+  // deferred K/V projection of an 8-row fusion (dflash_state_set_defer_kv):
+  // the committed rows' x * hidden_norm (chunked, like xn) and sums of
+  // squares, kept until the next draft pass projects them in its QKV GEMVs
+  int defer_kv = 0;
+  __nv_bfloat16* fuse_xn = nullptr;
+  float* fuse_ssq = nullptr;
+  int pend_n = 0;                     // rows waiting (0: none)
+  int pend_slot = 0;
+  const int32_t* pend_pos = nullptr;  // the caller's positions array of that fusion
+  int32_t* pend_status = nullptr;
   int32_t* status = nullptr;   // [1] the state's own device status word
   int max_grid = 0;
   void* prof_events[256] = {};     // optional per-kernel event marks

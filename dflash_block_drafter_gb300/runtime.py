@@ -14,6 +14,7 @@ from . import (DFLASH_MAX_BLOCK, dflash_accept, dflash_commit_positions, dflash_
                dflash_model_create, dflash_model_dequantize, dflash_model_destroy, dflash_model_device_bytes, dflash_state_create,
                dflash_state_destroy, dflash_state_device_bytes, dflash_state_read_kv, dflash_state_status,
                dflash_state_read_draft_probs, dflash_state_set_spec_min_p, dflash_state_write_kv, load_library,
+               dflash_state_set_defer_kv, dflash_state_flush,
                make_config, make_weights)
 
 
@@ -106,6 +107,8 @@ class DraftState:
         n = positions.numel()
         dflash_fuse_context(self.model.handle, self.handle, slot, taps.data_ptr(), positions.data_ptr(), n,
                             self.status.data_ptr(), _stream(stream))
+        # a deferring state reads the positions again in a later call: keep them alive
+        self._kept_positions = positions if getattr(self, "_defer_kv", False) and n <= 8 else None
 
     def draft(self, n_seq: int, want_hidden: bool = True, stream=None) -> None:
         """Draft with the anchor_tok / anchor_pos / block_len buffers as set."""
@@ -125,6 +128,15 @@ class DraftState:
         """k16, v16: float16 / int16 tensors [n_kv, n, d] on the device."""
         n = k16.shape[1]
         dflash_state_write_kv(self.handle, slot, layer, pos0, n, k16.data_ptr(), v16.data_ptr(), _stream())
+
+    def set_defer_kv(self, on: bool) -> None:
+        """Leave the K/V of 8-position fusions to the next one-slot draft pass."""
+        dflash_state_set_defer_kv(self.handle, on)
+        self._defer_kv = bool(on)
+
+    def flush(self, stream=None) -> None:
+        """Project the K/V of rows a deferring fusion kept, now."""
+        dflash_state_flush(self.handle, _stream(stream))
 
     def set_spec_min_p(self, floor: float) -> None:
         """Confidence floor of the offered drafts (0: all)."""

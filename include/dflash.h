@@ -328,6 +328,27 @@ int dflash_state_set_profile_events(dflash_state* state, void* const* events, in
  * non-NULL; pass chunks = 0 to only query).  Applies to later calls. */
 int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* max_chunks);
 
+/* Deferred K/V projection of committed rows ("#1426 ...", "Speculative decode
+ * integration": the rows the verifier commits are fused into the drafter's
+ * context before its next block).  With on = 1, a dflash_fuse_context call
+ * of at most 8 positions on this state runs only the tap projection (fc,
+ * RMSNorm) and keeps the rows; the next dflash_draft_block with n_seq = 1
+ * then projects their K/V in each layer's own q/k/v GEMV, next to the
+ * block's (the layer's W_k / W_v are read by both row sets at the same
+ * time instead of once more by a separate launch), so that layer's
+ * attention already sees them.  The positions array given to that fusion
+ * must stay valid and unchanged until then.  Any other call that needs the
+ * cells first projects the kept rows with a separate launch on its own
+ * stream: a draft pass with n_seq > 1, dflash_fuse_context,
+ * dflash_state_read_kv, dflash_state_write_kv and dflash_state_flush.
+ * Results are the same either way.  on = 0 is refused (INVALID_ARG) while
+ * rows are kept: call dflash_state_flush first.  Default 0. */
+int dflash_state_set_defer_kv(dflash_state* state, int32_t on);
+
+/* Projects the K/V of rows kept by a deferring dflash_fuse_context now
+ * (nothing to do: returns DFLASH_OK without enqueuing work). */
+int dflash_state_flush(dflash_state* state, dflash_stream_t stream);
+
 /* Confidence gate of the proposals ("--spec-min-p", "#3322 ...", "Long-prompt
  * diagnosis and fix": floor 0.5 by default there, 0.7 in its 256K run).  A
  * draft's confidence is the drafter's softmax probability of the drafted

@@ -18,7 +18,10 @@ def _setup():
     build_lib()
 
 
-def test_two_chained_cycles():
+@pytest.mark.parametrize("defer", [False, True], ids=["kv_separate", "kv_in_next_qkv"])
+def test_two_chained_cycles(defer):
+    """defer: the 8-row fusion leaves its K/V projection to the next draft
+    pass, whose per-layer QKV GEMVs carry the committed rows."""
     from dflash_block_drafter_gb300.runtime import DraftModel, DraftState, accept, commit_positions
     cfg = synth.CONFIGS["tiny"]
     seed, n_ctx, B = 81, 64, 8
@@ -31,6 +34,7 @@ def test_two_chained_cycles():
     O.fuse_context(om, ost, taps, np.arange(n_ctx))
     anchor = int(synth.make_token_ids(cfg, 1, seed=seed)[0])
     st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = anchor, n_ctx, B
+    st.set_defer_kv(defer)
 
     # cycle 1: the verifier agrees with the first two drafts (both clear of ties)
     r1 = O.draft_block(om, ost, anchor, n_ctx, B)
@@ -64,3 +68,63 @@ def test_two_chained_cycles():
         check_cells(k.cpu().numpy(), ost.K[l][:, : n_ctx + n1 + 1 + B], f"K l{l}")
         check_cells(v.cpu().numpy(), ost.V[l][:, : n_ctx + n1 + 1 + B], f"V l{l}")
     assert st.take_status() == 0  # the skipped (-1) fusion rows raise no error
+
+
+def test_deferred_fusion_flushed_by_reads():
+    """Rows kept by a deferring fusion reach their cells before any call that
+    needs them: dflash_state_read_kv, a later fusion, a multi-slot draft pass
+    and dflash_state_flush; switching deferral off is refused while rows are
+    kept."""
+    from dflash_block_drafter_gb300 import DflashError
+    from dflash_block_drafter_gb300.runtime import DraftModel, DraftState
+    cfg = synth.CONFIGS["tiny"]
+    seed, n_ctx = 82, 40
+    ck = synth.make_checkpoint(cfg, seed=seed)
+    model, om = DraftModel(cfg, ck), O.Model(cfg, ck)
+    st = DraftState(model, 2, 128)
+    ost = [O.State(cfg, 128), O.State(cfg, 128)]
+    st.set_defer_kv(True)
+    taps = synth.make_taps(cfg, 24, seed=seed)
+    # 8 positions of slot 1, one of them skipped: kept, then read back
+    # (a kept fusion's positions array must stay alive until its rows are projected)
+    pos_a = np.array([3, 4, 5, -1, 7, 8, 9, 10], np.int32)
+    dpos_a = device_ids(pos_a)
+    st.fuse(1, torch.as_tensor(taps[:8].view(np.int16), device="cuda"), dpos_a)
+    O.fuse_context(om, ost[1], taps[:8], pos_a)
+    with pytest.raises(DflashError):
+        st.set_defer_kv(False)
+    for l in range(cfg.n_layers):
+        k, v = st.read_kv(1, l, 0, 16)
+        check_cells(k.cpu().numpy(), ost[1].K[l][:, :16], f"K l{l} (read)")
+        check_cells(v.cpu().numpy(), ost[1].V[l][:, :16], f"V l{l} (read)")
+    # kept rows of slot 0, then a second fusion (which projects them first)
+    pos_b = np.arange(0, 8, dtype=np.int32)
+    pos_c = np.arange(8, 14, dtype=np.int32)
+    dpos_b, dpos_c = device_ids(pos_b), device_ids(pos_c)
+    st.fuse(0, torch.as_tensor(taps[8:16].view(np.int16), device="cuda"), dpos_b)
+    st.fuse(0, torch.as_tensor(taps[16:22].view(np.int16), device="cuda"), dpos_c)
+    O.fuse_context(om, ost[0], taps[8:16], pos_b)
+    O.fuse_context(om, ost[0], taps[16:22], pos_c)
+    st.flush()
+    st.set_defer_kv(False)
+    # kept rows of slot 1 and a two-slot draft pass, which projects them before its layers
+    st.set_defer_kv(True)
+    pos_d = np.arange(20, 28, dtype=np.int32)
+    dpos_d = device_ids(pos_d)
+    st.fuse(1, torch.as_tensor(taps[:8].view(np.int16), device="cuda"), dpos_d)
+    O.fuse_context(om, ost[1], taps[:8], pos_d)
+    st.anchor_tok[:2] = 1
+    st.anchor_pos[:2] = 64
+    st.block_len[:2] = 4
+    st.draft(2, want_hidden=False)
+    st.set_defer_kv(False)  # nothing kept any more
+    torch.cuda.synchronize()
+    for l in range(cfg.n_layers):
+        k, v = st.read_kv(1, l, 20, 8)
+        check_cells(k.cpu().numpy(), ost[1].K[l][:, 20:28], f"K l{l} (two-slot pass)")
+        check_cells(v.cpu().numpy(), ost[1].V[l][:, 20:28], f"V l{l} (two-slot pass)")
+    for l in range(cfg.n_layers):
+        k, v = st.read_kv(0, l, 0, 14)
+        check_cells(k.cpu().numpy(), ost[0].K[l][:, :14], f"K l{l} (slot 0)")
+        check_cells(v.cpu().numpy(), ost[0].V[l][:, :14], f"V l{l} (slot 0)")
+    assert st.take_status() == 0

@@ -123,11 +123,13 @@ def test_full_gate():
     assert st.take_status() == 0
 
 
-def test_full_two_chained_cycles():
+@pytest.mark.parametrize("defer", [False, True], ids=["kv_separate", "kv_in_next_qkv"])
+def test_full_two_chained_cycles(defer):
     """Cycle 1 drafts at p = 8192; the verifier agrees with its first two
     drafts; acceptance advances the anchor on the device, the committed rows
     p .. p + 2 are fused (the other five rows skipped) and cycle 2 drafts at
-    p + 3 from the device-resident anchor."""
+    p + 3 from the device-resident anchor.  defer: the committed rows' K/V
+    are projected inside cycle 2's QKV GEMVs."""
     from dflash_block_drafter_gb300.runtime import accept, commit_positions
     ctx, B = 8192, 8
     cfg, om, model, st, ost = _setup_context("bf16", ctx, ctx + 64, 0, seed=93)
@@ -148,6 +150,7 @@ def test_full_two_chained_cycles():
     new_taps = synth.make_taps(cfg, 8, seed=93, stream=1)
 
     st.anchor_tok[0], st.anchor_pos[0], st.block_len[0] = anchor, ctx, B
+    st.set_defer_kv(defer)
     acc = torch.zeros(1, dtype=torch.int32, device="cuda")
     pos8 = torch.zeros((1, 8), dtype=torch.int32, device="cuda")
     st.draft(1)
