@@ -210,8 +210,9 @@ size_t dflash_state_device_bytes(const dflash_state* state);
  *              a device-determined number of positions (dflash_commit_positions).
  * For every position and layer l: k = RoPE(rmsnorm_head(W_k,l h), pos) and
  * v = W_v,l h are rounded to FP16 and written to the slot's cells,
- * overwriting what was there ("Position-addressed context/KV cells are
- * overwritten when that position is later committed").
+ * overwriting what was there (a cell is addressed by its position, so a
+ * position committed again replaces its cell: "#1426 ...", "Speculative
+ * decode integration").
  *   dev_status: device int32 status word (DFLASH_DEV_* bits OR-ed in), or
  *               NULL to use the state's own word (dflash_state_status).
  * n may be 0 (nothing is enqueued). */
@@ -231,8 +232,8 @@ int dflash_fuse_context(const dflash_model* model, dflash_state* state, int32_t 
  *               RMSNorm output of every block row, rows >= B unspecified.
  * The pass writes each layer's block K/V into the slot's cells [p, p + B)
  * (FP16) and attends over cells [0, p + B), non-causally; no rollback is
- * needed because later fusion overwrites those cells ("Rejected candidate
- * cells do not need drafter-side rollback").  With an attention window W
+ * needed because later fusion overwrites those cells (the drafter keeps no
+ * undo log for cells of rejected drafts: same section).  With an attention window W
  * (ring state) the cells are those of positions [max(0, p + B - W), p + B),
  * each at pos mod capacity; those positions must have been fused. */
 int dflash_draft_block(const dflash_model* model, dflash_state* state, int32_t n_seq,

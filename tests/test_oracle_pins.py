@@ -36,7 +36,8 @@ def test_geometry_matches_pages():
     assert len(g["tap_boundaries"]) == cfg.n_taps
     assert [b - 1 for b in g["tap_boundaries"]] == g["trained_tap_layers"]
     assert cfg.tap_width == cfg.n_taps * g["tap_width"]
-    # "498M params, no embedding / LM head": the 36 backbone matrices.
+    # the pages' parameter count of the drafter (about 498M, embedding and LM
+    # head excluded): the 36 backbone matrices.
     n_params = sum(a * b for a, b in cfg.matrix_shapes().values())
     assert n_params == 498_073_600
     assert round(n_params / 1e6) == g["params_millions"]
