@@ -215,6 +215,31 @@ def test_device_detected_errors():
     assert st.take_status() & DFLASH_DEV_NONFINITE
 
 
+def test_attention_chunks_sixteen_slots():
+    """16 slots of a 1300-position context (11 super-tiles) in 9 and in 10
+    chunks per slot (144 and 160 CTAs, below and above the SM count), every
+    slot against the oracle."""
+    import dflash_block_drafter_gb300 as D
+    cfg = synth.CONFIGS["tiny"]
+    ck, model, om = _model(cfg, seed=31)
+    cap, n_ctx, n = 1408, 1300, 16
+    st = _state(model, n, cap)
+    osts = [_ostate(om, cfg, cap) for _ in range(n)]
+    taps = synth.make_taps(cfg, n_ctx, seed=31)
+    for s in range(n):
+        _fuse_both(st, osts[s], s, cfg, taps, np.arange(n_ctx))
+    toks = synth.make_token_ids(cfg, n, seed=31)
+    Bs = [2 + s % 7 for s in range(n)]
+    assert D.dflash_state_set_attn_chunks(st.handle, 0) >= 10
+    for chunks in (9, 10):
+        D.dflash_state_set_attn_chunks(st.handle, chunks)
+        res = _draft_both(st, osts, toks, [n_ctx] * n, Bs)
+        for s in range(n):
+            check_hidden(st.final_hidden[s, :Bs[s]].cpu().numpy(), res[s].final_hidden, f"chunks {chunks} slot {s}")
+            check_drafts(st.drafts[s].cpu().numpy(), res[s], Bs[s], f"chunks {chunks} slot {s}")
+        assert st.take_status() == 0
+
+
 def test_accept_matches_oracle():
     from dflash_block_drafter_gb300.runtime import accept
     rng = np.random.default_rng(29)
