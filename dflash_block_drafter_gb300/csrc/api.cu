@@ -190,7 +190,7 @@ void free_state(State* s) {
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
   f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
-  f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
+  f(s->head_keys); f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
 }
 
 int pow2ceil(int v) {
@@ -574,6 +574,14 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<uint32_t>(M)));
   STRY(make_map_2d(&s->k_map, s->K, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   STRY(make_map_2d(&s->v_map, s->V, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+  if (R == 128) {
+    // the final normed rows of a 128-row pass, one chunk of H inputs per row (row stride H + 32)
+    STRY(make_map_2d(&s->xhead_map, s->xnorm, 2 * 128, static_cast<uint64_t>(H) + 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     128));
+    STRY(dev_alloc(&s->head_keys, 128 * 8, &total));
+    if (cudaMemset(s->head_keys, 0, 128 * 8) != cudaSuccess)
+      return fail(cuda_fail(cudaGetLastError(), "cudaMemset head_keys"));
+  }
   {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail(cuda_fail(e, "state create"));
@@ -907,10 +915,34 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       prof_mark(s, stream);
       TRY(check_gemv(gemv_argmax(nt, a, p, lc), "lm head"));
       if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
+    } else if (nt == 16 && H % 64 == 0) {
+      // 128 rows: the head is a GEMM for the tcgen05 tensor cores
+      NormArgs na{s->x, m->final_norm, s->xnorm, 0, H, R, c.norm_eps, final_hidden, n_seq * 8, H};
+      prof_mark(s, stream);
+      TRY(check_gemv(launch_rmsnorm_rows(na, R, stream), "final norm"));
+      HeadTcArgs ha;
+      ha.wmap = m->head_map;
+      ha.xmap = s->xhead_map;
+      ha.V = c.vocab;
+      ha.H = H;
+      ha.n_seq = n_seq;
+      ha.block_len = block_len;
+      ha.drafts = drafts;
+      ha.probs = s->draft_probs;
+      ha.min_p = s->spec_min_p;
+      ha.keys = s->head_keys;
+      ha.ms = s->argmax_ms;
+      ha.grid_cnt = p.grid_cnt;
+      ha.status = status;
+      const int nv = (c.vocab + 255) / 256;
+      if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
+      prof_mark(s, stream);
+      TRY(check_gemv(launch_head_tc(ha, nv < m->sm_count ? nv : m->sm_count, stream), "lm head"));
+      if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
     } else {
-      // Up to 8 slots (64 rows) per head launch: a 128-row tile would spill
-      // the argmax epilogue's registers, so 16 slots take two launches, each
-      // over its own half of the rows (the head is streamed once per launch).
+      // Up to 8 slots (64 rows) per head launch: a 128-row mma.sync tile would
+      // spill the argmax epilogue's registers, so wider passes take launches of
+      // 8 slots, each over its own rows (the head is streamed once per launch).
       const int halves = nt > 8 ? nt / 8 : 1;
       const int hnt = nt > 8 ? 8 : nt;
       const int hr = hnt * 8;
@@ -1053,7 +1085,7 @@ int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   const int nt = pow2ceil(n_seq);
   const bool streamed = !fused_norm(nt);  // separate RMSNorm kernels
   const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
-  const int head_launches = nt > 8 ? (n_seq + 7) / 8 : 1;  // 8 slots per head launch
+  const int head_launches = (nt > 8 && !(nt == 16 && s->model->cfg.hidden % 64 == 0)) ? (n_seq + 7) / 8 : 1;
   return 1 + L * per_layer + head_launches * (streamed ? 2 : 1);
 }
 

@@ -127,6 +127,9 @@ struct State {
   CUtensorMap part_map;  // attn_part as [slots*n_kv*C_max*M, d], 64 x M boxes, 128-byte swizzle
   CUtensorMap k_map;  // K arena as [L*slots*n_kv*cap, d], 64x64 boxes, 128-byte swizzle
   CUtensorMap v_map;
+  // 128-row passes: xnorm as [2 * 128, H + 32] BF16 rows for the tcgen05 LM head, and its keys
+  CUtensorMap xhead_map;
+  unsigned long long* head_keys = nullptr;  // [128], zero between passes
   size_t device_bytes = 0;
 };
 

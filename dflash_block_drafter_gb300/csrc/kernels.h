@@ -44,6 +44,23 @@ struct NormArgs {
   int ku;           // chunked layout of the consuming GEMV: inputs per unit
 };
 
+// LM head + argmax of a 128-row pass on the tcgen05 tensor cores (head_tc.cu)
+struct HeadTcArgs {
+  CUtensorMap wmap;  // the head [V, H] BF16: 64 x 64 boxes, 128-byte swizzle
+  CUtensorMap xmap;  // the final normed rows as [2 * 128, H + 32] BF16 (hi rows, then lo rows):
+                     // 64 x 128 boxes, 128-byte swizzle
+  int V, H, n_seq;
+  const int32_t* block_len;
+  int32_t* drafts;   // [n_seq, 7]
+  float* probs;      // [n_seq, 7] or null
+  float min_p;       // confidence floor (0: none, confidences -1)
+  unsigned long long* keys;  // [128] packed (logit, id) keys, zero between launches
+  float2* ms;        // [grid, 128] per-CTA (max logit, sum of exp) when min_p > 0
+  int* grid_cnt;     // zero between launches
+  int32_t* status;
+};
+cudaError_t launch_head_tc(const HeadTcArgs& a, int grid, cudaStream_t stream);
+
 cudaError_t launch_repack(int wtype, const void* src, int rows, int K, uint8_t* dst, int row_off, int interleave,
                           cudaStream_t st);
 cudaError_t launch_dequant(int wtype, const uint8_t* packed, int N, int K, float* out, int row_off, int rows_out,

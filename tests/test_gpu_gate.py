@@ -50,7 +50,14 @@ def _setup_slots(wtype, ctxs, Bs, seed):
     return st, om, osts, toks
 
 
-@pytest.mark.parametrize("wtype,ctxs,Bs", [("bf16", [64], [8]), ("q4_0", [40, 61], [8, 6])])
+CTX12 = [64, 40, 61, 20, 33, 50, 12, 64, 9, 27, 44, 58]
+B12 = [8, 6, 2, 7, 3, 8, 4, 5, 8, 2, 6, 7]
+
+
+# twelve slots: a 128-row pass, whose LM head runs on the tcgen05 tensor cores
+@pytest.mark.parametrize("wtype,ctxs,Bs", [("bf16", [64], [8]), ("q4_0", [40, 61], [8, 6]),
+                                           ("bf16", CTX12, B12), ("q4_0", CTX12[::-1], B12[::-1])],
+                         ids=["bf16-1", "q4_0-2", "bf16-12", "q4_0-12"])
 def test_gate_parity(wtype, ctxs, Bs):
     st, om, osts, toks = _setup_slots(wtype, ctxs, Bs, seed=61)
     res = [O.draft_block(om, osts[s], int(toks[s]), ctxs[s], Bs[s]) for s in range(len(ctxs))]
