@@ -8,11 +8,14 @@
 // so QK^T and PV are real matrix products and run on the tcgen05 tensor
 // cores.  The keys are the slot's position-addressed cells [0, p + B): the
 // fused context plus the block's own rows, which the QKV epilogue wrote at
-// [p, p + B).  The context is split into C chunks of 128-key super-tiles
-// (split-K / flash-decode).  With C > 1 every chunk writes (O unnormalised,
-// running max, sum) and attn_combine_kernel merges them with the
-// log-sum-exp rule; with C == 1 the CTA normalises and writes the output
-// directly.
+// [p, p + B).  The keys are split into chunks of 128-key super-tiles
+// (split-K / flash-decode): a pass of n_seq sequences has n_seq * C chunks
+// (one CTA each per kv head), shared out by chunk_plan so that sequences
+// with longer contexts get more of them and every chunk has about the same
+// number of super-tiles.  With C > 1 every chunk writes (O unnormalised,
+// running max, sum) and attn_combine_kernel merges each sequence's chunks
+// with the log-sum-exp rule; with C == 1 (one chunk per sequence) the CTA
+// normalises and writes the output directly.
 #include "kernels.h"
 #include "layout.cuh"
 
@@ -154,6 +157,77 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t addr, float scale) {
   tmem_wait_st();
 }
 
+// Key super-tiles of sequence s in a pass: positions [lo, T) taken from the
+// tile-aligned base kbase (lo = 0, or T - window with a ring of cells).
+struct SeqKeys {
+  int p, B, T, lo, kbase, tiles;
+};
+__device__ __forceinline__ SeqKeys seq_keys(const int32_t* anchor_pos, const int32_t* block_len, int s, int window,
+                                            int cap) {
+  SeqKeys k;
+  k.p = anchor_pos[s];
+  int B = block_len[s];
+  k.B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+  int T = k.p + k.B;
+  int lo = 0;
+  if (window > 0) {
+    T = T < 0 ? 0 : T;
+    lo = T - window < 0 ? 0 : T - window;
+  } else {
+    T = T < 0 ? 0 : (T > cap ? cap : T);
+  }
+  k.T = T;
+  k.lo = lo;
+  k.kbase = lo - lo % kTcKS;
+  k.tiles = (T - k.kbase + kTcKS - 1) / kTcKS;
+  return k;
+}
+
+// Chunk plan of a pass, computed by a whole warp (lane s holds sequence s,
+// n_seq <= 32): the pass's Q = n_seq * C chunks are shared out so that the
+// longest chunk is as short as possible -- sequence s takes
+// c_s = max(1, ceil(tiles_s / t)) chunks of t super-tiles (its last one
+// shorter), t the smallest count with sum_s c_s <= Q (found by bisection; a
+// single sequence gets t = ceil(tiles / C) directly).  Chunks are numbered
+// sequence after sequence: sequence s owns [start_s, start_s + c_s).
+// Returns t; this lane's c_s and start_s in *cs / *start (lanes >= n_seq: 0).
+__device__ int chunk_plan(const int32_t* anchor_pos, const int32_t* block_len, int n_seq, int C, int window,
+                          int cap, int lane, int* cs, int* start) {
+  const int tiles = lane < n_seq ? seq_keys(anchor_pos, block_len, lane, window, cap).tiles : 0;
+  int t;
+  if (n_seq == 1) {
+    t = (tiles + C - 1) / C;
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t < 1) t = 1;
+  } else {
+    int hi = tiles;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    hi = hi < 1 ? 1 : hi;
+    int lo = 1;
+    const int Q = n_seq * C;
+    while (lo < hi) {  // uniform across the warp
+      const int mid = (lo + hi) >> 1;
+      int cnt = lane < n_seq ? max(1, (tiles + mid - 1) / mid) : 0;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (cnt <= Q) hi = mid;
+      else lo = mid + 1;
+    }
+    t = lo;
+  }
+  const int c = lane < n_seq ? max(1, (tiles + t - 1) / t) : 0;
+  int incl = c;  // inclusive prefix sum over the lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  *cs = c;
+  *start = incl - c;
+  return t;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   using Geo = TcGeom<D>;
@@ -181,29 +255,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int g = blockIdx.y;
   if (tid == 0) DFLASH_ATTN_STAMP(0);
 
+  // this CTA's chunk q of the pass (grid x, z: C x n_seq of them) -> its
+  // sequence s and chunk c of that sequence (chunk_plan; none: idle)
+  const int q = blockIdx.z * a.C + blockIdx.x;
+  int s = 0, c = 0, spc = 1;
+  bool idle = true;
+  {
+    int cs_l, start_l;
+    spc = chunk_plan(a.anchor_pos, a.block_len, a.n_seq, a.C, a.window, a.cap, lane, &cs_l, &start_l);
+    const unsigned own = __ballot_sync(0xffffffffu, lane < a.n_seq && q >= start_l && q < start_l + cs_l);
+    if (own) {
+      s = __ffs(own) - 1;
+      c = q - __shfl_sync(0xffffffffu, start_l, s);
+      idle = false;
+    }
+  }
   // key positions [lo, T), in super-tiles of kTcKS positions from `kbase`
   // (lo rounded down to a super-tile); with a window the cells are a ring and
   // a super-tile (cap % kTcKS == 0) is one contiguous run of cells
-  const int p = a.anchor_pos[s];
-  int B = a.block_len[s];
-  B = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
-  int T = p + B;
-  int lo = 0;
-  if (a.window > 0) {
-    T = T < 0 ? 0 : T;
-    lo = T - a.window < 0 ? 0 : T - a.window;
-  } else {
-    T = T < 0 ? 0 : (T > a.cap ? a.cap : T);
-  }
-  const int kbase = lo - lo % kTcKS;
-  const int nst_all = (T - kbase + kTcKS - 1) / kTcKS;
-  const int spc = (nst_all + a.C - 1) / a.C;
+  const SeqKeys sk_ = seq_keys(a.anchor_pos, a.block_len, s, a.window, a.cap);
+  const int p = sk_.p, T = sk_.T, lo = sk_.lo, kbase = sk_.kbase;
+  const int nst_all = sk_.tiles;
   const int st0 = c * spc;
   const int st1 = min(nst_all, st0 + spc);
-  const int nst = st1 > st0 ? st1 - st0 : 0;
+  const int nst = (!idle && st1 > st0) ? st1 - st0 : 0;
   const int row0 = ((a.layer * a.n_slots + s) * a.n_kv + g) * a.cap;
 
   if (tid == 0) {
@@ -520,7 +598,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // last softmax) as D/64 boxes of M rows x 128 bytes with the 128-byte
       // swizzle, then written by tensor-map stores.  An empty chunk writes
       // only (m, l) = (-inf, 0); the merge gives it no weight.
-      const size_t pbase = ((static_cast<size_t>(s) * a.n_kv + g) * a.C + c) * M;
+      // chunk partials of kv head g: [n_seq * C chunks of the pass][M] (chunk_plan's numbering)
+      const size_t pbase = (static_cast<size_t>(g) * a.n_seq * a.C + q) * M;
       if (nst > 0) {
         if (live) {
           float v[OC];
@@ -559,8 +638,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
 }
 
-// Log-sum-exp merge of the C chunk partials of one (slot, q head): all 8 block
-// rows, a 32-column slice of the head (blockIdx.y).  Chunk c of row m carries
+// Log-sum-exp merge of the chunk partials of one (slot, q head) -- the slot's
+// chunks of the pass's chunk plan: all 8 block rows, a 32-column slice of
+// the head (blockIdx.y).  Chunk c of row m carries
 // O_c / l_c (FP16) and (m_c, l_c); the row's output is
 //   sum_c w_c O_c / l_c,   w_c = l_c 2^(m_c - mx) / sum_c' l_c' 2^(m_c' - mx).
 // Lane = (row i = lane / 4, 8 columns from (lane % 4) * 8); warp w takes
@@ -575,6 +655,10 @@ struct CombineArgs {
   int out_f16;
   int out_rows, out_ku;
   int d, n_q, n_kv, gq, C;
+  // the pass's chunk plan (chunk_plan): sequence s owns chunks [start_s, start_s + c_s)
+  const int32_t* anchor_pos;
+  const int32_t* block_len;
+  int n_seq, window, cap;
   int32_t* status;
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
@@ -590,10 +674,19 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   const int M = a.gq * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(0);
+  // the plan depends only on the pass's inputs (set before its first kernel):
+  // formed while the attention kernel finishes
+  int n_ch, start;
+  {
+    int cs_l, start_l;
+    chunk_plan(a.anchor_pos, a.block_len, a.n_seq, a.C, a.window, a.cap, lane, &cs_l, &start_l);
+    n_ch = __shfl_sync(0xffffffffu, cs_l, s);
+    start = __shfl_sync(0xffffffffu, start_l, s);
+  }
   pdl_wait();
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(1);
   pdl_launch_dependents();
-  const size_t base = (static_cast<size_t>(s) * a.n_kv + g) * a.C * M;
+  const size_t base = (static_cast<size_t>(g) * a.n_seq * a.C + start) * M;
   const int i = lane >> 2, mrow = hl * 8 + i, col = cb * 32 + (lane & 3) * 8;
   const __half* pr = a.part + (base + mrow) * a.d + col;
   const float2* pml = a.ml + base + mrow;
@@ -602,13 +695,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   constexpr int U = 9;  // 8 warps x 9 loads cover the default 65 chunks in one round
-  for (int c0 = warp; c0 < a.C; c0 += 8 * U) {
+  for (int c0 = warp; c0 < n_ch; c0 += 8 * U) {
     uint4 v[U];
     float2 ml[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + 8 * u;
-      if (c < a.C) {
+      if (c < n_ch) {
         ml[u] = __ldcg(pml + static_cast<size_t>(c) * M);
         v[u] = __ldcg(reinterpret_cast<const uint4*>(pr + c * cstride));
       } else {
@@ -774,6 +867,11 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cb.n_kv = c.n_kv_heads;
   cb.gq = a.gq;
   cb.C = a.C;
+  cb.anchor_pos = anchor_pos;
+  cb.block_len = block_len;
+  cb.n_seq = n_seq;
+  cb.window = a.window;
+  cb.cap = a.cap;
   cb.status = status;
   cb.trace = trace_slot(st);
   cudaLaunchConfig_t cfg = {};
