@@ -189,7 +189,7 @@ void free_state(State* s) {
   if (!s) return;
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
-  f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
+  f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->attn_plan); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
   f(s->head_keys); f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
 }
 
@@ -544,6 +544,7 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->ssq, size_t(H / 64) * 8 * 4, &total));
   STRY(dev_alloc(&s->attn_part, size_t(n_slots) * nkv * s->attn_chunks_max * M * d * 2, &total));
   STRY(dev_alloc(&s->attn_ml, size_t(n_slots) * nkv * s->attn_chunks_max * M * 8, &total));
+  STRY(dev_alloc(&s->attn_plan, 32 * 4, &total));
   s->max_grid = 2 * m->sm_count;
   const int rmax = 128;
   STRY(dev_alloc(&s->partials, size_t(s->max_grid) * 2 * 64 * rmax * 4, &total));
@@ -1084,7 +1085,7 @@ int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   const int L = s->model->cfg.n_layers;
   const int nt = pow2ceil(n_seq);
   const bool streamed = !fused_norm(nt);  // separate RMSNorm kernels
-  const int per_layer = 5 + (s->attn_chunks > 1 ? 1 : 0) + (streamed ? 2 : 0);
+  const int per_layer = 5 + (attn_pass_chunks(*s->model, *s, n_seq) > n_seq ? 1 : 0) + (streamed ? 2 : 0);
   const int head_launches = (nt > 8 && !(nt == 16 && s->model->cfg.hidden % 64 == 0)) ? (n_seq + 7) / 8 : 1;
   return 1 + L * per_layer + head_launches * (streamed ? 2 : 1);
 }
@@ -1105,6 +1106,7 @@ int dflash_state_set_attn_chunks(dflash_state* s, int32_t chunks, int32_t* max_c
   if (chunks == 0) return DFLASH_OK;
   if (chunks < 1 || chunks > s->attn_chunks_max) return DFLASH_ERR_INVALID_ARG;
   s->attn_chunks = chunks;
+  s->attn_chunks_set = 1;
   return DFLASH_OK;
 }
 

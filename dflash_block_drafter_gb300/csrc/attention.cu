@@ -32,13 +32,15 @@ struct AttnArgs {
   void* out;              // attention output in the o-projection's chunked X layout (C == 1)
   int out_f16;            // 1: one FP16 plane; 0: BF16 hi and lo planes
   int out_rows, out_ku;   // chunked layout: rows R of the pass and inputs per unit
-  int layer, n_slots, n_kv, n_q, gq, cap, C, n_seq;
+  int layer, n_slots, n_kv, n_q, gq, cap, n_seq;
+  int Q;                  // chunks of the pass per kv head (grid x; chunk_plan shares them out)
   int window;             // 0: keys [0, p + B), cell = position; W > 0: keys
                           // [max(0, p + B - W), p + B) in a ring, cell = position mod cap
   int32_t* status;
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
   const __half* kbase_ptr;    // the K / V arenas (rows of d halves) the maps address
   const __half* vbase_ptr;
+  int* plan;                  // [n_seq] out (passes of several sequences): start_s | c_s << 16
 };
 
 #ifdef DFLASH_TRACE
@@ -184,19 +186,19 @@ __device__ __forceinline__ SeqKeys seq_keys(const int32_t* anchor_pos, const int
 }
 
 // Chunk plan of a pass, computed by a whole warp (lane s holds sequence s,
-// n_seq <= 32): the pass's Q = n_seq * C chunks are shared out so that the
+// n_seq <= 32): the pass's Q chunks (per kv head) are shared out so that the
 // longest chunk is as short as possible -- sequence s takes
 // c_s = max(1, ceil(tiles_s / t)) chunks of t super-tiles (its last one
 // shorter), t the smallest count with sum_s c_s <= Q (found by bisection; a
-// single sequence gets t = ceil(tiles / C) directly).  Chunks are numbered
+// single sequence gets t = ceil(tiles / Q) directly).  Chunks are numbered
 // sequence after sequence: sequence s owns [start_s, start_s + c_s).
 // Returns t; this lane's c_s and start_s in *cs / *start (lanes >= n_seq: 0).
-__device__ int chunk_plan(const int32_t* anchor_pos, const int32_t* block_len, int n_seq, int C, int window,
+__device__ int chunk_plan(const int32_t* anchor_pos, const int32_t* block_len, int n_seq, int Q, int window,
                           int cap, int lane, int* cs, int* start) {
   const int tiles = lane < n_seq ? seq_keys(anchor_pos, block_len, lane, window, cap).tiles : 0;
   int t;
   if (n_seq == 1) {
-    t = (tiles + C - 1) / C;
+    t = (tiles + Q - 1) / Q;
     t = __shfl_sync(0xffffffffu, t, 0);
     if (t < 1) t = 1;
   } else {
@@ -205,7 +207,6 @@ __device__ int chunk_plan(const int32_t* anchor_pos, const int32_t* block_len, i
     for (int o = 16; o; o >>= 1) hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     hi = hi < 1 ? 1 : hi;
     int lo = 1;
-    const int Q = n_seq * C;
     while (lo < hi) {  // uniform across the warp
       const int mid = (lo + hi) >> 1;
       int cnt = lane < n_seq ? max(1, (tiles + mid - 1) / mid) : 0;
@@ -253,25 +254,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint64_t* pfree = bars + 10;
   uint64_t* mdone = bars + 11;  // every MMA of the CTA has completed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
+  int* s_plan = reinterpret_cast<int*>(s_tmem + 1);  // [4]: sequence, its chunk, super-tiles per chunk, idle
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
   if (tid == 0) DFLASH_ATTN_STAMP(0);
 
-  // this CTA's chunk q of the pass (grid x, z: C x n_seq of them) -> its
+  // this CTA's chunk q of the pass (grid x: Q of them) -> its
   // sequence s and chunk c of that sequence (chunk_plan; none: idle)
-  const int q = blockIdx.z * a.C + blockIdx.x;
-  int s = 0, c = 0, spc = 1;
-  bool idle = true;
-  {
-    int cs_l, start_l;
-    spc = chunk_plan(a.anchor_pos, a.block_len, a.n_seq, a.C, a.window, a.cap, lane, &cs_l, &start_l);
-    const unsigned own = __ballot_sync(0xffffffffu, lane < a.n_seq && q >= start_l && q < start_l + cs_l);
-    if (own) {
-      s = __ffs(own) - 1;
-      c = q - __shfl_sync(0xffffffffu, start_l, s);
-      idle = false;
+  // (formed by warp 0 and handed to the others through shared memory; the
+  // first CTA also publishes the plan for the merge kernel)
+  const int q = blockIdx.x;
+  int s = 0, c = blockIdx.x, spc;
+  bool idle = false;
+  if (a.n_seq == 1) {
+    // one sequence: its C chunks, as the plan would give them
+    spc = max(1, (seq_keys(a.anchor_pos, a.block_len, 0, a.window, a.cap).tiles + a.Q - 1) / a.Q);
+  } else {
+    // several sequences (comment above)
+    if (warp == 0) {
+      int cs_l, start_l;
+      const int t = chunk_plan(a.anchor_pos, a.block_len, a.n_seq, a.Q, a.window, a.cap, lane, &cs_l, &start_l);
+      const unsigned own = __ballot_sync(0xffffffffu, lane < a.n_seq && q >= start_l && q < start_l + cs_l);
+      const int so = own ? __ffs(own) - 1 : 0;
+      const int co = q - __shfl_sync(0xffffffffu, start_l, so);
+      if (lane == 0) {
+        s_plan[0] = so;
+        s_plan[1] = own ? co : 0;
+        s_plan[2] = t;
+        s_plan[3] = own ? 0 : 1;
+      }
+      if (a.plan && q == 0 && g == 0 && lane < a.n_seq) a.plan[lane] = start_l | (cs_l << 16);
     }
+    __syncthreads();
+    s = s_plan[0];
+    c = s_plan[1];
+    spc = s_plan[2];
+    idle = s_plan[3] != 0;
   }
   // key positions [lo, T), in super-tiles of kTcKS positions from `kbase`
   // (lo rounded down to a super-tile); with a window the cells are a ring and
@@ -557,7 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     named_bar_sync(1, kTcSoftThreads);
     const float l_run = (red_l[m] + red_l[128 + m]) + (red_l[256 + m] + red_l[384 + m]);
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    if (a.C == 1) {
+    if (a.Q == a.n_seq) {  // one chunk per sequence
       // normalised rows straight into the o-projection's input layout
       if (live) {
         float v[OC];
@@ -598,8 +617,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // last softmax) as D/64 boxes of M rows x 128 bytes with the 128-byte
       // swizzle, then written by tensor-map stores.  An empty chunk writes
       // only (m, l) = (-inf, 0); the merge gives it no weight.
-      // chunk partials of kv head g: [n_seq * C chunks of the pass][M] (chunk_plan's numbering)
-      const size_t pbase = (static_cast<size_t>(g) * a.n_seq * a.C + q) * M;
+      // chunk partials of kv head g: [Q chunks of the pass][M] (chunk_plan's numbering)
+      const size_t pbase = (static_cast<size_t>(g) * a.Q + q) * M;
       if (nst > 0) {
         if (live) {
           float v[OC];
@@ -654,11 +673,12 @@ struct CombineArgs {
   void* out;
   int out_f16;
   int out_rows, out_ku;
-  int d, n_q, n_kv, gq, C;
+  int d, n_q, n_kv, gq, Q;  // Q: chunks of the pass per kv head
   // the pass's chunk plan (chunk_plan): sequence s owns chunks [start_s, start_s + c_s)
   const int32_t* anchor_pos;
   const int32_t* block_len;
   int n_seq, window, cap;
+  const int* plan;  // [n_seq] start_s | c_s << 16, written by the attention kernel (n_seq > 1)
   int32_t* status;
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
@@ -674,19 +694,24 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   const int M = a.gq * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(0);
-  // the plan depends only on the pass's inputs (set before its first kernel):
-  // formed while the attention kernel finishes
-  int n_ch, start;
-  {
-    int cs_l, start_l;
-    chunk_plan(a.anchor_pos, a.block_len, a.n_seq, a.C, a.window, a.cap, lane, &cs_l, &start_l);
-    n_ch = __shfl_sync(0xffffffffu, cs_l, s);
-    start = __shfl_sync(0xffffffffu, start_l, s);
+  // this sequence's chunks: one sequence's plan is formed here, while the
+  // attention kernel finishes (it depends only on the pass's inputs); a
+  // several-sequence plan is the one the attention kernel published
+  int n_ch = 0, start = 0;
+  if (a.n_seq == 1) {
+    const int tiles = seq_keys(a.anchor_pos, a.block_len, 0, a.window, a.cap).tiles;
+    const int t = max(1, (tiles + a.Q - 1) / a.Q);
+    n_ch = max(1, (tiles + t - 1) / t);
   }
   pdl_wait();
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(1);
   pdl_launch_dependents();
-  const size_t base = (static_cast<size_t>(g) * a.n_seq * a.C + start) * M;
+  if (a.n_seq > 1) {
+    const int pl = __ldcg(a.plan + s);
+    start = pl & 0xffff;
+    n_ch = pl >> 16;
+  }
+  const size_t base = (static_cast<size_t>(g) * a.Q + start) * M;
   const int i = lane >> 2, mrow = hl * 8 + i, col = cb * 32 + (lane & 3) * 8;
   const __half* pr = a.part + (base + mrow) * a.d + col;
   const float2* pml = a.ml + base + mrow;
@@ -823,6 +848,18 @@ int attn_smem_bytes(int D, int M) {
 
 // One layer's attention for slots [0, n_seq): chunked kernel plus, when the
 // context is split, the merge.
+// Chunks of a pass per kv head: C per sequence; a pass of several sequences
+// on the default C takes at least one wave of CTAs (one per SM), shared out
+// by context length (chunk_plan), within the partial buffers' n_slots * C_max.
+int attn_pass_chunks(const Model& m, const State& st, int n_seq) {
+  const int base = n_seq * st.attn_chunks;
+  if (n_seq == 1 || st.attn_chunks_set) return base;
+  int wave = m.sm_count / m.cfg.n_kv_heads;
+  const int cap = st.n_slots * st.attn_chunks_max;
+  if (wave > cap) wave = cap;
+  return wave > base ? wave : base;
+}
+
 cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,
                              const int32_t* block_len, int32_t* status, cudaStream_t stream) {
   const dflash_config& c = m.cfg;
@@ -844,15 +881,16 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.gq = c.n_q_heads / c.n_kv_heads;
   a.cap = st.capacity;
   a.window = c.attn_window;
-  a.C = st.attn_chunks;
+  a.Q = attn_pass_chunks(m, st, n_seq);
   a.n_seq = n_seq;
   a.status = status;
   a.qmap = st.q_map;
   a.trace = trace_slot(st);
   a.kbase_ptr = st.K;
   a.vbase_ptr = st.V;
-  cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.C, a.n_kv, n_seq), stream, true);
-  if (e != cudaSuccess || a.C == 1) return e;
+  a.plan = n_seq > 1 ? st.attn_plan : nullptr;
+  cudaError_t e = launch_attn_impl(c.head_dim, a, dim3(a.Q, a.n_kv, 1), stream, true);
+  if (e != cudaSuccess || a.Q == n_seq) return e;
   if (st.prof_n > 0 && st.prof_k < st.prof_n)
     cudaEventRecordWithFlags(static_cast<cudaEvent_t>(st.prof_events[st.prof_k++]), stream, cudaEventRecordExternal);
   CombineArgs cb;
@@ -866,12 +904,13 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cb.n_q = c.n_q_heads;
   cb.n_kv = c.n_kv_heads;
   cb.gq = a.gq;
-  cb.C = a.C;
+  cb.Q = a.Q;
   cb.anchor_pos = anchor_pos;
   cb.block_len = block_len;
   cb.n_seq = n_seq;
   cb.window = a.window;
   cb.cap = a.cap;
+  cb.plan = st.attn_plan;
   cb.status = status;
   cb.trace = trace_slot(st);
   cudaLaunchConfig_t cfg = {};

@@ -76,6 +76,7 @@ struct State {
   int nt = 0;              // n8 tiles of a pass (power of two >= n_slots)
   int attn_chunks = 0;     // context chunks per (slot, kv head)
   int attn_chunks_max = 0; // chunks the partial buffers are sized for
+  int attn_chunks_set = 0; // the caller chose attn_chunks (dflash_state_set_attn_chunks)
   // per-layer FP16 K/V arenas: [L][slot][n_kv][capacity][d]
   __half* K = nullptr;
   __half* V = nullptr;
@@ -90,6 +91,7 @@ struct State {
   float* ssq = nullptr;         // [H / 64, 8] partial sums of squares of x
   __half* attn_part = nullptr;  // [slots, n_kv, C, Gq*8, d] chunk partials O / l
   float2* attn_ml = nullptr;   // [slots, n_kv, C, Gq*8] (max in log2 units, sum)
+  int* attn_plan = nullptr;    // [32] the attention chunk plan of the last multi-sequence pass
   float* partials = nullptr;   // GEMV split fix-up slots [max_grid, 2, 64, R_max]
   int* counters = nullptr;     // [CNT_REGIONS][counter_stride]
   int counter_stride = 0;

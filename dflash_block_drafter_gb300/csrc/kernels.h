@@ -73,6 +73,7 @@ cudaError_t launch_commit_positions(const int32_t* anchor_pos, const int32_t* ac
                                     cudaStream_t st);
 cudaError_t launch_kv_copy(bool write, __half* cells, int cap, bool ring, int d, int n_kv, int pos0, int n, float* out,
                            const uint16_t* in, cudaStream_t st);
+int attn_pass_chunks(const Model& m, const State& st, int n_seq);
 cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, int pass_nt, const int32_t* anchor_pos,
                              const int32_t* block_len, int32_t* status, cudaStream_t stream);
 // Dynamic shared memory of the attention kernel for head dim D and M query rows.

@@ -322,11 +322,16 @@ int dflash_state_set_head_events(dflash_state* state, void* ev_begin, void* ev_e
  * off.  At most 256 events. */
 int dflash_state_set_profile_events(dflash_state* state, void* const* events, int32_t n_events);
 
-/* Tuning: number of context chunks the attention of a draft pass splits each
- * (sequence, kv head) into (split-context / flash-decode).  The default is
- * chosen at state creation from the capacity and the SM count; valid values
- * are 1 .. the maximum the state was sized for (returned in *max_chunks when
- * non-NULL; pass chunks = 0 to only query).  Applies to later calls. */
+/* Tuning: number of context chunks C the attention of a draft pass splits
+ * each (sequence, kv head) into (split-context / flash-decode).  A pass of n
+ * sequences has n * C chunks per kv head, shared out among its sequences in
+ * proportion to their key counts (a longer context gets more chunks, every
+ * chunk about as long).  The default C is chosen at state creation from the
+ * capacity and the SM count, and a pass of several sequences on the default
+ * takes at least one chunk per SM; once C is set here, every pass takes
+ * exactly n * C.  Valid values are 1 .. the maximum the state was sized for
+ * (returned in *max_chunks when non-NULL; pass chunks = 0 to only query).
+ * Applies to later calls. */
 int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* max_chunks);
 
 /* Deferred K/V projection of committed rows ("#1426 ...", "Speculative decode
