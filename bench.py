@@ -46,12 +46,12 @@ UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
 # DRAM bytes (read + write) of one LM-head launch at this workload, from one
-# ncu capture of that kernel (dram__bytes_read.sum 778136320 +
-# dram__bytes_write.sum 3187968).  Reset to None whenever the head kernel
+# ncu capture of that kernel (dram__bytes_read.sum 778093312 +
+# dram__bytes_write.sum 3127040).  Reset to None whenever the head kernel
 # changes.
-HEAD_TRAFFIC_BYTES = 781324288
+HEAD_TRAFFIC_BYTES = 781220352
 HEAD_TRAFFIC_SOURCE = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on one LM-head launch of "
-                       "`bench.py --steps 3 --warmup 3`, library as of commit 8df2510")
+                       "`bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-extras`, library as of commit 8b2e4ca")
 
 
 def load_peaks():
