@@ -342,8 +342,12 @@ int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* m
  * then projects their K/V in each layer's own q/k/v GEMV, next to the
  * block's (the layer's W_k / W_v are read by both row sets at the same
  * time instead of once more by a separate launch), so that layer's
- * attention already sees them.  The positions array given to that fusion
- * must stay valid and unchanged until then.  Any other call that needs the
+ * attention already sees them.  The positions array (and the dev_status
+ * word) given to that fusion must stay valid and unchanged until then;
+ * device errors of the kept rows are reported in the projecting call's
+ * status word.  The choice is made on the host when the calls are issued,
+ * so a CUDA graph should capture such a fusion together with the draft pass
+ * that projects its rows.  Any other call that needs the
  * cells first projects the kept rows with a separate launch on its own
  * stream: a draft pass with n_seq > 1, dflash_fuse_context,
  * dflash_state_read_kv, dflash_state_write_kv and dflash_state_flush.
