@@ -344,8 +344,9 @@ int dflash_state_set_attn_chunks(dflash_state* state, int32_t chunks, int32_t* m
  * time instead of once more by a separate launch), so that layer's
  * attention already sees them.  The positions array (and the dev_status
  * word) given to that fusion must stay valid and unchanged until then;
- * device errors of the kept rows are reported in the projecting call's
- * status word.  The choice is made on the host when the calls are issued,
+ * device errors of the kept rows are reported in the status word of the
+ * draft pass that projects them, or in the fusion's when a separate launch
+ * does.  The choice is made on the host when the calls are issued,
  * so a CUDA graph should capture such a fusion together with the draft pass
  * that projects its rows.  Any other call that needs the
  * cells first projects the kept rows with a separate launch on its own
