@@ -170,16 +170,24 @@ def test_empty_context_and_full_state():
     assert st2.take_status() == 0
 
 
-def test_ragged_vocab():
+@pytest.mark.parametrize("n_slots", [1, 12])
+def test_ragged_vocab(n_slots):
+    """A vocabulary that is not a multiple of the LM head's row tiles (64 for
+    the GEMV head, 256 for the tcgen05 head of 9..16 slots)."""
     cfg = synth.CONFIGS["tiny"].with_(vocab=1000)
     ck, model, om = _model(cfg, seed=27)
-    st = _state(model, 1, 128)
-    ost = _ostate(om, cfg, 128)
-    _fuse_both(st, ost, 0, cfg, synth.make_taps(cfg, 50, seed=27), np.arange(50))
-    (res,) = _draft_both(st, [ost], [999], [50], [6])
-    check_hidden(st.final_hidden[0, :6].cpu().numpy(), res.final_hidden)
-    check_drafts(st.drafts[0].cpu().numpy(), res, 6)
-    assert (st.drafts[0, :5] < 1000).all()
+    st = _state(model, n_slots, 128)
+    osts = []
+    for s in range(n_slots):
+        ost = _ostate(om, cfg, 128)
+        _fuse_both(st, ost, s, cfg, synth.make_taps(cfg, 50 + s, seed=27, stream=s), np.arange(50 + s))
+        osts.append(ost)
+    toks = [999] + list(synth.make_token_ids(cfg, n_slots - 1, seed=27))
+    res = _draft_both(st, osts, toks, [50 + s for s in range(n_slots)], [6] * n_slots)
+    for s in range(n_slots):
+        check_hidden(st.final_hidden[s, :6].cpu().numpy(), res[s].final_hidden, f"slot {s}")
+        check_drafts(st.drafts[s].cpu().numpy(), res[s], 6, f"slot {s}")
+    assert (st.drafts[:n_slots, :5] < 1000).all()
 
 
 def test_device_detected_errors():

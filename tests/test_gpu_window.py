@@ -80,3 +80,37 @@ def test_ring_state_capacity_checks():
             DraftState(model, 1, cap)
         assert e.value.status == DFLASH_ERR_UNSUPPORTED
     DraftState(model, 1, 128).close()
+
+
+def test_window_several_slots():
+    """Three slots with ring states of their own and contexts of different
+    lengths in one pass (the pass's attention chunks are shared out among
+    them by window length), each against the oracle."""
+    from dflash_block_drafter_gb300.runtime import DraftModel, DraftState
+    W, cap = 200, 256
+    cfg = synth.CONFIGS["tiny"].with_(weight_type="bf16", attn_window=W)
+    ck = synth.make_checkpoint(cfg, seed=43)
+    model, om = DraftModel(cfg, ck), O.Model(cfg, ck)
+    ctxs, Bs = [450, 90, 700], [6, 3, 8]
+    st = DraftState(model, 3, cap)
+    osts = []
+    for s, n in enumerate(ctxs):
+        ost = O.State(cfg, cap)
+        for lo in range(0, n, 128):
+            hi = min(n, lo + 128)
+            taps = synth.make_taps(cfg, hi - lo, seed=43, stream=100 * s + lo)
+            pos = np.arange(lo, hi)
+            st.fuse(s, torch.as_tensor(taps.view(np.int16), device="cuda"), device_ids(pos))
+            O.fuse_context(om, ost, taps, pos)
+        osts.append(ost)
+    toks = synth.make_token_ids(cfg, 3, seed=43)
+    st.anchor_tok[:3] = device_ids(toks)
+    st.anchor_pos[:3] = device_ids(ctxs)
+    st.block_len[:3] = device_ids(Bs)
+    st.draft(3)
+    torch.cuda.synchronize()
+    for s in range(3):
+        res = O.draft_block(om, osts[s], int(toks[s]), ctxs[s], Bs[s])
+        check_hidden(st.final_hidden[s, :Bs[s]].cpu().numpy(), res.final_hidden, f"slot {s}")
+        check_drafts(st.drafts[s].cpu().numpy(), res, Bs[s], f"slot {s}")
+    assert st.take_status() == 0
