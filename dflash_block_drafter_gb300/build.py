@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "-Xptxas", "-warn-spills", "-I", INCLUDE]
 SOURCES = ["api.cu", "attention.cu", "misc.cu", "gemv_head.cu", "gemv_bf16.cu", "gemv_q8_0.cu",
-           "gemv_q5_0.cu", "gemv_q4_0.cu", "head_static.cu", "head_tc.cu"]
+           "gemv_q5_0.cu", "gemv_q4_0.cu", "head_static.cu", "head_tc.cu", "gemv_tc.cu"]
 
 
 def nvcc() -> str:

@@ -575,6 +575,16 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<uint32_t>(M)));
   STRY(make_map_2d(&s->k_map, s->K, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
   STRY(make_map_2d(&s->v_map, s->V, static_cast<uint64_t>(arena_rows), d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
+  if (R == 128 && H % 256 == 0 && (nq * d) % 256 == 0 && I % 256 == 0) {
+    // the chunked activations of a 128-row pass as rows of one unit's inputs
+    // (K / KU * planes * 128 rows of KU + 32), for the tcgen05 layer GEMMs
+    const int ku = ku_of(m->wtype), pl = m->wtype == WT_BF16 ? 2 : 1;
+    const CUtensorMapDataType dt = m->wtype == WT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    STRY(make_map_2d(&s->tc_xnorm_map, s->xnorm, static_cast<uint64_t>(H / ku) * pl * 128, ku + 32, dt, 128));
+    STRY(make_map_2d(&s->tc_attn_map, s->attn_out, static_cast<uint64_t>(nq * d / ku) * pl * 128, ku + 32, dt, 128));
+    STRY(make_map_2d(&s->tc_hbuf_map, s->hbuf, static_cast<uint64_t>(I / ku) * pl * 128, ku + 32, dt, 128));
+    s->tc_maps = 1;
+  }
   if (R == 128) {
     // the final normed rows of a 128-row pass, one chunk of H inputs per row (row stride H + 32)
     STRY(make_map_2d(&s->xhead_map, s->xnorm, 2 * 128, static_cast<uint64_t>(H) + 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -767,6 +777,18 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     prof_mark(s, stream);
     TRY(check_gemv(launch_embed(ea, nt, stream), "embed"));
   }
+  // 128-row passes: the layer GEMMs on the tcgen05 tensor cores, every CTA
+  // owning whole 64-row groups
+  const bool tc = nt == 16 && s->tc_maps;
+  auto tc_grid = [&](const GemvArgs& a) {
+    const int groups = a.U / a.UPG;
+    return groups < m->sm_count ? groups : m->sm_count;
+  };
+  TcEpi tc_resid;
+  std::memset(&tc_resid, 0, sizeof(tc_resid));
+  tc_resid.mode = TcEpi::RESID;
+  tc_resid.out = s->x;
+  tc_resid.ldo = H;
   for (int l = 0; l < L; ++l) {
     // q, k, v projections with per-head norm, RoPE and block K/V cells
     {
@@ -826,10 +848,20 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         e.vn_valid = s->pend_n;
         e.vslot = s->pend_slot;
       }
-      LaunchCfg lc{stream, grid_for(*m, a), true};
-      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
-      prof_mark(s, stream);
-      TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "qkv"));
+      if (tc) {
+        a.xmap = s->tc_xnorm_map;
+        TcEpi te;
+        std::memset(&te, 0, sizeof(te));
+        te.mode = TcEpi::HEADS;
+        te.heads = e;
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, tc_grid(a), stream), "qkv"));
+      } else {
+        LaunchCfg lc{stream, grid_for(*m, a), true};
+        if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
+        prof_mark(s, stream);
+        TRY(check_gemv(gemv_heads_any(wt, nt, a, e, lc), "qkv"));
+      }
     }
     prof_mark(s, stream);
     TRY(check_gemv(launch_attention(*m, *s, l, n_seq, nt, anchor_pos, block_len, status, stream), "attention"));
@@ -840,10 +872,16 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       a.ldx = nq * d;
       EpiResid e{s->x, H,
                  PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt), wt != WT_BF16}};
-      LaunchCfg lc{stream, grid_for(*m, a), true};
-      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
-      prof_mark(s, stream);
-      TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
+      if (tc) {
+        a.xmap = s->tc_attn_map;
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_gemv_tc(wt, a, tc_resid, tc_grid(a), stream), "o proj"));
+      } else {
+        LaunchCfg lc{stream, grid_for(*m, a), true};
+        if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
+        prof_mark(s, stream);
+        TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "o proj"));
+      }
     }
     {
       GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
@@ -859,9 +897,21 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         a.X = s->xnorm;
         a.ldx = H;
       }
-      LaunchCfg lc{stream, grid_for(*m, a), true};
-      prof_mark(s, stream);
-      TRY(check_gemv(gemv_swiglu_any(wt, nt, a, s->hbuf, lc), "gate/up"));
+      if (tc) {
+        a.xmap = s->tc_xnorm_map;
+        TcEpi te;
+        std::memset(&te, 0, sizeof(te));
+        te.mode = TcEpi::SWIGLU;
+        te.h = s->hbuf;
+        te.h_ku = ku_of(wt);
+        te.h_f16 = wt != WT_BF16;
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, tc_grid(a), stream), "gate/up"));
+      } else {
+        LaunchCfg lc{stream, grid_for(*m, a), true};
+        prof_mark(s, stream);
+        TRY(check_gemv(gemv_swiglu_any(wt, nt, a, s->hbuf, lc), "gate/up"));
+      }
     }
     {
       GemvArgs a = base_args(m->down[l], *s, CNT_DOWN, status);
@@ -872,10 +922,16 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
                  PackNext{packed ? s->xn : nullptr, s->ssq,
                           l + 1 < L ? m->attn_norm + size_t(l + 1) * H : m->final_norm,
                           l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB, l + 1 < L && wt != WT_BF16}};
-      LaunchCfg lc{stream, grid_for(*m, a), true};
-      if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
-      prof_mark(s, stream);
-      TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
+      if (tc) {
+        a.xmap = s->tc_hbuf_map;
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_gemv_tc(wt, a, tc_resid, tc_grid(a), stream), "down"));
+      } else {
+        LaunchCfg lc{stream, grid_for(*m, a), true};
+        if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
+        prof_mark(s, stream);
+        TRY(check_gemv(gemv_resid_any(wt, nt, a, e, lc), "down"));
+      }
     }
   }
   // final norm + LM head + argmax

@@ -151,6 +151,25 @@ cudaError_t gemv_heads(int nt, const GemvArgs& a, const EpiHeads& e, const Launc
   DFLASH_NT_SWITCH(nt, return launch_gemv<WT, NT, X_STREAM>(a, e, lc);)
 }
 
+// Epilogue of the tcgen05 GEMM of 128-row passes (gemv_tc.cu): applied per
+// finished 64-row group by the thread of each activation row.
+struct TcEpi {
+  enum { STORE = 0, RESID = 1, SWIGLU = 2, HEADS = 3 };
+  int mode;
+  float* out;     // STORE: out[n][m]; RESID: x[n][m] += (fp32, row stride ldo)
+  int ldo;
+  void* h;        // SWIGLU: the down projection's chunked input (128 rows, h_ku inputs per unit)
+  int h_ku;
+  int h_f16;      // one FP16 plane, else BF16 hi and lo planes
+  EpiHeads heads; // HEADS: raw q/k/v into heads.raw, then the per-head epilogue
+  __device__ void apply(int g, int n, const float (&v)[64]) const;
+};
+
+// The 128-row GEMM on tcgen05: a.xmap maps the chunked activations as
+// [K / KU * planes * 128 rows, KU + 32] 16-bit, 64 x 128 boxes, 128-byte
+// swizzle; grid <= the group count (every CTA owns whole 64-row groups).
+cudaError_t launch_gemv_tc(int wt, const GemvArgs& a, const TcEpi& e, int grid, cudaStream_t stream);
+
 // LM head + argmax over the borrowed row-major BF16 head.
 inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc) {
   DFLASH_NT_SWITCH(

@@ -149,6 +149,32 @@ def test_batched_slots(wtype):
     assert st.take_status() == 0
 
 
+@pytest.mark.parametrize("wtype", WTYPES)
+def test_twelve_slots(wtype):
+    """A 128-row pass (12 sequences of their own contexts and block sizes):
+    the layer GEMMs and the LM head on the tcgen05 tensor cores, every slot
+    against the oracle run on that sequence alone, with its K/V cells."""
+    cfg = synth.CONFIGS["tiny"].with_(weight_type=wtype)
+    ck, model, om = _model(cfg, seed=26)
+    cap = 160
+    n = 12
+    st = _state(model, n, cap)
+    ctxs = [40, 97, 5, 64, 130, 18, 77, 2, 150, 33, 88, 120]
+    Bs = [3, 8, 2, 5, 8, 4, 7, 6, 2, 8, 3, 5]
+    osts = []
+    for s_, c in enumerate(ctxs):
+        ost = _ostate(om, cfg, cap)
+        _fuse_both(st, ost, s_, cfg, synth.make_taps(cfg, c, seed=26, stream=s_), np.arange(c))
+        osts.append(ost)
+    toks = synth.make_token_ids(cfg, n, seed=26)
+    res = _draft_both(st, osts, toks, ctxs, Bs)
+    for s_ in range(n):
+        check_hidden(st.final_hidden[s_, :Bs[s_]].cpu().numpy(), res[s_].final_hidden, f"slot {s_}")
+        check_drafts(st.drafts[s_].cpu().numpy(), res[s_], Bs[s_], f"slot {s_}")
+        compare_state(st, osts[s_], s_, ctxs[s_] + Bs[s_], f"slot {s_}")
+    assert st.take_status() == 0
+
+
 def test_empty_context_and_full_state():
     cfg = synth.CONFIGS["tiny"]
     ck, model, om = _model(cfg, seed=26)
