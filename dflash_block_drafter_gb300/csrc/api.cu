@@ -856,6 +856,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         te.heads = e;
         prof_mark(s, stream);
         TRY(check_gemv(launch_gemv_tc(wt, a, te, tc_grid(a), stream), "qkv"));
+        prof_mark(s, stream);
+        TRY(check_gemv(launch_heads_rows(e, nq + 2 * nkv, n_seq, stream), "qkv heads"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, e.gph);
@@ -1141,7 +1143,8 @@ int32_t dflash_draft_launches(const dflash_state* s, int32_t n_seq) {
   const int L = s->model->cfg.n_layers;
   const int nt = pow2ceil(n_seq);
   const bool streamed = !fused_norm(nt);  // separate RMSNorm kernels
-  const int per_layer = 5 + (attn_pass_chunks(*s->model, *s, n_seq) > n_seq ? 1 : 0) + (streamed ? 2 : 0);
+  const int per_layer = 5 + (attn_pass_chunks(*s->model, *s, n_seq) > n_seq ? 1 : 0) + (streamed ? 2 : 0) +
+                        (nt == 16 && s->tc_maps ? 1 : 0);  // the per-head step after a tcgen05 QKV GEMM
   const int head_launches = (nt > 8 && !(nt == 16 && s->model->cfg.hidden % 64 == 0)) ? (n_seq + 7) / 8 : 1;
   return 1 + L * per_layer + head_launches * (streamed ? 2 : 1);
 }

@@ -161,7 +161,7 @@ struct TcEpi {
   void* h;        // SWIGLU: the down projection's chunked input (128 rows, h_ku inputs per unit)
   int h_ku;
   int h_f16;      // one FP16 plane, else BF16 hi and lo planes
-  EpiHeads heads; // HEADS: raw q/k/v into heads.raw, then the per-head epilogue
+  EpiHeads heads; // HEADS: raw q/k/v into heads.raw (launch_heads_rows finishes them)
   __device__ void apply(int g, int n, const float (&v)[64]) const;
 };
 
@@ -169,6 +169,8 @@ struct TcEpi {
 // [K / KU * planes * 128 rows, KU + 32] 16-bit, 64 x 128 boxes, 128-byte
 // swizzle; grid <= the group count (every CTA owns whole 64-row groups).
 cudaError_t launch_gemv_tc(int wt, const GemvArgs& a, const TcEpi& e, int grid, cudaStream_t stream);
+// The per-head epilogue of a 128-row pass's raw q/k/v (mode 0), one CTA per (head, sequence).
+cudaError_t launch_heads_rows(const EpiHeads& e, int n_heads, int n_seq, cudaStream_t stream);
 
 // LM head + argmax over the borrowed row-major BF16 head.
 inline cudaError_t gemv_argmax_impl(int nt, const GemvArgs& a, const ArgmaxParams& p, const LaunchCfg& lc) {

@@ -18,9 +18,9 @@
 //               accumulator -- 64 TMEM columns, 4 groups in flight;
 //   warps 6..9  read a finished group back (thread = activation row, its 64
 //               outputs) and apply the epilogue: store, residual add, SwiGLU
-//               into the down projection's chunked input, or the raw q/k/v
-//               of a head followed by the per-head norm / RoPE / cell writes
-//               of the GEMV's EpiHeads once all groups of the head are done.
+//               into the down projection's chunked input, or the raw q/k/v,
+//               whose per-head norm / RoPE / cell writes heads_rows_kernel
+//               then applies with one CTA per (head, sequence).
 //
 // Every CTA owns whole 64-row groups (grid <= groups), so no partial sums
 // cross CTAs.
@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   uint64_t* acce = accf + kTcSlots;   // [kTcSlots] epilogue warps (4)
   uint64_t* mdone = acce + kTcSlots;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
-  int* sflag = reinterpret_cast<int*>(s_tmem + 1);  // [4]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = static_cast<int>(gridDim.x);
@@ -256,7 +255,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // ------------------------------------------------------------ epilogue
     pdl_launch_dependents();
     const int q = warp & 3;               // TMEM lane quarter
-    const int et = (warp - 6) * 32 + lane; // 0..127 among the epilogue threads
     const int n = q * 32 + lane;          // activation row = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int ng = g1 - g0;
@@ -283,11 +281,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[slot]);
       epi.apply(g, n, v);
-      if (epi.mode == TcEpi::HEADS) {
-        named_bar_sync(1, 128);  // this CTA's raw head values are stored
-        epi.heads.after_group(a, g, et, sflag);
-        named_bar_sync(1, 128);  // sflag reuse
-      }
     }
     if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
   }
@@ -348,6 +341,39 @@ __device__ void TcEpi::apply(int g, int n, const float (&v)[64]) const {
       }
     }
   }
+}
+
+// Per-head RMSNorm, RoPE, FP16 rounding and query / cell writes of a 128-row
+// pass's raw q/k/v (the GEMV's EpiHeads mode 0), one CTA per (head, sequence)
+// over that sequence's 8 block rows.
+__global__ void __launch_bounds__(128) heads_rows_kernel(const __grid_constant__ EpiHeads e) {
+  const int hh = blockIdx.x, s = blockIdx.y;
+  pdl_wait();
+  pdl_launch_dependents();
+  EpiHeads es = e;
+  const int gq = e.n_q / e.n_kv;
+  es.raw = e.raw + static_cast<size_t>(s) * 8 * e.ldr;
+  es.anchor_pos = e.anchor_pos + s;
+  es.block_len = e.block_len + s;
+  es.n_seq = 1;
+  es.rows_ = 8;
+  es.q_ready = e.q_ready + static_cast<size_t>(s) * e.n_kv * gq * 8 * e.d;
+  es.Kst = e.Kst + static_cast<size_t>(s) * e.n_kv * e.cap * e.d;
+  es.Vst = e.Vst + static_cast<size_t>(s) * e.n_kv * e.cap * e.d;
+  es.process_head(hh, threadIdx.x);
+}
+
+cudaError_t launch_heads_rows(const EpiHeads& e, int n_heads, int n_seq, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_heads, n_seq);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, heads_rows_kernel, e);
 }
 
 template <int WT>
