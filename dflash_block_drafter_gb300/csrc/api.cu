@@ -784,6 +784,13 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     const int groups = a.U / a.UPG;
     return groups < m->sm_count ? groups : m->sm_count;
   };
+  // few groups (outputs of the hidden size): each group's inputs in slices
+  auto tc_parts = [&](const GemvArgs& a) {
+    const int groups = a.U / a.UPG;
+    int p = m->sm_count / groups;
+    p = p > a.UPG ? a.UPG : p;
+    return p < 2 ? 1 : p;
+  };
   TcEpi tc_resid;
   std::memset(&tc_resid, 0, sizeof(tc_resid));
   tc_resid.mode = TcEpi::RESID;
@@ -876,8 +883,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
                  PackNext{packed ? s->xn : nullptr, s->ssq, m->mlp_norm + size_t(l) * H, ku_of(wt), wt != WT_BF16}};
       if (tc) {
         a.xmap = s->tc_attn_map;
+        TcEpi te = tc_resid;
+        te.parts = tc_parts(a);
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, tc_resid, tc_grid(a), stream), "o proj"));
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, te.parts > 1 ? (a.U / a.UPG) * te.parts : tc_grid(a), stream),
+                       "o proj"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
@@ -926,8 +936,11 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
                           l + 1 < L ? ku_of(wt) : 32 * Fmt<WT_HEAD>::CB, l + 1 < L && wt != WT_BF16}};
       if (tc) {
         a.xmap = s->tc_hbuf_map;
+        TcEpi te = tc_resid;
+        te.parts = tc_parts(a);
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, tc_resid, tc_grid(a), stream), "down"));
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, te.parts > 1 ? (a.U / a.UPG) * te.parts : tc_grid(a), stream),
+                       "down"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);

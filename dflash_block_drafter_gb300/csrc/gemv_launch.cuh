@@ -162,6 +162,8 @@ struct TcEpi {
   int h_ku;
   int h_f16;      // one FP16 plane, else BF16 hi and lo planes
   EpiHeads heads; // HEADS: raw q/k/v into heads.raw (launch_heads_rows finishes them)
+  int parts;      // > 1: the grid is groups x parts slices of each group's inputs
+                  // (partial sums in GemvArgs::partials, arrivals in GemvArgs::counters)
   __device__ void apply(int g, int n, const float (&v)[64]) const;
 };
 

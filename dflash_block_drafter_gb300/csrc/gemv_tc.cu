@@ -22,8 +22,10 @@
 //               whose per-head norm / RoPE / cell writes heads_rows_kernel
 //               then applies with one CTA per (head, sequence).
 //
-// Every CTA owns whole 64-row groups (grid <= groups), so no partial sums
-// cross CTAs.
+// A CTA owns whole 64-row groups (grid <= groups), or, for matrices of few
+// groups (the projections back to the hidden size), one of `parts` slices of
+// a group's inputs; the slices' sums meet in global memory and the CTA that
+// arrives last adds them in slice order and applies the epilogue.
 #include "gemv_launch.cuh"
 #include "kernels.h"
 
@@ -89,13 +91,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   uint64_t* acce = accf + kTcSlots;   // [kTcSlots] epilogue warps (4)
   uint64_t* mdone = acce + kTcSlots;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
+  int* s_last = reinterpret_cast<int*>(s_tmem + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = static_cast<int>(gridDim.x);
   const int groups = a.U / a.UPG;
-  const int g0 = static_cast<int>(static_cast<long long>(blockIdx.x) * groups / G);
-  const int g1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * groups / G);
-  const int n_units = (g1 - g0) * a.UPG;
+  // whole groups [g0, g1) per CTA, or (epi.parts > 1) part p of group g0's
+  // inputs: units [ub, ue) of the packed matrix, in order
+  int g0, g1, ub, ue;
+  if (epi.parts > 1) {
+    g0 = blockIdx.x / epi.parts;
+    g1 = g0 + 1;
+    const int p = blockIdx.x - g0 * epi.parts;
+    ub = g0 * a.UPG + p * a.UPG / epi.parts;
+    ue = g0 * a.UPG + (p + 1) * a.UPG / epi.parts;
+  } else {
+    g0 = static_cast<int>(static_cast<long long>(blockIdx.x) * groups / G);
+    g1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * groups / G);
+    ub = g0 * a.UPG;
+    ue = g1 * a.UPG;
+  }
+  const int n_units = ue - ub;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -128,7 +144,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     if (lane == 0 && n_units > 0) {
       prefetch_tensormap(&a.xmap);
       const uint64_t pol = l2_policy_evict_first();
-      const int u0 = g0 * a.UPG;
+      const int u0 = ub;
       auto issue_w = [&](int it) {
         uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
         bulk_g2s_hint(dst, a.W + static_cast<size_t>(u0 + it) * F::UNIT, F::UNIT, &full[it % STAGES], pol);
@@ -221,8 +237,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       const uint32_t ring_s = smem_u32(ring), bt_s = smem_u32(btile);
       for (int it = 0; it < n_units && ok; ++it) {
         const int s = it % STAGES, b = it % NB;
-        const int gi = it / a.UPG, j = it - gi * a.UPG, slot = gi % kTcSlots;
-        if (j == 0 && gi >= kTcSlots && !mbar_wait(&acce[slot], ((gi / kTcSlots) - 1) & 1)) {
+        const int u = ub + it, gi = u / a.UPG - g0, slot = gi % kTcSlots;
+        const bool first = u == ub || u % a.UPG == 0;     // the group's first unit in this CTA
+        const bool last = u == ue - 1 || u % a.UPG == a.UPG - 1;
+        if (first && gi >= kTcSlots && !mbar_wait(&acce[slot], ((gi / kTcSlots) - 1) & 1)) {
           ok = false;
           break;
         }
@@ -239,12 +257,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
           for (int p = 0; p < PLANES; ++p) {
             const uint64_t da =
                 umma_desc_sw128(xs + (p * (KU / 64) + (kk >> 2)) * Geo::XBOX + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + slot * 64, da, db, idesc, (j | kk | p) ? 1u : 0u);
+            umma_f16(tmem + slot * 64, da, db, idesc, (!first || kk || p) ? 1u : 0u);
           }
         }
         umma_commit(&empty[s]);
         umma_commit(&bempty[b]);
-        if (j == a.UPG - 1) umma_commit(&accf[slot]);
+        if (last) umma_commit(&accf[slot]);
       }
       // tensor memory may only be freed once every issued MMA has finished
       umma_commit(mdone);
@@ -280,7 +298,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[slot]);
-      epi.apply(g, n, v);
+      if (epi.parts > 1) {
+        // part of the group's sum: published, then the CTA arriving last adds
+        // every part in order and applies the epilogue
+        float* mine = a.partials + (static_cast<size_t>(blockIdx.x) * 128 + n) * 64;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) __stcg(reinterpret_cast<float4*>(mine + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+        named_bar_sync(1, 128);
+        if (warp == 6 && lane == 0) s_last[0] = atomic_add_acq_rel(&a.counters[g], 1) == epi.parts - 1;
+        named_bar_sync(1, 128);
+        if (s_last[0]) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) v[c] = 0.f;
+          for (int p = 0; p < epi.parts; ++p) {
+            const float* pp = a.partials + (static_cast<size_t>(g * epi.parts + p) * 128 + n) * 64;
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(pp + c));
+              v[c] += q4.x;
+              v[c + 1] += q4.y;
+              v[c + 2] += q4.z;
+              v[c + 3] += q4.w;
+            }
+          }
+          epi.apply(g, n, v);
+          if (warp == 6 && lane == 0) a.counters[g] = 0;
+        }
+        named_bar_sync(1, 128);  // s_last reuse
+      } else {
+        epi.apply(g, n, v);
+      }
     }
     if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
   }
