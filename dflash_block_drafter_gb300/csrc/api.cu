@@ -190,7 +190,7 @@ void free_state(State* s) {
   auto f = [](void* p) { if (p) cudaFree(p); };
   f(s->K); f(s->V); f(s->x); f(s->qkv_raw); f(s->q_ready); f(s->attn_out); f(s->hbuf); f(s->xnorm);
   f(s->xn); f(s->ssq); f(s->attn_part); f(s->attn_ml); f(s->attn_plan); f(s->partials); f(s->counters); f(s->argmax_slots); f(s->argmax_ms); f(s->draft_probs); f(s->nonfinite);
-  f(s->head_keys); f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
+  f(s->head_keys); f(s->head_keys8); f(s->h_raw); f(s->kv_raw); f(s->fuse_xnorm); f(s->fuse_xn); f(s->fuse_ssq); f(s->status);
 }
 
 int pow2ceil(int v) {
@@ -585,6 +585,14 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
     STRY(make_map_2d(&s->tc_hbuf_map, s->hbuf, static_cast<uint64_t>(I / ku) * pl * 128, ku + 32, dt, 128));
     s->tc_maps = 1;
   }
+  if (H % 128 == 0) {
+    // the packed rows the LM head of a one-sequence pass reads: per 128-input
+    // chunk the 8 hi rows then the 8 lo rows (row stride 160)
+    STRY(make_map_2d(&s->xn_map, s->xn, static_cast<uint64_t>(H / 128) * 16, 160, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 16));
+  }
+  STRY(dev_alloc(&s->head_keys8, 8 * 8, &total));
+  if (cudaMemset(s->head_keys8, 0, 8 * 8) != cudaSuccess)
+    return fail(cuda_fail(cudaGetLastError(), "cudaMemset head_keys8"));
   if (R == 128) {
     // the final normed rows of a 128-row pass, one chunk of H inputs per row (row stride H + 32)
     STRY(make_map_2d(&s->xhead_map, s->xnorm, 2 * 128, static_cast<uint64_t>(H) + 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -980,7 +988,34 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p.x = s->x;
     p.norm_w = m->final_norm;
     p.status = status;
-    if (packed) {
+    if (packed && H % 128 == 0) {
+      // one sequence: the head on tcgen05, 128 vocabulary rows per MMA
+      HeadTcArgs ha;
+      std::memset(&ha, 0, sizeof(ha));
+      ha.wmap = m->head_map;
+      ha.xmap = s->xn_map;
+      ha.V = c.vocab;
+      ha.H = H;
+      ha.n_seq = 1;
+      ha.block_len = block_len;
+      ha.drafts = drafts;
+      ha.probs = s->draft_probs;
+      ha.min_p = s->spec_min_p;
+      ha.keys = s->head_keys8;
+      ha.ms = s->argmax_ms;
+      ha.grid_cnt = p.grid_cnt;
+      ha.status = status;
+      ha.ssq = s->ssq;
+      ha.eps = c.norm_eps;
+      ha.final_hidden = final_hidden;
+      ha.x = s->x;
+      ha.norm_w = m->final_norm;
+      const int nv = (c.vocab + 127) / 128;
+      if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));
+      prof_mark(s, stream);
+      TRY(check_gemv(launch_head_tc8(ha, nv < m->sm_count ? nv : m->sm_count, stream), "lm head"));
+      if (s->head_ev_end) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_end), stream, cudaEventRecordExternal));
+    } else if (packed) {
       set_packed(a);
       LaunchCfg lc{stream, grid_for(*m, a), true};
       if (s->head_ev_begin) CK(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(s->head_ev_begin), stream, cudaEventRecordExternal));

@@ -131,6 +131,8 @@ struct State {
   CUtensorMap v_map;
   // 128-row passes: xnorm as [2 * 128, H + 32] BF16 rows for the tcgen05 LM head, and its keys
   CUtensorMap xhead_map;
+  CUtensorMap xn_map;  // one-sequence passes: xn as [H / 128 * 16, 160] BF16 rows for the tcgen05 LM head
+  unsigned long long* head_keys8 = nullptr;  // [8], zero between passes
   CUtensorMap tc_xnorm_map, tc_attn_map, tc_hbuf_map;  // 128-row passes: the layer GEMMs' activations
   int tc_maps = 0;
   unsigned long long* head_keys = nullptr;  // [128], zero between passes

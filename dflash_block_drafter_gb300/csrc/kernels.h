@@ -58,8 +58,19 @@ struct HeadTcArgs {
   float2* ms;        // [grid, 128] per-CTA (max logit, sum of exp) when min_p > 0
   int* grid_cnt;     // zero between launches
   int32_t* status;
+  // 8-row passes (launch_head_tc8): xmap maps the packed rows x * w_final (the
+  // chunked layout of 8 rows and 128 inputs per unit, BF16 hi then lo plane)
+  // as [H / 128 * 16 rows, 160] with 64 x 16 boxes; outputs are divided by
+  // each row's RMS from ssq [H / 64][8]; optional final_hidden [8, H] =
+  // x * (1 / RMS) * norm_w
+  const float* ssq;
+  float eps;
+  float* final_hidden;
+  const float* x;
+  const float* norm_w;
 };
 cudaError_t launch_head_tc(const HeadTcArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_head_tc8(const HeadTcArgs& a, int grid, cudaStream_t stream);
 
 cudaError_t launch_repack(int wtype, const void* src, int rows, int K, uint8_t* dst, int row_off, int interleave,
                           cudaStream_t st);
