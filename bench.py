@@ -46,12 +46,13 @@ UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
 # DRAM bytes (read + write) of one LM-head launch at this workload, from one
-# ncu capture of that kernel (dram__bytes_read.sum 778093312 +
-# dram__bytes_write.sum 3127040).  Reset to None whenever the head kernel
+# ncu capture of that kernel (dram__bytes_read.sum 778102016 +
+# dram__bytes_write.sum 3433984).  Reset to None whenever the head kernel
 # changes.
-HEAD_TRAFFIC_BYTES = 781220352
-HEAD_TRAFFIC_SOURCE = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on one LM-head launch of "
-                       "`bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-extras`, library as of commit 8b2e4ca")
+HEAD_TRAFFIC_BYTES = 781536000
+HEAD_TRAFFIC_SOURCE = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on one LM-head launch "
+                       "(head_tc8_kernel) of `bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-extras`, "
+                       "library as of commit 08b743c")
 
 
 def load_peaks():
@@ -610,7 +611,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "step_stats": replay_stats(rep_ev, G),
         "achieved_gbs_step": step_gbs,
         "algorithmic_bytes_per_step": ab["step"],
-        "roofline": {"bound": "hbm", "kernel": "lm_head_argmax (gemv_kernel<WT_HEAD>)",
+        "roofline": {"bound": "hbm", "kernel": "lm_head_argmax (head_tc8_kernel, tcgen05)",
                      "achieved": head_gbs, "peak": peak, "unit": "GB/s", "frac": head_gbs / peak,
                      "peak_kind": peak_kind, "traffic": HEAD_TRAFFIC_BYTES, "traffic_source": HEAD_TRAFFIC_SOURCE,
                      "bytes_per_launch": ab["head"], "avg_launch_ms": head_avg_ms},
