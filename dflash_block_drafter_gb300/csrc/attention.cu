@@ -60,10 +60,11 @@ struct AttnArgs {
 // tcgen05 attention.  Per CTA (chunk, kv head, slot) the M = 8 * GQ query rows
 // (96 for DFlash) are multiplied against the chunk's keys in super-tiles of
 // 128 keys:
-//   warp 0       TMA producer: Q once, then per super-tile two 64-key K tiles
-//                and two V tiles (64 x 64 boxes, 128-byte swizzle);
+//   warp 0       TMA producer: Q once (one barrier per 64-column box), then
+//                per super-tile two 64-key K tiles and two V tiles (64 x 64
+//                boxes, 128-byte swizzle; a K box's two tiles back to back);
 //   warp 1       owns the tensor memory and, from one thread, issues
-//                tcgen05.mma: S[j % 2] = Q K_j^T (M 128, N 64, K 16 per
+//                tcgen05.mma: S[j % 2] = Q K_j^T (M 128, N 128, K 16 per
 //                instruction, FP32 in TMEM) and O += P_j V_j (N = d, V read
 //                MN-major straight from its TMA tile);
 //   warps 2..17  softmax: warp w reads TMEM lane quarter w % 4 (query rows
@@ -76,8 +77,8 @@ struct AttnArgs {
 // softmax; O (d columns) accumulates in TMEM across the chunk.
 //
 // Q occupies only its M rows per 64-column box; the MMA's rows M..127 read
-// whatever follows (the next box, or the K buffer): finite values whose
-// scores, probabilities and outputs stay in those rows and are never used.
+// whatever follows (the next box, or the K buffer): values whose scores,
+// probabilities and outputs stay in those rows and are never used.
 // A lane quarter with no query row skips the softmax arithmetic.
 //
 // Every wait is bounded.  After a timeout a warp stops waiting but still
@@ -243,17 +244,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   float* red_max = reinterpret_cast<float*>(sp + Geo::P_BYTES);  // [2][4 slices][128 rows]
   float* red_l = red_max + 2 * 4 * 128;                          // [4 slices][128 rows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_l + 4 * 128);
-  uint64_t* qfull = bars + 0;
-  uint64_t* kfull = bars + 1;
-  uint64_t* kfree = bars + 2;
-  uint64_t* vfull = bars + 3;
-  uint64_t* vfree = bars + 4;
-  uint64_t* sfull = bars + 5;   // [2]
-  uint64_t* sfree = bars + 7;   // [2]
-  uint64_t* pfull = bars + 9;
-  uint64_t* pfree = bars + 10;
-  uint64_t* mdone = bars + 11;  // every MMA of the CTA has completed
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* qfull = bars + 0;   // [D / 64]: one per 64-column box of Q
+  uint64_t* kfull = bars + 4;
+  uint64_t* kfree = bars + 5;
+  uint64_t* vfull = bars + 6;
+  uint64_t* vfree = bars + 7;
+  uint64_t* sfull = bars + 8;   // [2]
+  uint64_t* sfree = bars + 10;  // [2]
+  uint64_t* pfull = bars + 12;
+  uint64_t* pfree = bars + 13;
+  uint64_t* mdone = bars + 14;  // every MMA of the CTA has completed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 15);
   int* s_plan = reinterpret_cast<int*>(s_tmem + 1);  // [4]: sequence, its chunk, super-tiles per chunk, idle
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int row0 = ((a.layer * a.n_slots + s) * a.n_kv + g) * a.cap;
 
   if (tid == 0) {
-    mbar_init(qfull, 1);
+    for (int b = 0; b < Geo::BOXES; ++b) mbar_init(&qfull[b], 1);
     mbar_init(kfull, 1);
     mbar_init(kfree, 1);
     mbar_init(vfull, 1);
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         mbar_arrive_expect_tx(kfull, 2 * Geo::TILE_BYTES);
         for (int t = 0; t < 2; ++t)
           for (int b = 0; b < Geo::BOXES; ++b)
-            tma_load_2d(sk + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.kmap, b * 64, y + t * kTcKT, kfull);
+            tma_load_2d(sk + b * (kTcKS * 128) + t * (kTcKT * 128), &a.kmap, b * 64, y + t * kTcKT, kfull);
       };
       // tiles kLookAhead super-tiles ahead are asked of L2, so that long
       // chunks find their next K / V there instead of waiting on HBM
@@ -375,8 +376,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       pdl_wait();
       DFLASH_ATTN_STAMP(8);
-      mbar_arrive_expect_tx(qfull, M * D * 2);
-      for (int b = 0; b < Geo::BOXES; ++b) tma_load_2d(sq + b * (M * 128), &a.qmap, b * 64, (s * a.n_kv + g) * M, qfull);
+      for (int b = 0; b < Geo::BOXES; ++b) {
+        mbar_arrive_expect_tx(&qfull[b], M * 128);
+        tma_load_2d(sq + b * (M * 128), &a.qmap, b * 64, (s * a.n_kv + g) * M, &qfull[b]);
+      }
       if (!early) {
         issue_k(0);
         issue_v(0);
@@ -395,7 +398,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // Only the last K and V copies can still be in flight (each earlier one
       // was consumed before its buffer was refilled); they and Q must land
       // before the CTA may exit, also after a timeout.
-      if (!mbar_wait(qfull, 0)) ok = false;
+      for (int b = 0; b < Geo::BOXES; ++b)
+        if (!mbar_wait(&qfull[b], 0)) ok = false;
       if (!mbar_wait(kfull, (nk - 1) & 1)) ok = false;
       if (!mbar_wait(vfull, (nv - 1) & 1)) ok = false;
       if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
@@ -403,24 +407,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nst > 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_f16(128, kTcKT, false, false);
+      // one MMA covers the super-tile's 128 keys: the two 64-key tiles of a
+      // 64-column box lie back to back, 128 rows of 128 bytes
+      constexpr uint32_t idesc_qk = umma_idesc_f16(128, kTcKS, false, false);
       constexpr uint32_t idesc_pv = umma_idesc_f16(128, D, false, true);
       const uint32_t q_s = smem_u32(sq), k_s = smem_u32(sk), v_s = smem_u32(sv), p_s = smem_u32(sp);
       const uint32_t q_box = static_cast<uint32_t>(M) * 128;
-      // S[j % 2] = Q K_j^T; the K buffer is released when it completes
+      // S[j % 2] = Q K_j^T; the K buffer is released when it completes.  The
+      // first super-tile takes each 64-column box of Q as it lands (rows M..127
+      // of a box's MMAs read the next box's memory, landed or not: values
+      // confined to those rows, which nothing uses).
       auto issue_qk = [&](int j) -> bool {
         if (!mbar_wait(kfull, j & 1)) return false;
         if (j == 0) DFLASH_ATTN_STAMP(10);
         if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t da = umma_desc_sw128(q_s + (kk >> 2) * q_box + (kk & 3) * 32, 16, 1024);
-            const uint64_t db =
-                umma_desc_sw128(k_s + t * Geo::TILE_BYTES + (kk >> 2) * (kTcKT * 128) + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + (j & 1) * kTcKS + t * kTcKT, da, db, idesc_qk, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          if (j == 0 && (kk & 3) == 0) {
+            if (!mbar_wait(&qfull[kk >> 2], 0)) return false;
+            tc_fence_after();
           }
+          const uint64_t da = umma_desc_sw128(q_s + (kk >> 2) * q_box + (kk & 3) * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(k_s + (kk >> 2) * (kTcKS * 128) + (kk & 3) * 32, 16, 1024);
+          umma_f16(tmem + (j & 1) * kTcKS, da, db, idesc_qk, kk > 0);
+        }
         umma_commit(&sfull[j & 1]);
         umma_commit(kfree);
         return true;
@@ -429,9 +440,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // it is issued as soon as its K tile (and S buffer) is there, and the PV
       // of super-tile j as soon as P_j and V_j are -- whichever is ready first
       // goes first, so a late K tile never holds up the PV before it.
-      const bool qok = mbar_wait(qfull, 0);
       DFLASH_ATTN_STAMP(9);
-      if (!qok || !issue_qk(0)) ok = false;
+      if (!issue_qk(0)) ok = false;
       DFLASH_ATTN_STAMP(11);
       for (int j = 0; j < nst && ok; ++j) {
         bool qk_next = j + 1 < nst;
