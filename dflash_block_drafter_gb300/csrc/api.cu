@@ -788,16 +788,34 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
   // 128-row passes: the layer GEMMs on the tcgen05 tensor cores, every CTA
   // owning whole 64-row groups
   const bool tc = nt == 16 && s->tc_maps;
-  auto tc_grid = [&](const GemvArgs& a) {
-    const int groups = a.U / a.UPG;
-    return groups < m->sm_count ? groups : m->sm_count;
-  };
   // few groups (outputs of the hidden size): each group's inputs in slices
   auto tc_parts = [&](const GemvArgs& a) {
     const int groups = a.U / a.UPG;
     int p = m->sm_count / groups;
     p = p > a.UPG ? a.UPG : p;
+    p = p > 4 ? 4 : p;  // the GEMM sums at most 4 slices
     return p < 2 ? 1 : p;
+  };
+  // The grid and the multicast cluster of a 128-row GEMM: slices, groups x
+  // parts CTAs in clusters of groups of the same slice; whole groups, the
+  // largest grid of at most one CTA per SM (and at least 70 % of that) that
+  // gives every CTA the same number of groups in clusters of 4 or 2; else
+  // one group range per CTA without clusters.
+  auto tc_launch = [&](const GemvArgs& a, TcEpi& te) {
+    const int groups = a.U / a.UPG;
+    te.mc = 1;
+    if (te.parts > 1) {
+      te.mc = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1);
+      return groups * te.parts;
+    }
+    const int gmax = groups < m->sm_count ? groups : m->sm_count;
+    for (int mc = 4; mc >= 2; mc /= 2)
+      for (int G = gmax - gmax % mc; G >= mc && G * 10 >= gmax * 7; G -= mc)
+        if (groups % G == 0) {
+          te.mc = mc;
+          return G;
+        }
+    return gmax;
   };
   TcEpi tc_resid;
   std::memset(&tc_resid, 0, sizeof(tc_resid));
@@ -870,7 +888,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         te.mode = TcEpi::HEADS;
         te.heads = e;
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, te, tc_grid(a), stream), "qkv"));
+        const int grid = tc_launch(a, te);
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, grid, stream), "qkv"));
         prof_mark(s, stream);
         TRY(check_gemv(launch_heads_rows(e, nq + 2 * nkv, n_seq, stream), "qkv heads"));
       } else {
@@ -893,9 +912,9 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         a.xmap = s->tc_attn_map;
         TcEpi te = tc_resid;
         te.parts = tc_parts(a);
+        const int grid = tc_launch(a, te);
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, te, te.parts > 1 ? (a.U / a.UPG) * te.parts : tc_grid(a), stream),
-                       "o proj"));
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, grid, stream), "o proj"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);
@@ -926,7 +945,8 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         te.h_ku = ku_of(wt);
         te.h_f16 = wt != WT_BF16;
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, te, tc_grid(a), stream), "gate/up"));
+        const int grid = tc_launch(a, te);
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, grid, stream), "gate/up"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         prof_mark(s, stream);
@@ -946,9 +966,9 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
         a.xmap = s->tc_hbuf_map;
         TcEpi te = tc_resid;
         te.parts = tc_parts(a);
+        const int grid = tc_launch(a, te);
         prof_mark(s, stream);
-        TRY(check_gemv(launch_gemv_tc(wt, a, te, te.parts > 1 ? (a.U / a.UPG) * te.parts : tc_grid(a), stream),
-                       "down"));
+        TRY(check_gemv(launch_gemv_tc(wt, a, te, grid, stream), "down"));
       } else {
         LaunchCfg lc{stream, grid_for(*m, a), true};
         if (nt == 1) lc.cluster = plan_cluster(a, lc.grid, 1);

@@ -657,6 +657,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
   }
   // release the tensor memory once every tcgen05 operation of the CTA is done
+  // every warp whole again (lanes that finished their role early wait for
+  // the one still working) before the CTA-wide barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (tid == 0) DFLASH_ATTN_STAMP(7);
@@ -895,7 +898,7 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   a.n_seq = n_seq;
   a.status = status;
   a.qmap = st.q_map;
-  a.trace = trace_slot(st);
+  a.trace = a.Q * a.n_kv <= st.max_grid ? trace_slot(st) : nullptr;
   a.kbase_ptr = st.K;
   a.vbase_ptr = st.V;
   a.plan = n_seq > 1 ? st.attn_plan : nullptr;
@@ -922,7 +925,8 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cb.cap = a.cap;
   cb.plan = st.attn_plan;
   cb.status = status;
-  cb.trace = trace_slot(st);
+  // (diagnostic builds: a grid larger than a trace slot records nothing)
+  cb.trace = c.n_q_heads * (c.head_dim / 32) * n_seq <= st.max_grid ? trace_slot(st) : nullptr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c.n_q_heads, c.head_dim / 32, n_seq);
   cfg.blockDim = dim3(256);

@@ -3,29 +3,45 @@
 // projections are real GEMMs (about 24 GFLOP per layer), which the legacy
 // mma.sync GEMV issues far below its throughput.  Here:
 //
-//   warp 0      streams, per weight unit (64 rows x KU inputs, the packed
-//               fragment-native format of the GEMV), the unit and the
-//               activation chunk it multiplies (128 rows x KU inputs per
-//               plane, as 64-input tensor-map boxes in 128-byte swizzle) into
-//               a 2-stage ring;
-//   warps 1..4  decode the unit with the GEMV's own decoders (warp w: 16-row
+//   warp 0      streams the CTA's weight units (64 rows x KU inputs, the
+//               packed fragment-native format of the GEMV) into a ring of
+//               3..4 stages that the decoders free;
+//   warp 10     streams the activation chunks the units multiply (128 rows x
+//               KU inputs per plane, 64-input tensor-map boxes in 128-byte
+//               swizzle) in half chunks (KU / 2 inputs) into a ring of 3..4
+//               half stages that the MMAs free;
+//   warps 1..4  decode each unit with the GEMV's own decoders (warp w: 16-row
 //               m-tile w) and write it, the GGUF block scale folded in (one
 //               FP16 rounding of d * (q - offset)), as a 64 x KU K-major
-//               operand in 128-byte swizzle;
+//               operand in 128-byte swizzle (two tiles);
 //   warp 5      issues tcgen05.mma kind::f16, M 128 (activation rows, A from
-//               the streamed chunk) x N 64 (the group's weight rows, B from
-//               the decoded tile) x K 16, every plane into the group's FP32
-//               accumulator -- 64 TMEM columns, 4 groups in flight;
+//               the chunk) x N 64 (the group's weight rows, B from the decoded
+//               tile) x K 16, every plane, half by half as the chunk arrives,
+//               into the group's FP32 accumulator -- 64 TMEM columns, 4 groups
+//               in flight;
 //   warps 6..9  read a finished group back (thread = activation row, its 64
 //               outputs) and apply the epilogue: store, residual add, SwiGLU
 //               into the down projection's chunked input, or the raw q/k/v,
 //               whose per-head norm / RoPE / cell writes heads_rows_kernel
 //               then applies with one CTA per (head, sequence).
 //
+// The weights and the activations travel separately, so the weight stream
+// (HBM) runs ahead of the tensor cores by its ring and the decoders never
+// wait for activations; a CTA with at most 4 groups takes its units
+// input-major (for each chunk, every group's unit), one chunk serving all its
+// groups.
+//
 // A CTA owns whole 64-row groups (grid <= groups), or, for matrices of few
 // groups (the projections back to the hidden size), one of `parts` slices of
 // a group's inputs; the slices' sums meet in global memory and the CTA that
 // arrives last adds them in slice order and applies the epilogue.
+//
+// Every unit of one input range multiplies the same activation chunk, so the
+// CTAs of a cluster of e.mc (different groups, the same input range) walk
+// their chunks in step and share them: each loads its share of a half
+// chunk's boxes with a multicast copy into every CTA of the cluster, and a
+// half stage is refilled once the MMAs of all of them have read it (their
+// commits arrive on every CTA's barrier).
 #include "gemv_launch.cuh"
 #include "kernels.h"
 
@@ -33,8 +49,9 @@ namespace dflash {
 
 namespace {
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;
 constexpr int kTcSlots = 4;  // accumulators of 64 TMEM columns in flight
+constexpr int kMaxParts = 4;  // input slices per group (the host plans at most this many)
 
 template <int WT>
 struct TcGeo {
@@ -42,12 +59,19 @@ struct TcGeo {
   static constexpr int KU = F::CB * 32;
   static constexpr int PLANES = F::kF16 ? 1 : 2;  // GGUF: FP16 activations; BF16: hi and lo planes
   static constexpr int XBOX = 128 * 128;          // one 128-row x 64-input box: 16 KB
-  static constexpr int XBYTES = PLANES * (KU / 64) * XBOX;
-  static constexpr int STAGE = ((F::UNIT + XBYTES + 1023) / 1024) * 1024;
+  static constexpr int BOXES = PLANES * (KU / 64);  // boxes of a unit's activation chunk (4 for every format)
+  static constexpr int KBH = KU / 128;            // 64-input columns per half chunk and plane
+  static constexpr int XHALF = (BOXES / 2) * XBOX;  // half a chunk: inputs [h * KU / 2, (h + 1) * KU / 2)
   static constexpr int BTILE = 64 * KU * 2;       // decoded unit, 16-bit
-  static constexpr int STAGES = 2;
-  static constexpr int NB = (1024 + STAGES * STAGE + 2 * BTILE + 1024 <= 227 * 1024) ? 2 : 1;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + NB * BTILE + 1024;
+  static constexpr int NB = 2;
+  static constexpr int BUDGET = 227 * 1024 - 2048;  // alignment slack and barriers
+  // half-chunk stages and weight-unit stages: 4 and at least 3 where they fit, else 3
+  static constexpr int XS = (BUDGET - 4 * XHALF - NB * BTILE) / F::UNIT >= 3 ? 4 : 3;
+  static constexpr int WS0 = (BUDGET - XS * XHALF - NB * BTILE) / F::UNIT;
+  static constexpr int WS = WS0 > 6 ? 6 : WS0;
+  static constexpr int SMEM = 1024 + XS * XHALF + NB * BTILE + WS * F::UNIT + 1024;
+  static_assert(BOXES == 4 && WS >= 2 && SMEM <= 227 * 1024, "GEMM stage plan");
+  static_assert(F::UNIT % 1024 == 0, "weight units keep the 1024-byte alignment of what follows");
 };
 
 // Instruction descriptor of kind::f16, FP32 accumulation, K-major A and B,
@@ -78,14 +102,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
                                                                 const __grid_constant__ TcEpi epi) {
   using Geo = TcGeo<WT>;
   using F = Fmt<WT>;
-  constexpr int KU = Geo::KU, PLANES = Geo::PLANES, STAGES = Geo::STAGES, NB = Geo::NB;
+  constexpr int KU = Geo::KU, PLANES = Geo::PLANES, NB = Geo::NB, XS = Geo::XS, WS = Geo::WS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;                          // [STAGES][unit | X boxes]
-  uint8_t* btile = ring + STAGES * Geo::STAGE;   // [NB][64 x KU, 16-bit]
-  uint64_t* full = reinterpret_cast<uint64_t*>(btile + NB * Geo::BTILE);
-  uint64_t* empty = full + STAGES;    // decoders (4) + MMA commit (1)
-  uint64_t* bfull = empty + STAGES;   // [NB] decoders (4)
+  uint8_t* xring = smem;                          // [XS][half chunk: BOXES / 2 boxes]
+  uint8_t* btile = xring + XS * Geo::XHALF;       // [NB][64 x KU, 16-bit]
+  uint8_t* wring = btile + NB * Geo::BTILE;       // [WS][weight unit]
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + WS * F::UNIT);
+  uint64_t* xempty = xfull + XS;      // the MMA commits of the cluster's CTAs
+  uint64_t* wfull = xempty + XS;
+  uint64_t* wempty = wfull + WS;      // decoders (4)
+  uint64_t* bfull = wempty + WS;      // [NB] decoders (4)
   uint64_t* bempty = bfull + NB;      // [NB] MMA commit
   uint64_t* accf = bempty + NB;       // [kTcSlots] MMA commit at a group's end
   uint64_t* acce = accf + kTcSlots;   // [kTcSlots] epilogue warps (4)
@@ -97,26 +124,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const int G = static_cast<int>(gridDim.x);
   const int groups = a.U / a.UPG;
   // whole groups [g0, g1) per CTA, or (epi.parts > 1) part p of group g0's
-  // inputs: units [ub, ue) of the packed matrix, in order
-  int g0, g1, ub, ue;
+  // inputs: units j in [jb, je) of each of the CTA's groups
+  int g0, g1, jb, je, slice = blockIdx.x;
   if (epi.parts > 1) {
-    g0 = blockIdx.x / epi.parts;
+    // CTA p * groups + g: a cluster's CTAs share the slice p of the inputs
+    const int p = blockIdx.x / groups;
+    g0 = blockIdx.x - p * groups;
     g1 = g0 + 1;
-    const int p = blockIdx.x - g0 * epi.parts;
-    ub = g0 * a.UPG + p * a.UPG / epi.parts;
-    ue = g0 * a.UPG + (p + 1) * a.UPG / epi.parts;
+    slice = g0 * epi.parts + p;
+    jb = p * a.UPG / epi.parts;
+    je = (p + 1) * a.UPG / epi.parts;
   } else {
     g0 = static_cast<int>(static_cast<long long>(blockIdx.x) * groups / G);
     g1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * groups / G);
-    ub = g0 * a.UPG;
-    ue = g1 * a.UPG;
+    jb = 0;
+    je = a.UPG;
   }
-  const int n_units = ue - ub;
+  const int ng = g1 - g0, nj = je - jb;
+  const int n_units = ng * nj;
+  // Unit order.  With at most kTcSlots groups the units go input-major
+  // (j outer, group inner): one activation chunk serves all the CTA's groups,
+  // every group in its own accumulator.  Else group-major, a chunk per unit.
+  const bool jmajor = ng <= kTcSlots;
+  const int n_chunks = jmajor ? nj : n_units;
+  auto unit_of = [&](int it, int& gi, int& j) {
+    if (jmajor) {
+      j = jb + it / ng;
+      gi = it - (it / ng) * ng;
+    } else {
+      gi = it / nj;
+      j = jb + it - gi * nj;
+    }
+  };
+  const int mc = epi.mc > 1 ? epi.mc : 1;
+  const uint32_t rank = mc > 1 ? cluster_ctarank() : 0u;
+  const uint16_t mask = static_cast<uint16_t>((1u << mc) - 1u);
+#ifdef DFLASH_TRACE
+  unsigned long long* tr = a.trace ? a.trace + static_cast<size_t>(blockIdx.x) * kTraceSlots : nullptr;
+  if (tr && tid == 0) tr[0] = globaltimer_ns();
+  long long tw_a = 0, tw_b = 0;
+#define TW(acc, expr) ([&]() { const long long t0_ = clock64(); const bool r_ = (expr); acc += clock64() - t0_; return r_; }())
+#else
+#define TW(acc, expr) (expr)
+#endif
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 5);
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], mc);
+    }
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 4);
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(&bfull[b], 4);
@@ -136,67 +195,94 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peers' barriers are initialised once every CTA has signalled here
+  // (each role waits for that before its first access to a peer)
+  if (mc > 1) cluster_arrive_relaxed();
   const uint32_t tmem = *s_tmem;
   bool ok = true;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ---------------------------------------------------- weight producer
+    if (mc > 1) cluster_wait();
     if (lane == 0 && n_units > 0) {
-      prefetch_tensormap(&a.xmap);
       const uint64_t pol = l2_policy_evict_first();
-      const int u0 = ub;
-      auto issue_w = [&](int it) {
-        uint8_t* dst = ring + (it % STAGES) * Geo::STAGE;
-        bulk_g2s_hint(dst, a.W + static_cast<size_t>(u0 + it) * F::UNIT, F::UNIT, &full[it % STAGES], pol);
-      };
-      auto issue_x = [&](int it) {
-        const int j = (u0 + it) % a.UPG;
-        uint8_t* dst = ring + (it % STAGES) * Geo::STAGE + F::UNIT;
-        // F::UNIT is a multiple of 1024 for every format (16384, 17408, 9216, 11264)
-        for (int p = 0; p < PLANES; ++p)
-          for (int kb = 0; kb < KU / 64; ++kb)
-            tma_load_2d(dst + (p * (KU / 64) + kb) * Geo::XBOX, &a.xmap, kb * 64, (j * PLANES + p) * 128,
-                        &full[it % STAGES]);
-      };
-      const int npre = n_units < STAGES ? n_units : STAGES;
-      for (int it = 0; it < npre; ++it) {
-        mbar_arrive_expect_tx(&full[it], F::UNIT + Geo::XBYTES);
-        issue_w(it);
-      }
-      pdl_wait();  // the activations come from the previous kernel
-      for (int it = 0; it < npre; ++it) issue_x(it);
-      int issued = npre;
-      for (int it = npre; it < n_units; ++it) {
-        const int s = it % STAGES;
-        if (!mbar_wait(&empty[s], ((it / STAGES) - 1) & 1)) {
+      int issued = 0;
+      for (int it = 0; it < n_units; ++it) {
+        const int s = it % WS;
+        if (it >= WS && !TW(tw_a, mbar_wait(&wempty[s], ((it / WS) - 1) & 1))) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], F::UNIT + Geo::XBYTES);
-        issue_w(it);
-        issue_x(it);
+        int gi, j;
+        unit_of(it, gi, j);
+        mbar_arrive_expect_tx(&wfull[s], F::UNIT);
+        bulk_g2s_hint(wring + s * F::UNIT, a.W + (static_cast<size_t>(g0 + gi) * a.UPG + j) * F::UNIT, F::UNIT,
+                      &wfull[s], pol);
         issued = it + 1;
       }
-      for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-        if (!mbar_wait(&full[it % STAGES], (it / STAGES) & 1)) {
+      // every issued copy must land before the CTA may exit
+      for (int it = (issued > WS ? issued - WS : 0); it < issued; ++it)
+        if (!mbar_wait(&wfull[it % WS], (it / WS) & 1)) ok = false;
+      if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------ activation producer
+    if (mc > 1) cluster_wait();
+    if (lane == 0 && n_units > 0) {
+      prefetch_tensormap(&a.xmap);
+      pdl_wait();  // the activations come from the previous kernel
+#ifdef DFLASH_TRACE
+      if (tr) tr[9] = globaltimer_ns();
+#endif
+      // half chunk q = 2 c + h of chunk c (inputs j's half h), stage q % XS;
+      // its boxes are shared out over the cluster, each multicast to all
+      const int nq = 2 * n_chunks;
+      int issued = 0;
+      for (int q = 0; q < nq; ++q) {
+        const int s = q % XS, c = q >> 1, h = q & 1;
+        if (q >= XS && !TW(tw_b, mbar_wait(&xempty[s], ((q / XS) - 1) & 1))) {
           ok = false;
           break;
         }
+        int gi, j;
+        unit_of(jmajor ? c * ng : c, gi, j);
+        mbar_arrive_expect_tx(&xfull[s], Geo::XHALF);
+        uint8_t* dst = xring + s * Geo::XHALF;
+#pragma unroll
+        for (int p = 0; p < PLANES; ++p)
+#pragma unroll
+          for (int kh = 0; kh < Geo::KBH; ++kh) {
+            const int i = p * Geo::KBH + kh;  // box of the half
+            const int x = (h * Geo::KBH + kh) * 64, y = (j * PLANES + p) * 128;
+            if (mc == 1) tma_load_2d(dst + i * Geo::XBOX, &a.xmap, x, y, &xfull[s]);
+            else if ((q * 2 + i) % mc == static_cast<int>(rank))
+              tma_load_2d_mc(dst + i * Geo::XBOX, &a.xmap, x, y, &xfull[s], mask);
+          }
+        issued = q + 1;
+      }
+      for (int q = (issued > XS ? issued - XS : 0); q < issued; ++q)
+        if (!mbar_wait(&xfull[q % XS], (q / XS) & 1)) ok = false;
+      // the cluster's last commits on this CTA's stages have arrived (no
+      // peer signals it after this)
+      if (mc > 1)
+        for (int s = 0; s < XS && s < issued; ++s)
+          if (!mbar_wait(&xempty[s], ((issued - 1 - s) / XS) & 1)) ok = false;
       if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
     } else if (lane == 0) {
       pdl_wait();
     }
   } else if (warp >= 1 && warp <= 4) {
     // ------------------------------------------------------------ decoders
+    if (mc > 1) cluster_wait();
     const int w = warp - 1;  // m-tile: weight rows 16 w .. 16 w + 15 of the group
     const int gr = lane >> 2, t4 = lane & 3;
-    const uint32_t ring_s = smem_u32(ring), bt_s = smem_u32(btile);
+    const uint32_t w_s = smem_u32(wring), bt_s = smem_u32(btile);
     for (int it = 0; it < n_units && ok; ++it) {
-      const int s = it % STAGES, b = it % NB;
-      if (!mbar_wait(&full[s], (it / STAGES) & 1)) ok = false;
-      if (ok && it >= NB && !mbar_wait(&bempty[b], ((it / NB) - 1) & 1)) ok = false;
+      const int s = it % WS, b = it % NB;
+      if (!TW(tw_a, mbar_wait(&wfull[s], (it / WS) & 1))) ok = false;
+      if (ok && it >= NB && !TW(tw_b, mbar_wait(&bempty[b], ((it / NB) - 1) & 1))) ok = false;
       if (!ok) break;
-      const uint32_t ub = ring_s + s * Geo::STAGE, bb = bt_s + b * Geo::BTILE;
+      const uint32_t ub = w_s + s * F::UNIT, bb = bt_s + b * Geo::BTILE;
       auto put = [&](int bl, const BlockFrag& f) {
         uint32_t d0 = 0, d8 = 0;
         if constexpr (F::kF16) {
@@ -221,49 +307,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
           put(bl, decode_block<WT, F::kF16>(ub, w, lane, bl));
         }
       }
-      // generic-proxy writes of the tile, then its hand-off to the tensor cores
+      // the unit's codes have been read; generic-proxy writes of the tile,
+      // then its hand-off to the tensor cores
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&wempty[s]);
         mbar_arrive(&bfull[b]);
-        mbar_arrive(&empty[s]);  // the unit's codes have been read
       }
     }
     if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    if (mc > 1) cluster_wait();
     if (lane == 0 && n_units > 0) {
       constexpr uint32_t idesc = idesc_16(128, 64, !F::kF16);
-      const uint32_t ring_s = smem_u32(ring), bt_s = smem_u32(btile);
+      const uint32_t x_s = smem_u32(xring), bt_s = smem_u32(btile);
       for (int it = 0; it < n_units && ok; ++it) {
-        const int s = it % STAGES, b = it % NB;
-        const int u = ub + it, gi = u / a.UPG - g0, slot = gi % kTcSlots;
-        const bool first = u == ub || u % a.UPG == 0;     // the group's first unit in this CTA
-        const bool last = u == ue - 1 || u % a.UPG == a.UPG - 1;
-        if (first && gi >= kTcSlots && !mbar_wait(&acce[slot], ((gi / kTcSlots) - 1) & 1)) {
+        const int b = it % NB;
+        int gi, j;
+        unit_of(it, gi, j);
+        const int slot = gi % kTcSlots;
+        const int c = jmajor ? it / ng : it;             // the unit's chunk
+        const bool new_chunk = !jmajor || gi == 0;
+        const bool end_chunk = !jmajor || gi == ng - 1;  // the chunk's last unit
+        const bool first = j == jb, last = j == je - 1;  // the group's first / last unit here
+        if (first && !jmajor && gi >= kTcSlots && !mbar_wait(&acce[slot], ((gi / kTcSlots) - 1) & 1)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&full[s], (it / STAGES) & 1) || !mbar_wait(&bfull[b], (it / NB) & 1)) {
+        if (!TW(tw_b, mbar_wait(&bfull[b], (it / NB) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t xs = ring_s + s * Geo::STAGE + F::UNIT, bs = bt_s + b * Geo::BTILE;
+        const uint32_t bs = bt_s + b * Geo::BTILE;
 #pragma unroll
-        for (int kk = 0; kk < KU / 16; ++kk) {
-          const uint64_t db = umma_desc_sw128(bs + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
+        for (int h = 0; h < 2; ++h) {
+          const int q = 2 * c + h, s = q % XS;
+          if (new_chunk) {
+            if (!TW(tw_a, mbar_wait(&xfull[s], (q / XS) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t xs = x_s + s * Geo::XHALF;
 #pragma unroll
-          for (int p = 0; p < PLANES; ++p) {
-            const uint64_t da =
-                umma_desc_sw128(xs + (p * (KU / 64) + (kk >> 2)) * Geo::XBOX + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + slot * 64, da, db, idesc, (!first || kk || p) ? 1u : 0u);
+          for (int kq = 0; kq < KU / 32; ++kq) {  // the half's k-steps of 16 inputs
+            const int kk = h * (KU / 32) + kq;
+            const uint64_t db = umma_desc_sw128(bs + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
+#pragma unroll
+            for (int p = 0; p < PLANES; ++p) {
+              const uint64_t da =
+                  umma_desc_sw128(xs + (p * Geo::KBH + (kq >> 2)) * Geo::XBOX + (kq & 3) * 32, 16, 1024);
+              umma_f16(tmem + slot * 64, da, db, idesc, (!first || kk || p) ? 1u : 0u);
+            }
+          }
+          // the half chunk may be refilled once its last unit's MMAs are done
+          if (end_chunk) {
+            if (mc > 1) umma_commit_mc(&xempty[s], mask);
+            else umma_commit(&xempty[s]);
           }
         }
-        umma_commit(&empty[s]);
+        if (!ok) break;
         umma_commit(&bempty[b]);
         if (last) umma_commit(&accf[slot]);
       }
+#ifdef DFLASH_TRACE
+      if (tr) tr[10] = globaltimer_ns();
+#endif
       // tensor memory may only be freed once every issued MMA has finished
       umma_commit(mdone);
       if (!mbar_wait(mdone, 0)) ok = false;
@@ -271,14 +384,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    if (mc > 1) cluster_wait();
     pdl_launch_dependents();
     const int q = warp & 3;               // TMEM lane quarter
     const int n = q * 32 + lane;          // activation row = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int ng = g1 - g0;
+    bool staged_ok = false;
     for (int gi = 0; gi < ng; ++gi) {
       const int slot = gi % kTcSlots, g = g0 + gi;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&accf[slot], (gi / kTcSlots) & 1));
+      if (ok) ok = __all_sync(0xffffffffu, TW(tw_a, mbar_wait(&accf[slot], (gi / kTcSlots) & 1)));
       tc_fence_after();
       float v[64];
       {
@@ -299,46 +413,107 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[slot]);
       if (epi.parts > 1) {
-        // part of the group's sum: published, then the CTA arriving last adds
-        // every part in order and applies the epilogue
-        float* mine = a.partials + (static_cast<size_t>(blockIdx.x) * 128 + n) * 64;
+        // part of the group's sum: published ([slice][16-byte column][row],
+        // so that a warp's accesses are consecutive), then the CTA arriving
+        // last adds every part in order and applies the epilogue
+        float4* part4 = reinterpret_cast<float4*>(a.partials);
+        float4* mine = part4 + static_cast<size_t>(slice) * 16 * 128 + n;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) __stcg(reinterpret_cast<float4*>(mine + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+        for (int c4 = 0; c4 < 16; ++c4)
+          __stcg(mine + c4 * 128, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
         named_bar_sync(1, 128);
+#ifdef DFLASH_TRACE
+        if (tr && warp == 6 && lane == 0) tr[12] = globaltimer_ns();
+#endif
         if (warp == 6 && lane == 0) s_last[0] = atomic_add_acq_rel(&a.counters[g], 1) == epi.parts - 1;
         named_bar_sync(1, 128);
-        if (s_last[0]) {
+#ifdef DFLASH_TRACE
+        if (tr && warp == 6 && lane == 0) tr[13] = globaltimer_ns();
+#endif
+        const bool last_part = s_last[0] != 0;
+        named_bar_sync(1, 128);  // s_last may be reused
+        if (!last_part) continue;
+        // every part's row, this CTA's own included, in part order; a quarter
+        // row's loads of all parts are issued together, then added
 #pragma unroll
-          for (int c = 0; c < 64; ++c) v[c] = 0.f;
-          for (int p = 0; p < epi.parts; ++p) {
-            const float* pp = a.partials + (static_cast<size_t>(g * epi.parts + p) * 128 + n) * 64;
+        for (int c0 = 0; c0 < 16; c0 += 4) {
+          float4 q4[kMaxParts][4];
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(pp + c));
-              v[c] += q4.x;
-              v[c + 1] += q4.y;
-              v[c + 2] += q4.z;
-              v[c + 3] += q4.w;
+          for (int p = 0; p < kMaxParts; ++p)
+            if (p < epi.parts) {
+              const float4* pp = part4 + static_cast<size_t>(g * epi.parts + p) * 16 * 128 + n;
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) q4[p][c4] = __ldcg(pp + (c0 + c4) * 128);
             }
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float4 acc4 = q4[0][c4];
+#pragma unroll
+            for (int p = 1; p < kMaxParts; ++p)
+              if (p < epi.parts) {
+                acc4.x += q4[p][c4].x;
+                acc4.y += q4[p][c4].y;
+                acc4.z += q4[p][c4].z;
+                acc4.w += q4[p][c4].w;
+              }
+            const int c = 4 * (c0 + c4);
+            v[c] = acc4.x;
+            v[c + 1] = acc4.y;
+            v[c + 2] = acc4.z;
+            v[c + 3] = acc4.w;
           }
-          epi.apply(g, n, v);
-          if (warp == 6 && lane == 0) a.counters[g] = 0;
         }
-        named_bar_sync(1, 128);  // s_last reuse
+#ifdef DFLASH_TRACE
+        if (tr && warp == 6 && lane == 0) tr[11] = globaltimer_ns();
+#endif
+        if (warp == 6 && lane == 0) a.counters[g] = 0;
+      }
+      if (jmajor) {
+        // every MMA is done once the last group's are (input-major order):
+        // the activation ring is free, and each warp stages its 32 rows
+        // there to write them out row-contiguously
+        if (!staged_ok) {
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mdone, 0));
+          staged_ok = true;
+        }
+        epi.apply_staged(g, q, lane, v, reinterpret_cast<float*>(xring) + (warp - 6) * 32 * TcEpi::kStageLd);
       } else {
         epi.apply(g, n, v);
       }
     }
     if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
+#ifdef DFLASH_TRACE
+    if (tr && warp == 6 && lane == 0) tr[14] = globaltimer_ns();
+#endif
   }
-  // release the tensor memory once every tcgen05 operation of the CTA is done
+  // release the tensor memory once every tcgen05 operation of the CTA is done;
+  // no CTA leaves while a peer may still write to its shared memory
+#ifdef DFLASH_TRACE
+  if (tr) {
+    if (warp == 0 && lane == 0) { tr[1] = tw_a; }
+    if (warp == 1 && lane == 0) { tr[2] = tw_a; tr[3] = tw_b; }
+    if (warp == 5 && lane == 0) { tr[4] = tw_a; tr[5] = tw_b; }
+    if (warp == 6 && lane == 0) { tr[6] = tw_a; tr[8] = n_units; }
+  }
+#endif
+  // every warp whole again (lanes that finished their role early wait for
+  // the one still working) before the CTA-wide barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
+#ifdef DFLASH_TRACE
+  if (tr && tid == 0) tr[15] = globaltimer_ns();
+#endif
+  if (mc > 1) cluster_sync_all();
+#ifdef DFLASH_TRACE
+  if (tr && threadIdx.x == 0) tr[7] = globaltimer_ns();
+#endif
   if (warp == 5) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 64 * kTcSlots);
   }
+#undef TW
 }
 
 }  // namespace
@@ -352,15 +527,18 @@ __device__ void TcEpi::apply(int g, int n, const float (&v)[64]) const {
 #pragma unroll
     for (int c = 0; c < 64; c += 4) __stcg(reinterpret_cast<float4*>(o + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
   } else if (mode == RESID) {
-    float* o = out + static_cast<size_t>(n) * ldo + g * 64;
+    // the row's 16 loads first (in flight together), then the adds and stores
+    float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(n) * ldo + g * 64);
+    float4 x[16];
 #pragma unroll
-    for (int c = 0; c < 64; c += 4) {
-      float4 x = __ldcg(reinterpret_cast<const float4*>(o + c));
-      x.x += v[c];
-      x.y += v[c + 1];
-      x.z += v[c + 2];
-      x.w += v[c + 3];
-      __stcg(reinterpret_cast<float4*>(o + c), x);
+    for (int c4 = 0; c4 < 16; ++c4) x[c4] = __ldcg(o + c4);
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4) {
+      x[c4].x += v[4 * c4];
+      x[c4].y += v[4 * c4 + 1];
+      x[c4].z += v[4 * c4 + 2];
+      x[c4].w += v[4 * c4 + 3];
+      __stcg(o + c4, x[c4]);
     }
   } else {  // SWIGLU: per 16-row m-tile, 8 gate rows then the 8 up rows of outputs g * 32 + 8 w' + r
 #pragma unroll
@@ -388,6 +566,84 @@ __device__ void TcEpi::apply(int g, int n, const float (&v)[64]) const {
       }
     }
   }
+}
+
+__device__ void TcEpi::apply_staged(int g, int q, int lane, const float (&v)[64], float* S) const {
+  float* mine = S + lane * kStageLd;  // 272-byte rows: a quarter warp's 16-byte stores hit all 32 banks once
+  if (mode == SWIGLU) {
+    // per 16-row m-tile, 8 gate rows then the 8 up rows of outputs g * 32 + 8 w' + r
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) {
+      float hv[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float gt = v[w2 * 16 + r];
+        hv[r] = gt / (1.f + __expf(-gt)) * v[w2 * 16 + 8 + r];
+      }
+      reinterpret_cast<float4*>(mine)[2 * w2] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+      reinterpret_cast<float4*>(mine)[2 * w2 + 1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+    }
+  } else {
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4)
+      reinterpret_cast<float4*>(mine)[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+  }
+  __syncwarp();
+  if (mode == SWIGLU) {
+    // row r's 32 outputs are 64 contiguous bytes of its chunk row (per plane):
+    // four lanes per row, eight rows per step
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int r = it * 8 + (lane >> 2), pc = lane & 3;
+      const float4 a = reinterpret_cast<const float4*>(S + r * kStageLd)[2 * pc];
+      const float4 b = reinterpret_cast<const float4*>(S + r * kStageLd)[2 * pc + 1];
+      const int o = g * 32 + pc * 8, n = q * 32 + r;
+      if (h_f16) {
+        *reinterpret_cast<uint4*>(static_cast<__half*>(h) + xchunk_index(o, n, 0, 128, h_ku, 1)) =
+            make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(b.x, b.y), pack_f16x2(b.z, b.w));
+      } else {
+        uint4 hi, lo;
+        split_bf16x2(a.x, a.y, hi.x, lo.x);
+        split_bf16x2(a.z, a.w, hi.y, lo.y);
+        split_bf16x2(b.x, b.y, hi.z, lo.z);
+        split_bf16x2(b.z, b.w, hi.w, lo.w);
+        __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(h);
+        *reinterpret_cast<uint4*>(hp + xchunk_index(o, n, 0, 128, h_ku, 2)) = hi;
+        *reinterpret_cast<uint4*>(hp + xchunk_index(o, n, 1, 128, h_ku, 2)) = lo;
+      }
+    }
+  } else {
+    // two rows per step: lanes 0..15 and 16..31 each cover one row's 64 outputs
+    float* base = mode == HEADS ? heads.raw : out;
+    const int ld = mode == HEADS ? heads.ldr : ldo;
+    const int c4 = lane & 15;
+    if (mode == RESID) {
+      float4 x[16];
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int n = q * 32 + 2 * it + (lane >> 4);
+        x[it] = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(n) * ld + g * 64) + c4);
+      }
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int r = 2 * it + (lane >> 4), n = q * 32 + r;
+        const float4 y = reinterpret_cast<const float4*>(S + r * kStageLd)[c4];
+        x[it].x += y.x;
+        x[it].y += y.y;
+        x[it].z += y.z;
+        x[it].w += y.w;
+        __stcg(reinterpret_cast<float4*>(base + static_cast<size_t>(n) * ld + g * 64) + c4, x[it]);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int r = 2 * it + (lane >> 4), n = q * 32 + r;
+        __stcg(reinterpret_cast<float4*>(base + static_cast<size_t>(n) * ld + g * 64) + c4,
+               reinterpret_cast<const float4*>(S + r * kStageLd)[c4]);
+      }
+    }
+  }
+  __syncwarp();  // S is reused by the next group
 }
 
 // Per-head RMSNorm, RoPE, FP16 rounding and query / cell writes of a 128-row
@@ -426,6 +682,9 @@ cudaError_t launch_heads_rows(const EpiHeads& e, int n_heads, int n_seq, cudaStr
 template <int WT>
 static cudaError_t launch_tc(const GemvArgs& a, const TcEpi& e, int grid, cudaStream_t stream) {
   using Geo = TcGeo<WT>;
+  // a cluster's CTAs share each chunk's boxes: mc must divide the box count and the grid
+  if (e.mc > 1 && (e.mc > 4 || Geo::BOXES % e.mc != 0 || grid % e.mc != 0)) return cudaErrorInvalidValue;
+  if (e.parts > kMaxParts) return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(gemv_tc_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo::SMEM);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -433,11 +692,15 @@ static cudaError_t launch_tc(const GemvArgs& a, const TcEpi& e, int grid, cudaSt
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = Geo::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = e.mc > 1 ? e.mc : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = e.mc > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<WT>, a, e);
 }
 

@@ -285,6 +285,9 @@ __global__ void __launch_bounds__(kHtThreads, 1) head_tc_kernel(const __grid_con
     }
   }
   // release the tensor memory once every tcgen05 operation of the CTA is done
+  // every warp whole again (lanes that finished their role early wait for
+  // the one still working) before the CTA-wide barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -602,6 +605,9 @@ __global__ void __launch_bounds__(kHtThreads, 1) head_tc8_kernel(const __grid_co
       if (et == 0) *a.grid_cnt = 0;
     }
   }
+  // every warp whole again (lanes that finished their role early wait for
+  // the one still working) before the CTA-wide barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
