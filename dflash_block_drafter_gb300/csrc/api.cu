@@ -796,25 +796,16 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     p = p > 4 ? 4 : p;  // the GEMM sums at most 4 slices
     return p < 2 ? 1 : p;
   };
-  // The grid and the multicast cluster of a 128-row GEMM: slices, groups x
-  // parts CTAs in clusters of groups of the same slice; whole groups, the
-  // largest grid of at most one CTA per SM (and at least 70 % of that) that
-  // gives every CTA the same number of groups in clusters of 4 or 2; else
-  // one group range per CTA without clusters.
-  auto tc_launch = [&](const GemvArgs& a, TcEpi& te) {
+  // The grid of a 128-row GEMM: slices, groups x parts CTAs; whole groups,
+  // the largest grid of at most one CTA per SM (and at least 70 % of that)
+  // that gives every CTA the same number of groups, else one group range
+  // per CTA over min(groups, SMs) CTAs.
+  auto tc_launch = [&](const GemvArgs& a, const TcEpi& te) {
     const int groups = a.U / a.UPG;
-    te.mc = 1;
-    if (te.parts > 1) {
-      te.mc = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1);
-      return groups * te.parts;
-    }
+    if (te.parts > 1) return groups * te.parts;
     const int gmax = groups < m->sm_count ? groups : m->sm_count;
-    for (int mc = 4; mc >= 2; mc /= 2)
-      for (int G = gmax - gmax % mc; G >= mc && G * 10 >= gmax * 7; G -= mc)
-        if (groups % G == 0) {
-          te.mc = mc;
-          return G;
-        }
+    for (int G = gmax; G >= 1 && G * 10 >= gmax * 7; --G)
+      if (groups % G == 0) return G;
     return gmax;
   };
   TcEpi tc_resid;

@@ -164,9 +164,6 @@ struct TcEpi {
   EpiHeads heads; // HEADS: raw q/k/v into heads.raw (launch_heads_rows finishes them)
   int parts;      // > 1: the grid is groups x parts slices of each group's inputs
                   // (partial sums in GemvArgs::partials, arrivals in GemvArgs::counters)
-  int mc;         // CTAs per cluster sharing each activation chunk (1, 2 or 4): the
-                  // CTAs of a cluster walk the same input units in step, each loads
-                  // 1 / mc of the chunk's boxes and multicasts them to all
   __device__ void apply(int g, int n, const float (&v)[64]) const;
   // The same for the 32 rows q * 32 .. q * 32 + 31 of one warp, row q * 32 +
   // lane's values in this lane, staged in S ([32][kStageLd] floats of shared
@@ -178,8 +175,7 @@ struct TcEpi {
 // The 128-row GEMM on tcgen05: a.xmap maps the chunked activations as
 // [K / KU * planes * 128 rows, KU + 32] 16-bit, 64 x 128 boxes, 128-byte
 // swizzle; grid <= the group count (every CTA owns whole 64-row groups).
-// With e.mc > 1 the grid is a multiple of e.mc, every CTA owns the same
-// number of groups (or slices), and a slice's CTA is p * groups + g.
+// With slices (e.parts > 1), slice p of group g is CTA p * groups + g.
 cudaError_t launch_gemv_tc(int wt, const GemvArgs& a, const TcEpi& e, int grid, cudaStream_t stream);
 // The per-head epilogue of a 128-row pass's raw q/k/v (mode 0), one CTA per (head, sequence).
 cudaError_t launch_heads_rows(const EpiHeads& e, int n_heads, int n_seq, cudaStream_t stream);

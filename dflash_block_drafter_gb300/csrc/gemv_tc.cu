@@ -35,13 +35,6 @@
 // groups (the projections back to the hidden size), one of `parts` slices of
 // a group's inputs; the slices' sums meet in global memory and the CTA that
 // arrives last adds them in slice order and applies the epilogue.
-//
-// Every unit of one input range multiplies the same activation chunk, so the
-// CTAs of a cluster of e.mc (different groups, the same input range) walk
-// their chunks in step and share them: each loads its share of a half
-// chunk's boxes with a multicast copy into every CTA of the cluster, and a
-// half stage is refilled once the MMAs of all of them have read it (their
-// commits arrive on every CTA's barrier).
 #include "gemv_launch.cuh"
 #include "kernels.h"
 
@@ -63,7 +56,7 @@ struct TcGeo {
   static constexpr int KBH = KU / 128;            // 64-input columns per half chunk and plane
   static constexpr int XHALF = (BOXES / 2) * XBOX;  // half a chunk: inputs [h * KU / 2, (h + 1) * KU / 2)
   static constexpr int BTILE = 64 * KU * 2;       // decoded unit, 16-bit
-  static constexpr int NB = 2;
+  static constexpr int NB = 2;  // decoded tiles, interleaved by 64-input column (btile_addr)
   static constexpr int BUDGET = 227 * 1024 - 2048;  // alignment slack and barriers
   // half-chunk stages and weight-unit stages: 4 and at least 3 where they fit, else 3
   static constexpr int XS = (BUDGET - 4 * XHALF - NB * BTILE) / F::UNIT >= 3 ? 4 : 3;
@@ -86,9 +79,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 // Row R (0..63), inputs k0 .. k0 + 7 (k0 % 8 == 0) of a decoded 64 x KU
-// K-major tile in 128-byte swizzle: 64-input columns of 64 rows x 128 bytes.
-__device__ __forceinline__ uint32_t btile_addr(uint32_t base, int R, int k0) {
-  return base + (k0 >> 6) * (64 * 128) + R * 128 + ((((k0 & 63) >> 3) ^ (R & 7)) << 4);
+// K-major tile in 128-byte swizzle, 64-input columns of 64 rows x 128 bytes.
+// The two tiles are interleaved column by column (tile t's column kb at
+// (2 kb + t) * 8 KB), so that a column of both is one 128-row operand.
+__device__ __forceinline__ uint32_t btile_addr(uint32_t tile_base, int R, int k0) {
+  return tile_base + (k0 >> 6) * (2 * 64 * 128) + R * 128 + ((((k0 & 63) >> 3) ^ (R & 7)) << 4);
 }
 
 template <int WT>
@@ -109,12 +104,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   uint8_t* btile = xring + XS * Geo::XHALF;       // [NB][64 x KU, 16-bit]
   uint8_t* wring = btile + NB * Geo::BTILE;       // [WS][weight unit]
   uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + WS * F::UNIT);
-  uint64_t* xempty = xfull + XS;      // the MMA commits of the cluster's CTAs
+  uint64_t* xempty = xfull + XS;      // MMA commit
   uint64_t* wfull = xempty + XS;
   uint64_t* wempty = wfull + WS;      // decoders (4)
-  uint64_t* bfull = wempty + WS;      // [NB] decoders (4)
-  uint64_t* bempty = bfull + NB;      // [NB] MMA commit
-  uint64_t* accf = bempty + NB;       // [kTcSlots] MMA commit at a group's end
+  uint64_t* bfull = wempty + WS;      // [NB][2 halves] decoders (4)
+  uint64_t* bempty = bfull + 2 * NB;  // [NB][2 halves] MMA commit
+  uint64_t* accf = bempty + 2 * NB;   // [kTcSlots] MMA commit at a group's end
   uint64_t* acce = accf + kTcSlots;   // [kTcSlots] epilogue warps (4)
   uint64_t* mdone = acce + kTcSlots;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
@@ -127,7 +122,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   // inputs: units j in [jb, je) of each of the CTA's groups
   int g0, g1, jb, je, slice = blockIdx.x;
   if (epi.parts > 1) {
-    // CTA p * groups + g: a cluster's CTAs share the slice p of the inputs
+    // CTA p * groups + g
     const int p = blockIdx.x / groups;
     g0 = blockIdx.x - p * groups;
     g1 = g0 + 1;
@@ -156,9 +151,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       j = jb + it - gi * nj;
     }
   };
-  const int mc = epi.mc > 1 ? epi.mc : 1;
-  const uint32_t rank = mc > 1 ? cluster_ctarank() : 0u;
-  const uint16_t mask = static_cast<uint16_t>((1u << mc) - 1u);
 #ifdef DFLASH_TRACE
   unsigned long long* tr = a.trace ? a.trace + static_cast<size_t>(blockIdx.x) * kTraceSlots : nullptr;
   if (tr && tid == 0) tr[0] = globaltimer_ns();
@@ -171,15 +163,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   if (tid == 0) {
     for (int s = 0; s < XS; ++s) {
       mbar_init(&xfull[s], 1);
-      mbar_init(&xempty[s], mc);
+      mbar_init(&xempty[s], 1);
     }
     for (int s = 0; s < WS; ++s) {
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 4);
     }
     for (int b = 0; b < NB; ++b) {
-      mbar_init(&bfull[b], 4);
-      mbar_init(&bempty[b], 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&bfull[2 * b + h], 4);
+        mbar_init(&bempty[2 * b + h], 1);
+      }
     }
     for (int k = 0; k < kTcSlots; ++k) {
       mbar_init(&accf[k], 1);
@@ -195,15 +189,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the peers' barriers are initialised once every CTA has signalled here
-  // (each role waits for that before its first access to a peer)
-  if (mc > 1) cluster_arrive_relaxed();
   const uint32_t tmem = *s_tmem;
   bool ok = true;
 
   if (warp == 0) {
     // ---------------------------------------------------- weight producer
-    if (mc > 1) cluster_wait();
     if (lane == 0 && n_units > 0) {
       const uint64_t pol = l2_policy_evict_first();
       int issued = 0;
@@ -227,15 +217,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
   } else if (warp == 10) {
     // ------------------------------------------------ activation producer
-    if (mc > 1) cluster_wait();
     if (lane == 0 && n_units > 0) {
       prefetch_tensormap(&a.xmap);
       pdl_wait();  // the activations come from the previous kernel
 #ifdef DFLASH_TRACE
       if (tr) tr[9] = globaltimer_ns();
 #endif
-      // half chunk q = 2 c + h of chunk c (inputs j's half h), stage q % XS;
-      // its boxes are shared out over the cluster, each multicast to all
+      // half chunk q = 2 c + h of chunk c (inputs j's half h), stage q % XS
       const int nq = 2 * n_chunks;
       int issued = 0;
       for (int q = 0; q < nq; ++q) {
@@ -254,97 +242,109 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
           for (int kh = 0; kh < Geo::KBH; ++kh) {
             const int i = p * Geo::KBH + kh;  // box of the half
             const int x = (h * Geo::KBH + kh) * 64, y = (j * PLANES + p) * 128;
-            if (mc == 1) tma_load_2d(dst + i * Geo::XBOX, &a.xmap, x, y, &xfull[s]);
-            else if ((q * 2 + i) % mc == static_cast<int>(rank))
-              tma_load_2d_mc(dst + i * Geo::XBOX, &a.xmap, x, y, &xfull[s], mask);
+            tma_load_2d(dst + i * Geo::XBOX, &a.xmap, x, y, &xfull[s]);
           }
         issued = q + 1;
       }
       for (int q = (issued > XS ? issued - XS : 0); q < issued; ++q)
         if (!mbar_wait(&xfull[q % XS], (q / XS) & 1)) ok = false;
-      // the cluster's last commits on this CTA's stages have arrived (no
-      // peer signals it after this)
-      if (mc > 1)
-        for (int s = 0; s < XS && s < issued; ++s)
-          if (!mbar_wait(&xempty[s], ((issued - 1 - s) / XS) & 1)) ok = false;
       if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
     } else if (lane == 0) {
       pdl_wait();
     }
   } else if (warp >= 1 && warp <= 4) {
     // ------------------------------------------------------------ decoders
-    if (mc > 1) cluster_wait();
     const int w = warp - 1;  // m-tile: weight rows 16 w .. 16 w + 15 of the group
     const int gr = lane >> 2, t4 = lane & 3;
     const uint32_t w_s = smem_u32(wring), bt_s = smem_u32(btile);
-    for (int it = 0; it < n_units && ok; ++it) {
-      const int s = it % WS, b = it % NB;
-      if (!TW(tw_a, mbar_wait(&wfull[s], (it / WS) & 1))) ok = false;
-      if (ok && it >= NB && !TW(tw_b, mbar_wait(&bempty[b], ((it / NB) - 1) & 1))) ok = false;
-      if (!ok) break;
-      const uint32_t ub = w_s + s * F::UNIT, bb = bt_s + b * Geo::BTILE;
-      auto put = [&](int bl, const BlockFrag& f) {
-        uint32_t d0 = 0, d8 = 0;
-        if constexpr (F::kF16) {
-          const __half2 h0 = __float2half2_rn(f.d_r), h8 = __float2half2_rn(f.d_r8);
-          d0 = *reinterpret_cast<const uint32_t*>(&h0);
-          d8 = *reinterpret_cast<const uint32_t*>(&h8);
-        }
-        const int k0 = bl * 32 + t4 * 8;
-        sts128(btile_addr(bb, w * 16 + gr, k0), scale_pair<WT>(f.a[0][0], d0), scale_pair<WT>(f.a[0][2], d0),
-               scale_pair<WT>(f.a[1][0], d0), scale_pair<WT>(f.a[1][2], d0));
-        sts128(btile_addr(bb, w * 16 + gr + 8, k0), scale_pair<WT>(f.a[0][1], d8), scale_pair<WT>(f.a[0][3], d8),
-               scale_pair<WT>(f.a[1][1], d8), scale_pair<WT>(f.a[1][3], d8));
-      };
+    // Units in steps (two units when the MMA pairs them, else one), each
+    // step's tiles written half by half (inputs [0, KU / 2) of every unit of
+    // the step, then the rest), so the MMA starts on a step's first half
+    // while its second is decoded.
+    const bool pair = jmajor && ng == 2;
+    const int per = pair ? 2 : 1;
+    for (int it0 = 0; it0 < n_units && ok; it0 += per) {
 #pragma unroll
-      for (int bl = 0; bl < F::CB; bl += (WT == WT_Q4_0 || WT == WT_Q5_0) ? 2 : 1) {
-        if constexpr (WT == WT_Q4_0 || WT == WT_Q5_0) {
-          BlockFrag f0, f1;
-          decode_pair<WT, F::kF16>(ub, w, lane, bl >> 1, f0, f1);
-          put(bl, f0);
-          put(bl + 1, f1);
-        } else {
-          put(bl, decode_block<WT, F::kF16>(ub, w, lane, bl));
+      for (int h = 0; h < 2; ++h) {
+        for (int t = 0; t < per && ok; ++t) {
+          const int it = it0 + t;
+          const int s = it % WS, b = it % NB;
+          if (h == 0 && !TW(tw_a, mbar_wait(&wfull[s], (it / WS) & 1))) ok = false;
+          if (ok && it >= NB && !TW(tw_b, mbar_wait(&bempty[2 * b + h], ((it / NB) - 1) & 1))) ok = false;
+          if (!ok) break;
+          const uint32_t ub = w_s + s * F::UNIT, bb = bt_s + b * (64 * 128);
+          auto put = [&](int bl, const BlockFrag& f) {
+            uint32_t d0 = 0, d8 = 0;
+            if constexpr (F::kF16) {
+              const __half2 h0 = __float2half2_rn(f.d_r), h8 = __float2half2_rn(f.d_r8);
+              d0 = *reinterpret_cast<const uint32_t*>(&h0);
+              d8 = *reinterpret_cast<const uint32_t*>(&h8);
+            }
+            const int k0 = bl * 32 + t4 * 8;
+            sts128(btile_addr(bb, w * 16 + gr, k0), scale_pair<WT>(f.a[0][0], d0), scale_pair<WT>(f.a[0][2], d0),
+                   scale_pair<WT>(f.a[1][0], d0), scale_pair<WT>(f.a[1][2], d0));
+            sts128(btile_addr(bb, w * 16 + gr + 8, k0), scale_pair<WT>(f.a[0][1], d8),
+                   scale_pair<WT>(f.a[0][3], d8), scale_pair<WT>(f.a[1][1], d8), scale_pair<WT>(f.a[1][3], d8));
+          };
+          constexpr int HB = F::CB / 2;  // 32-input blocks per half
+#pragma unroll
+          for (int bl = h * HB; bl < (h + 1) * HB; bl += (WT == WT_Q4_0 || WT == WT_Q5_0) ? 2 : 1) {
+            if constexpr (WT == WT_Q4_0 || WT == WT_Q5_0) {
+              BlockFrag f0, f1;
+              decode_pair<WT, F::kF16>(ub, w, lane, bl >> 1, f0, f1);
+              put(bl, f0);
+              put(bl + 1, f1);
+            } else {
+              put(bl, decode_block<WT, F::kF16>(ub, w, lane, bl));
+            }
+          }
+          // generic-proxy writes of the half tile, then its hand-off to the
+          // tensor cores (and, after the second half, the unit's codes are read)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bfull[2 * b + h]);
+            if (h == 1) mbar_arrive(&wempty[s]);
+          }
         }
-      }
-      // the unit's codes have been read; generic-proxy writes of the tile,
-      // then its hand-off to the tensor cores
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&wempty[s]);
-        mbar_arrive(&bfull[b]);
       }
     }
     if (!ok && lane == 0) set_status(a.status, DFLASH_DEV_TIMEOUT);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (mc > 1) cluster_wait();
     if (lane == 0 && n_units > 0) {
-      constexpr uint32_t idesc = idesc_16(128, 64, !F::kF16);
+      // Two groups taken input-major: their units of one chunk sit in the
+      // two decoded tiles, which make one 128-row operand -- one MMA of
+      // N 128 into both groups' accumulators (adjacent TMEM columns).
+      const bool pair = jmajor && ng == 2;
+      const uint32_t idesc = pair ? idesc_16(128, 128, !F::kF16) : idesc_16(128, 64, !F::kF16);
       const uint32_t x_s = smem_u32(xring), bt_s = smem_u32(btile);
-      for (int it = 0; it < n_units && ok; ++it) {
+      const int n_steps = pair ? n_units / 2 : n_units;
+      for (int stp = 0; stp < n_steps && ok; ++stp) {
+        const int it = pair ? 2 * stp : stp;
         const int b = it % NB;
         int gi, j;
         unit_of(it, gi, j);
         const int slot = gi % kTcSlots;
         const int c = jmajor ? it / ng : it;             // the unit's chunk
         const bool new_chunk = !jmajor || gi == 0;
-        const bool end_chunk = !jmajor || gi == ng - 1;  // the chunk's last unit
+        const bool end_chunk = pair || !jmajor || gi == ng - 1;  // the chunk's last unit
         const bool first = j == jb, last = j == je - 1;  // the group's first / last unit here
         if (first && !jmajor && gi >= kTcSlots && !mbar_wait(&acce[slot], ((gi / kTcSlots) - 1) & 1)) {
           ok = false;
           break;
         }
-        if (!TW(tw_b, mbar_wait(&bfull[b], (it / NB) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t bs = bt_s + b * Geo::BTILE;
+        const uint32_t bs = bt_s + b * (64 * 128);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int q = 2 * c + h, s = q % XS;
+          // this half of the step's decoded tiles
+          if (!TW(tw_b, mbar_wait(&bfull[2 * b + h], (it / NB) & 1)) ||
+              (pair && !TW(tw_b, mbar_wait(&bfull[2 * (b + 1) + h], ((it + 1) / NB) & 1)))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           if (new_chunk) {
             if (!TW(tw_a, mbar_wait(&xfull[s], (q / XS) & 1))) {
               ok = false;
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 #pragma unroll
           for (int kq = 0; kq < KU / 32; ++kq) {  // the half's k-steps of 16 inputs
             const int kk = h * (KU / 32) + kq;
-            const uint64_t db = umma_desc_sw128(bs + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = umma_desc_sw128(bs + (kk >> 2) * (NB * 64 * 128) + (kk & 3) * 32, 16, 1024);
 #pragma unroll
             for (int p = 0; p < PLANES; ++p) {
               const uint64_t da =
@@ -364,15 +364,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
               umma_f16(tmem + slot * 64, da, db, idesc, (!first || kk || p) ? 1u : 0u);
             }
           }
-          // the half chunk may be refilled once its last unit's MMAs are done
-          if (end_chunk) {
-            if (mc > 1) umma_commit_mc(&xempty[s], mask);
-            else umma_commit(&xempty[s]);
-          }
+          // the half chunk may be refilled once its last unit's MMAs are done,
+          // the half tiles once these are
+          if (end_chunk) umma_commit(&xempty[s]);
+          umma_commit(&bempty[2 * b + h]);
+          if (pair) umma_commit(&bempty[2 * (b + 1) + h]);
         }
         if (!ok) break;
-        umma_commit(&bempty[b]);
-        if (last) umma_commit(&accf[slot]);
+        if (last) {
+          umma_commit(&accf[slot]);
+          if (pair) umma_commit(&accf[slot + 1]);
+        }
       }
 #ifdef DFLASH_TRACE
       if (tr) tr[10] = globaltimer_ns();
@@ -384,7 +386,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    if (mc > 1) cluster_wait();
     pdl_launch_dependents();
     const int q = warp & 3;               // TMEM lane quarter
     const int n = q * 32 + lane;          // activation row = TMEM lane
@@ -486,8 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     if (tr && warp == 6 && lane == 0) tr[14] = globaltimer_ns();
 #endif
   }
-  // release the tensor memory once every tcgen05 operation of the CTA is done;
-  // no CTA leaves while a peer may still write to its shared memory
+  // release the tensor memory once every tcgen05 operation of the CTA is done
 #ifdef DFLASH_TRACE
   if (tr) {
     if (warp == 0 && lane == 0) { tr[1] = tw_a; }
@@ -504,7 +504,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
 #ifdef DFLASH_TRACE
   if (tr && tid == 0) tr[15] = globaltimer_ns();
 #endif
-  if (mc > 1) cluster_sync_all();
 #ifdef DFLASH_TRACE
   if (tr && threadIdx.x == 0) tr[7] = globaltimer_ns();
 #endif
@@ -682,8 +681,6 @@ cudaError_t launch_heads_rows(const EpiHeads& e, int n_heads, int n_seq, cudaStr
 template <int WT>
 static cudaError_t launch_tc(const GemvArgs& a, const TcEpi& e, int grid, cudaStream_t stream) {
   using Geo = TcGeo<WT>;
-  // a cluster's CTAs share each chunk's boxes: mc must divide the box count and the grid
-  if (e.mc > 1 && (e.mc > 4 || Geo::BOXES % e.mc != 0 || grid % e.mc != 0)) return cudaErrorInvalidValue;
   if (e.parts > kMaxParts) return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(gemv_tc_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo::SMEM);
   if (err != cudaSuccess) return err;
@@ -692,15 +689,11 @@ static cudaError_t launch_tc(const GemvArgs& a, const TcEpi& e, int grid, cudaSt
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = Geo::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = e.mc > 1 ? e.mc : 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = e.mc > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<WT>, a, e);
 }
 
