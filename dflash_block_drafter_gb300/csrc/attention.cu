@@ -670,9 +670,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   }
 }
 
-// Log-sum-exp merge of the chunk partials of one (slot, q head) -- the slot's
-// chunks of the pass's chunk plan: all 8 block rows, a 32-column slice of
-// the head (blockIdx.y).  Chunk c of row m carries
+// Log-sum-exp merge of the chunk partials of a one-sequence pass, per q head:
+// all 8 block rows, a 32-column slice of the head (blockIdx.y).  Chunk c of
+// row m carries
 // O_c / l_c (FP16) and (m_c, l_c); the row's output is
 //   sum_c w_c O_c / l_c,   w_c = l_c 2^(m_c - mx) / sum_c' l_c' 2^(m_c' - mx).
 // Lane = (row i = lane / 4, 8 columns from (lane % 4) * 8); warp w takes
@@ -702,28 +702,19 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   __shared__ float smx[8][32];
   __shared__ float ssum[8][32];
   __shared__ float4 sacc[8][32][2];
-  const int hq = blockIdx.x, cb = blockIdx.y, s = blockIdx.z;
+  const int hq = blockIdx.x, cb = blockIdx.y, s = 0;
   const int g = hq / a.gq, hl = hq - g * a.gq;
   const int M = a.gq * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(0);
-  // this sequence's chunks: one sequence's plan is formed here, while the
-  // attention kernel finishes (it depends only on the pass's inputs); a
-  // several-sequence plan is the one the attention kernel published
-  int n_ch = 0, start = 0;
-  if (a.n_seq == 1) {
-    const int tiles = seq_keys(a.anchor_pos, a.block_len, 0, a.window, a.cap).tiles;
-    const int t = max(1, (tiles + a.Q - 1) / a.Q);
-    n_ch = max(1, (tiles + t - 1) / t);
-  }
+  // the sequence's chunks, as the attention kernel's plan gives them, formed
+  // here while that kernel finishes (it depends only on the pass's inputs)
+  const int tiles = seq_keys(a.anchor_pos, a.block_len, 0, a.window, a.cap).tiles;
+  const int t_per = max(1, (tiles + a.Q - 1) / a.Q);
+  const int n_ch = max(1, (tiles + t_per - 1) / t_per), start = 0;
   pdl_wait();
   if (threadIdx.x == 0) DFLASH_ATTN_STAMP(1);
   pdl_launch_dependents();
-  if (a.n_seq > 1) {
-    const int pl = __ldcg(a.plan + s);
-    start = pl & 0xffff;
-    n_ch = pl >> 16;
-  }
   const size_t base = (static_cast<size_t>(g) * a.Q + start) * M;
   const int i = lane >> 2, mrow = hl * 8 + i, col = cb * 32 + (lane & 3) * 8;
   const __half* pr = a.part + (base + mrow) * a.d + col;
@@ -821,6 +812,95 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + ob + lo_off) = lo;
     }
     if (threadIdx.x == 0) DFLASH_ATTN_STAMP(7);
+  }
+}
+
+// The same merge for a pass of several sequences, whose sequences own few
+// chunks each: one thread per (sequence, q head, block row, 8 columns) folds
+// all of its sequence's chunks, loading up to kMultiU of them at once; a
+// warp covers one row of a head (256 columns: 32 consecutive 16-byte pieces).
+constexpr int kMultiU = 8;
+
+__global__ void __launch_bounds__(256) attn_combine_multi_kernel(const __grid_constant__ CombineArgs a) {
+  const int s = blockIdx.y;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n8 = a.d / 8;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (t >= a.n_q * 8 * n8) return;
+  const int c8 = t % n8, i = (t / n8) % 8, hq = t / (n8 * 8);
+  const int g = hq / a.gq, hl = hq - g * a.gq;
+  const int M = a.gq * 8;
+  const int pl = __ldcg(a.plan + s);
+  const int start = pl & 0xffff, n_ch = pl >> 16;
+  const size_t base = (static_cast<size_t>(g) * a.Q + start) * M;
+  const int mrow = hl * 8 + i, col = c8 * 8;
+  const __half* pr = a.part + (base + mrow) * a.d + col;
+  const float2* pml = a.ml + base + mrow;
+  const size_t cstride = static_cast<size_t>(M) * a.d;
+  float mw = -INFINITY, lw = 0.f, acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int c0 = 0; c0 < n_ch; c0 += kMultiU) {
+    uint4 v[kMultiU];
+    float2 ml[kMultiU];
+#pragma unroll
+    for (int u = 0; u < kMultiU; ++u) {
+      const int c = c0 + u;
+      if (c < n_ch) {
+        ml[u] = __ldcg(pml + static_cast<size_t>(c) * M);
+        v[u] = __ldcg(reinterpret_cast<const uint4*>(pr + c * cstride));
+      } else {
+        ml[u] = make_float2(-INFINITY, 0.f);
+        v[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float bm = mw;
+#pragma unroll
+    for (int u = 0; u < kMultiU; ++u)
+      if (ml[u].y > 0.f) bm = fmaxf(bm, ml[u].x);
+    const float sc = mw == -INFINITY ? 0.f : ex2_approx(mw - bm);
+    lw *= sc;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= sc;
+    mw = bm;
+#pragma unroll
+    for (int u = 0; u < kMultiU; ++u) {
+      if (ml[u].y > 0.f) {  // chunks without keys hold no partial
+        const float w = ml[u].y * ex2_approx(ml[u].x - bm);
+        lw += w;
+        const __half2* h = reinterpret_cast<const __half2*>(&v[u]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h[e]);
+          acc[2 * e] = fmaf(f.x, w, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(f.y, w, acc[2 * e + 1]);
+        }
+      }
+    }
+  }
+  if (!(lw > 0.f)) {
+    set_status(a.status, DFLASH_DEV_NONFINITE);
+    lw = 1.f;
+  }
+  const float inv = 1.f / lw;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] *= inv;
+  const int P = a.out_f16 ? 1 : 2;
+  const size_t ob = xchunk_index(hq * a.d + col, s * 8 + i, 0, a.out_rows, a.out_ku, P);
+  if (a.out_f16) {
+    *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + ob) =
+        make_uint4(pack_f16x2(acc[0], acc[1]), pack_f16x2(acc[2], acc[3]), pack_f16x2(acc[4], acc[5]),
+                   pack_f16x2(acc[6], acc[7]));
+  } else {
+    uint4 hi, lo;
+    split_bf16x2(acc[0], acc[1], hi.x, lo.x);
+    split_bf16x2(acc[2], acc[3], hi.y, lo.y);
+    split_bf16x2(acc[4], acc[5], hi.z, lo.z);
+    split_bf16x2(acc[6], acc[7], hi.w, lo.w);
+    const size_t lo_off = static_cast<size_t>(a.out_rows) * (a.out_ku + 32);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + ob) = hi;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + ob + lo_off) = lo;
   }
 }
 
@@ -926,9 +1006,12 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cb.plan = st.attn_plan;
   cb.status = status;
   // (diagnostic builds: a grid larger than a trace slot records nothing)
-  cb.trace = c.n_q_heads * (c.head_dim / 32) * n_seq <= st.max_grid ? trace_slot(st) : nullptr;
+  cb.trace = n_seq == 1 && c.n_q_heads * (c.head_dim / 32) <= st.max_grid ? trace_slot(st) : nullptr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(c.n_q_heads, c.head_dim / 32, n_seq);
+  // one sequence: many chunks, spread over the warps of a CTA per (head, 32
+  // columns); several: a thread per (sequence, head, row, 8 columns)
+  const int per_seq = c.n_q_heads * 8 * (c.head_dim / 8);
+  cfg.gridDim = n_seq == 1 ? dim3(c.n_q_heads, c.head_dim / 32, 1) : dim3((per_seq + 255) / 256, n_seq, 1);
   cfg.blockDim = dim3(256);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -936,7 +1019,8 @@ cudaError_t launch_attention(const Model& m, State& st, int layer, int n_seq, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, cb);
+  return n_seq == 1 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel, cb)
+                    : cudaLaunchKernelEx(&cfg, attn_combine_multi_kernel, cb);
 }
 
 }  // namespace dflash

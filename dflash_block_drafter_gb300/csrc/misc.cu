@@ -260,44 +260,65 @@ cudaError_t launch_embed(const EmbedArgs& a, int nt, cudaStream_t st) {
 // ---------------------------------------------------------- row RMSNorm
 // out[r] = act(x[r] / sqrt(mean(x[r]^2) + eps) * w) for the streamed-X
 // GEMVs, and optionally the same rows in fp32 (final hidden state output).
+// One CTA per row: the row is read once, as 16-byte loads all issued
+// together (up to kNormV per thread), and normalised from registers.
 
-__global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const __grid_constant__ NormArgs a) {
+constexpr int kNormThreads = 128, kNormV = 16;  // rows of up to 8192 floats
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(const __grid_constant__ NormArgs a) {
   const int r = blockIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  __shared__ float red[8];
-  const float* xr = a.x + static_cast<size_t>(r) * a.H;
+  __shared__ float red[kNormThreads / 32];
+  const int H4 = a.H >> 2;
+  const bool valid = r < a.rows_valid;
+  const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(r) * a.H);
+  float4 v[kNormV];
+#pragma unroll
+  for (int i = 0; i < kNormV; ++i) {
+    const int k4 = static_cast<int>(threadIdx.x) + i * kNormThreads;
+    v[i] = (valid && k4 < H4) ? __ldcg(xr + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float ss = 0.f;
-  if (r < a.rows_valid)
-    for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
-      const float v = __ldcg(xr + k);
-      ss += v * v;
-    }
+#pragma unroll
+  for (int i = 0; i < kNormV; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
-  for (int i = 0; i < (blockDim.x >> 5); ++i) tot += red[i];
-  const float rs = r < a.rows_valid ? rsqrtf(tot / a.H + a.eps) : 0.f;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
-    const float v = r < a.rows_valid ? __ldcg(xr + k) * rs * a.w[k] : 0.f;
-    const int R = gridDim.x;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += red[i];
+  const float rs = valid ? rsqrtf(tot / a.H + a.eps) : 0.f;
+  const int R = gridDim.x;
+#pragma unroll
+  for (int i = 0; i < kNormV; ++i) {
+    const int k4 = static_cast<int>(threadIdx.x) + i * kNormThreads;
+    if (k4 >= H4) break;
+    const int k = 4 * k4;
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w) + k4);
+    const float y0 = v[i].x * rs * w4.x, y1 = v[i].y * rs * w4.y, y2 = v[i].z * rs * w4.z, y3 = v[i].w * rs * w4.w;
+    // four consecutive inputs of one chunk row (KU is a multiple of 4)
     if (a.out_f16) {
-      static_cast<__half*>(a.out)[xchunk_index(k, r, 0, R, a.ku, 1)] = __float2half_rn(v);
+      *reinterpret_cast<uint2*>(static_cast<__half*>(a.out) + xchunk_index(k, r, 0, R, a.ku, 1)) =
+          make_uint2(pack_f16x2(y0, y1), pack_f16x2(y2, y3));
     } else {
+      uint32_t h01, l01, h23, l23;
+      split_bf16x2(y0, y1, h01, l01);
+      split_bf16x2(y2, y3, h23, l23);
       __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out);
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      o[xchunk_index(k, r, 0, R, a.ku, 2)] = hi;
-      o[xchunk_index(k, r, 1, R, a.ku, 2)] = __float2bfloat16_rn(v - __bfloat162float(hi));
+      *reinterpret_cast<uint2*>(o + xchunk_index(k, r, 0, R, a.ku, 2)) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(o + xchunk_index(k, r, 1, R, a.ku, 2)) = make_uint2(l01, l23);
     }
-    if (a.f32_out && r < a.rows_f32) a.f32_out[static_cast<size_t>(r) * a.H + k] = v;
+    if (a.f32_out && r < a.rows_f32)
+      reinterpret_cast<float4*>(a.f32_out + static_cast<size_t>(r) * a.H)[k4] = make_float4(y0, y1, y2, y3);
   }
 }
 
 cudaError_t launch_rmsnorm_rows(const NormArgs& a, int rows, cudaStream_t st) {
+  if (a.H % 4 != 0 || a.H > 4 * kNormThreads * kNormV || a.ku % 4 != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kNormThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
