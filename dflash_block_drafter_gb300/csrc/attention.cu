@@ -247,14 +247,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint64_t* qfull = bars + 0;   // [D / 64]: one per 64-column box of Q
   uint64_t* kfull = bars + 4;
   uint64_t* kfree = bars + 5;
-  uint64_t* vfull = bars + 6;
-  uint64_t* vfree = bars + 7;
-  uint64_t* sfull = bars + 8;   // [2]
-  uint64_t* sfree = bars + 10;  // [2]
-  uint64_t* pfull = bars + 12;
-  uint64_t* pfree = bars + 13;
-  uint64_t* mdone = bars + 14;  // every MMA of the CTA has completed
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* vfull = bars + 6;   // [2]: one per 64-key V tile
+  uint64_t* vfree = bars + 8;   // [2]
+  uint64_t* sfull = bars + 10;  // [2]
+  uint64_t* sfree = bars + 12;  // [2]
+  uint64_t* pfull = bars + 14;
+  uint64_t* pfree = bars + 15;
+  uint64_t* mdone = bars + 16;  // every MMA of the CTA has completed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 17);
   int* s_plan = reinterpret_cast<int*>(s_tmem + 1);  // [4]: sequence, its chunk, super-tiles per chunk, idle
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -308,8 +308,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int b = 0; b < Geo::BOXES; ++b) mbar_init(&qfull[b], 1);
     mbar_init(kfull, 1);
     mbar_init(kfree, 1);
-    mbar_init(vfull, 1);
-    mbar_init(vfree, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&vfull[t], 1);
+      mbar_init(&vfree[t], 1);
+    }
     mbar_init(&sfull[0], 1);
     mbar_init(&sfull[1], 1);
     mbar_init(&sfree[0], kTcSoftWarps);
@@ -359,12 +361,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         bulk_prefetch_l2_plain(a.kbase_ptr + static_cast<size_t>(row) * D, bytes);
         bulk_prefetch_l2_plain(a.vbase_ptr + static_cast<size_t>(row) * D, bytes);
       };
-      auto issue_v = [&](int j) {
+      // V tile t of super-tile j: its buffer is refilled as soon as the PV
+      // MMAs of the previous super-tile's tile t are done
+      auto issue_v_tile = [&](int j, int t) {
         const int y = tile_row(j);
-        mbar_arrive_expect_tx(vfull, 2 * Geo::TILE_BYTES);
-        for (int t = 0; t < 2; ++t)
-          for (int b = 0; b < Geo::BOXES; ++b)
-            tma_load_2d(sv + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.vmap, b * 64, y + t * kTcKT, vfull);
+        mbar_arrive_expect_tx(&vfull[t], Geo::TILE_BYTES);
+        for (int b = 0; b < Geo::BOXES; ++b)
+          tma_load_2d(sv + t * Geo::TILE_BYTES + b * kTcKT * 128, &a.vmap, b * 64, y + t * kTcKT, &vfull[t]);
+      };
+      auto issue_v = [&](int j) {
+        issue_v_tile(j, 0);
+        issue_v_tile(j, 1);
       };
       // A first super-tile wholly before the block's positions does not
       // depend on the previous kernel (which writes the block cells; in a
@@ -391,8 +398,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (!mbar_wait(kfree, (j - 1) & 1)) { ok = false; break; }
         issue_k(j);
         ++nk;
-        if (!mbar_wait(vfree, (j - 1) & 1)) { ok = false; break; }
-        issue_v(j);
+        if (!mbar_wait(&vfree[0], (j - 1) & 1)) { ok = false; break; }
+        issue_v_tile(j, 0);
+        if (!mbar_wait(&vfree[1], (j - 1) & 1)) { ok = false; break; }
+        issue_v_tile(j, 1);
         ++nv;
       }
       // Only the last K and V copies can still be in flight (each earlier one
@@ -401,7 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       for (int b = 0; b < Geo::BOXES; ++b)
         if (!mbar_wait(&qfull[b], 0)) ok = false;
       if (!mbar_wait(kfull, (nk - 1) & 1)) ok = false;
-      if (!mbar_wait(vfull, (nv - 1) & 1)) ok = false;
+      for (int t = 0; t < 2; ++t)
+        if (!mbar_wait(&vfull[t], (nv - 1) & 1)) ok = false;
       if (!ok) set_status(a.status, DFLASH_DEV_TIMEOUT);
     }
   } else if (warp == 1) {
@@ -445,29 +455,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       DFLASH_ATTN_STAMP(11);
       for (int j = 0; j < nst && ok; ++j) {
         bool qk_next = j + 1 < nst;
-        {
+        // wait for `ready`, issuing QK^T of super-tile j + 1 meanwhile if its
+        // K tile and S buffer come first
+        auto spin_until = [&](auto ready) -> bool {
           const unsigned long long t0 = globaltimer_ns();
           for (int spin = 0;; ++spin) {
             if (qk_next && mbar_test(kfull, (j + 1) & 1) &&
                 (j + 1 < 2 || mbar_test(&sfree[(j + 1) & 1], (((j + 1) >> 1) - 1) & 1))) {
-              if (!issue_qk(j + 1)) { ok = false; break; }
+              if (!issue_qk(j + 1)) return false;
               qk_next = false;
             }
-            if (mbar_test(pfull, j & 1) && mbar_test(vfull, j & 1)) break;
-            if ((spin & 63) == 63 && globaltimer_ns() - t0 > kWaitTimeoutNs) { ok = false; break; }
+            if (ready()) return true;
+            if ((spin & 63) == 63 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
           }
-          if (!ok) break;
-        }
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
+        };
+        // PV tile by tile: each V tile's buffer is released once its MMAs are done
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!spin_until([&]() { return (t > 0 || mbar_test(pfull, j & 1)) && mbar_test(&vfull[t], j & 1); })) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTcKT / 16; ++kk) {
             const uint64_t da = umma_desc_sw128(p_s + t * 16384 + kk * 32, 16, 1024);
             const uint64_t db = umma_desc_sw128(v_s + t * Geo::TILE_BYTES + kk * 2048, kTcKT * 128, 1024);
             umma_f16(tmem + 2 * kTcKS, da, db, idesc_pv, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
           }
-        umma_commit(pfree);
-        umma_commit(vfree);
+          if (t == 1) umma_commit(pfree);
+          umma_commit(&vfree[t]);
+        }
+        if (!ok) break;
         if (qk_next && !issue_qk(j + 1)) { ok = false; break; }
       }
       // tensor memory may only be freed once every issued MMA has finished
