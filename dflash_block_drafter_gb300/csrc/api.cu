@@ -215,6 +215,19 @@ GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* statu
   return a;
 }
 
+// The GEMV asks L2 for `units` units of the next projection's weights once it
+// has issued its last unit (the next kernel's stream then starts from L2).
+constexpr int kPrefetchUnits = 8;
+void set_prefetch(GemvArgs& a, const PackedMatrix& next, int units) {
+  const int upg = next.k / (32 * cb_of(next.wtype));
+  const int U = (next.n / 64) * upg;
+  if (U <= 0) return;
+  a.pf_W = next.data;
+  a.pf_U = U;
+  a.pf_unit = static_cast<int>(next.bytes / static_cast<size_t>(U));
+  a.pf_units = units;
+}
+
 // Grid of a GEMV: one CTA per SM at most, with the CTAs' unit ranges aligned
 // to the 64-row groups where the counts allow, so that no CTA meets a group
 // end in the middle of its range (a split group's fix-up, or a whole head's
@@ -819,6 +832,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       GemvArgs a = base_args(m->qkv[l], *s, CNT_QKV, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
+      set_prefetch(a, m->o[l], kPrefetchUnits);
       if (packed) {
         set_packed(a);
       } else {
@@ -895,6 +909,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->o[l], *s, CNT_O, status);
       a.n_valid_rows = R;
+      set_prefetch(a, m->gu[l], kPrefetchUnits);
       a.X = s->attn_out;
       a.ldx = nq * d;
       EpiResid e{s->x, H,
@@ -916,6 +931,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
       a.n_valid_rows = R;
+      set_prefetch(a, m->down[l], kPrefetchUnits);
       a.eps = c.norm_eps;
       if (packed) {
         set_packed(a);
@@ -947,6 +963,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->down[l], *s, CNT_DOWN, status);
       a.n_valid_rows = R;
+      if (l + 1 < L) set_prefetch(a, m->qkv[l + 1], kPrefetchUnits);
       a.X = s->hbuf;
       a.ldx = I;
       EpiResid e{s->x, H,

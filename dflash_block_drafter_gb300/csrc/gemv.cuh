@@ -42,6 +42,12 @@ struct GemvArgs {
   const float* ssq;
   int n_ssq;
   int rs_early;                  // X_NORM: 1 / RMS needed before the first group (final hidden rows)
+  // The next projection's weights (constant): once this CTA has issued its
+  // last unit, it asks L2 for pf_units units of them, from unit
+  // blockIdx * pf_U / gridDim (the start of the matching share of that
+  // matrix), so the next kernel's stream starts from L2 (pf_units 0: none)
+  const uint8_t* pf_W;
+  int pf_unit, pf_U, pf_units;
   // Extra groups (X_NORM, groups aligned to CTAs): the last vgroups of the
   // U / UPG groups re-read weight groups [vwg0, vwg0 + vgroups) with their
   // own activations X2, row sums of squares ssq2 and n_valid2 valid rows (an
@@ -264,6 +270,12 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
         issue_w(it, u_begin + it);
         if constexpr (kStream) issue_x(it, u_begin + it);
         issued = it + 1;
+      }
+      if (a.pf_units > 0 && issued == n_units) {
+        const long long u0 = static_cast<long long>(blockIdx.x) * a.pf_U / G;
+        const long long u1 = u0 + a.pf_units < a.pf_U ? u0 + a.pf_units : a.pf_U;
+        if (u1 > u0)
+          bulk_prefetch_l2_plain(a.pf_W + u0 * a.pf_unit, static_cast<uint32_t>((u1 - u0) * a.pf_unit));
       }
       // Every issued copy must land before the CTA may exit.
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
