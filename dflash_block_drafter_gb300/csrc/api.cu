@@ -215,17 +215,23 @@ GemvArgs base_args(const PackedMatrix& pm, State& st, int region, int32_t* statu
   return a;
 }
 
-// The GEMV asks L2 for `units` units of the next projection's weights once it
-// has issued its last unit (the next kernel's stream then starts from L2).
+// The GEMV asks L2 for the first kPrefetchUnits units of each share of the
+// next projection's weights once it has issued its last unit (the next
+// kernel's stream then starts from L2); the shares follow the next GEMV's grid.
 constexpr int kPrefetchUnits = 8;
-void set_prefetch(GemvArgs& a, const PackedMatrix& next, int units) {
-  const int upg = next.k / (32 * cb_of(next.wtype));
-  const int U = (next.n / 64) * upg;
-  if (U <= 0) return;
+int grid_for(const Model& m, const GemvArgs& a);
+void set_prefetch(const Model& m, GemvArgs& a, const PackedMatrix& next) {
+  GemvArgs t;
+  std::memset(&t, 0, sizeof(t));
+  t.UPG = next.k / (32 * cb_of(next.wtype));
+  t.U = (next.n / 64) * t.UPG;
+  if (t.U <= 0) return;
   a.pf_W = next.data;
-  a.pf_U = U;
-  a.pf_unit = static_cast<int>(next.bytes / static_cast<size_t>(U));
-  a.pf_units = units;
+  a.pf_total = next.bytes;
+  a.pf_U = t.U;
+  a.pf_unit = static_cast<int>(next.bytes / static_cast<size_t>(t.U));
+  a.pf_G = grid_for(m, t);
+  a.pf_bytes = kPrefetchUnits * a.pf_unit;
 }
 
 // Grid of a GEMV: one CTA per SM at most, with the CTAs' unit ranges aligned
@@ -712,6 +718,8 @@ int dflash_fuse_context(const dflash_model* m, dflash_state* s, int32_t slot, co
     {
       GemvArgs a = base_args(m->fc, *s, CNT_FC, status);
       a.n_valid_rows = rows;
+      // a deferring fusion is followed by a draft pass, which starts with layer 0's QKV
+      if (defer) set_prefetch(*m, a, m->qkv[0]);
       a.X = taps + static_cast<size_t>(base) * tw;
       a.ldx = tw;
       if (ku_of(wt) + 32 <= 256)
@@ -832,7 +840,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
       GemvArgs a = base_args(m->qkv[l], *s, CNT_QKV, status);
       a.n_valid_rows = R;
       a.eps = c.norm_eps;
-      set_prefetch(a, m->o[l], kPrefetchUnits);
+      set_prefetch(*m, a, m->o[l]);
       if (packed) {
         set_packed(a);
       } else {
@@ -909,7 +917,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->o[l], *s, CNT_O, status);
       a.n_valid_rows = R;
-      set_prefetch(a, m->gu[l], kPrefetchUnits);
+      set_prefetch(*m, a, m->gu[l]);
       a.X = s->attn_out;
       a.ldx = nq * d;
       EpiResid e{s->x, H,
@@ -931,7 +939,7 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->gu[l], *s, CNT_GU, status);
       a.n_valid_rows = R;
-      set_prefetch(a, m->down[l], kPrefetchUnits);
+      set_prefetch(*m, a, m->down[l]);
       a.eps = c.norm_eps;
       if (packed) {
         set_packed(a);
@@ -963,7 +971,19 @@ int dflash_draft_block(const dflash_model* m, dflash_state* s, int32_t n_seq, co
     {
       GemvArgs a = base_args(m->down[l], *s, CNT_DOWN, status);
       a.n_valid_rows = R;
-      if (l + 1 < L) set_prefetch(a, m->qkv[l + 1], kPrefetchUnits);
+      if (l + 1 < L) {
+        set_prefetch(*m, a, m->qkv[l + 1]);
+      } else if (nt == 1) {
+        // the LM head of a one-sequence pass: 128-row chunks, CTA c' of
+        // min(chunks, SMs) starting at chunk c' * chunks / grid
+        const int nv = (c.vocab + 127) / 128;
+        a.pf_W = reinterpret_cast<const uint8_t*>(m->head);
+        a.pf_total = static_cast<size_t>(c.vocab) * H * 2;
+        a.pf_U = nv;
+        a.pf_unit = 128 * H * 2;
+        a.pf_G = nv < m->sm_count ? nv : m->sm_count;
+        a.pf_bytes = 128 * 1024;
+      }
       a.X = s->hbuf;
       a.ldx = I;
       EpiResid e{s->x, H,

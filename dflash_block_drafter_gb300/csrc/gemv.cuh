@@ -42,12 +42,14 @@ struct GemvArgs {
   const float* ssq;
   int n_ssq;
   int rs_early;                  // X_NORM: 1 / RMS needed before the first group (final hidden rows)
-  // The next projection's weights (constant): once this CTA has issued its
-  // last unit, it asks L2 for pf_units units of them, from unit
-  // blockIdx * pf_U / gridDim (the start of the matching share of that
-  // matrix), so the next kernel's stream starts from L2 (pf_units 0: none)
+  // The next kernel's weights (constant, pf_total bytes in pf_U units of
+  // pf_unit bytes, its CTA c' of pf_G starting at unit c' * pf_U / pf_G):
+  // once this CTA has issued its last unit, it asks L2 for the first
+  // pf_bytes of the shares of next CTAs [c * pf_G / G, (c + 1) * pf_G / G),
+  // so that the next kernel's stream starts from L2 (pf_bytes 0: none)
   const uint8_t* pf_W;
-  int pf_unit, pf_U, pf_units;
+  size_t pf_total;
+  int pf_unit, pf_U, pf_G, pf_bytes;
   // Extra groups (X_NORM, groups aligned to CTAs): the last vgroups of the
   // U / UPG groups re-read weight groups [vwg0, vwg0 + vgroups) with their
   // own activations X2, row sums of squares ssq2 and n_valid2 valid rows (an
@@ -271,11 +273,15 @@ __global__ void __launch_bounds__(GemvGeom<WT, NT, XMODE>::THREADS, 1)
         if constexpr (kStream) issue_x(it, u_begin + it);
         issued = it + 1;
       }
-      if (a.pf_units > 0 && issued == n_units) {
-        const long long u0 = static_cast<long long>(blockIdx.x) * a.pf_U / G;
-        const long long u1 = u0 + a.pf_units < a.pf_U ? u0 + a.pf_units : a.pf_U;
-        if (u1 > u0)
-          bulk_prefetch_l2_plain(a.pf_W + u0 * a.pf_unit, static_cast<uint32_t>((u1 - u0) * a.pf_unit));
+      if (a.pf_bytes > 0 && issued == n_units) {
+        const int n0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.pf_G / G);
+        const int n1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.pf_G / G);
+        for (int c2 = n0; c2 < n1; ++c2) {
+          const size_t off = static_cast<size_t>(static_cast<long long>(c2) * a.pf_U / a.pf_G) * a.pf_unit;
+          if (off >= a.pf_total) break;
+          const size_t left = a.pf_total - off;
+          bulk_prefetch_l2_plain(a.pf_W + off, static_cast<uint32_t>(left < size_t(a.pf_bytes) ? left : size_t(a.pf_bytes)));
+        }
       }
       // Every issued copy must land before the CTA may exit.
       for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
