@@ -46,13 +46,13 @@ UNIT = "draft passes/s"
 WORKLOAD = "full_bf16"
 FUSE_PER_STEP = 8
 # DRAM bytes (read + write) of one LM-head launch at this workload, from one
-# ncu capture of that kernel (dram__bytes_read.sum 778084608 +
-# dram__bytes_write.sum 3592960).  Reset to None whenever the head kernel
+# ncu capture of that kernel (dram__bytes_read.sum 778135552 +
+# dram__bytes_write.sum 3333888).  Reset to None whenever the head kernel
 # changes.
-HEAD_TRAFFIC_BYTES = 781677568
+HEAD_TRAFFIC_BYTES = 781469440
 HEAD_TRAFFIC_SOURCE = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on one LM-head launch "
                        "(head_tc8_kernel) of `bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-extras`, "
-                       "library as of commit 2a7fc00")
+                       "library as of commit f3b1c08")
 
 
 def load_peaks():
