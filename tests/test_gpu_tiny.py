@@ -295,6 +295,31 @@ def test_accept_matches_oracle():
         assert int(d_acc[s]) == n and int(d_next[s]) == bonus and int(d_pos[s]) == pos[s] + n + 1, s
 
 
+def test_attention_chunks_two_long_slots():
+    """Two slots of 3000 and 1100 positions (24 and 9 super-tiles) at 12
+    chunks per slot: the plan gives the first sequence 12 chunks and the
+    second 5, so the several-sequence merge folds more chunks than one batch
+    of loads holds; both slots against the oracle."""
+    import dflash_block_drafter_gb300 as D
+    cfg = synth.CONFIGS["tiny"]
+    ck, model, om = _model(cfg, seed=32)
+    cap = 3072
+    ctxs, Bs = [3000, 1100], [7, 4]
+    st = _state(model, 2, cap)
+    osts = []
+    for s, n_ctx in enumerate(ctxs):
+        ost = _ostate(om, cfg, cap)
+        _fuse_both(st, ost, s, cfg, synth.make_taps(cfg, n_ctx, seed=32, stream=s), np.arange(n_ctx))
+        osts.append(ost)
+    assert D.dflash_state_set_attn_chunks(st.handle, 0) >= 12
+    D.dflash_state_set_attn_chunks(st.handle, 12)
+    res = _draft_both(st, osts, synth.make_token_ids(cfg, 2, seed=32), ctxs, Bs)
+    for s in range(2):
+        check_hidden(st.final_hidden[s, :Bs[s]].cpu().numpy(), res[s].final_hidden, f"slot {s}")
+        check_drafts(st.drafts[s].cpu().numpy(), res[s], Bs[s], f"slot {s}")
+    assert st.take_status() == 0
+
+
 @pytest.mark.parametrize("chunks", [1, 2, 4, 5])
 def test_attention_context_chunks(chunks):
     """The split-context attention and its log-sum-exp merge: a 600-position
