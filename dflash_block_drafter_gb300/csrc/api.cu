@@ -360,7 +360,8 @@ int dflash_config_check(const dflash_config* c) {
   if ((gq * 8) % 16 || gq * 8 > 128) return DFLASH_ERR_UNSUPPORTED;
   // the attention CTA holds the M = 8 * gq query rows, two K and two V tiles and P in shared memory
   if (attn_smem_bytes(c->head_dim, gq * 8) > 232448) return DFLASH_ERR_UNSUPPORTED;
-  if (c->hidden < 256 || c->hidden % 256) return DFLASH_ERR_UNSUPPORTED;
+  // (the row RMSNorm holds a row of at most 8192 values in one CTA's registers)
+  if (c->hidden < 256 || c->hidden % 256 || c->hidden > 8192) return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_q_heads * c->head_dim) % 256 || c->intermediate < 256 || c->intermediate % 256)
     return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_kv_heads * c->head_dim) % 64) return DFLASH_ERR_UNSUPPORTED;

@@ -166,7 +166,8 @@ const char* dflash_last_cuda_error(void);
  * 256}; n_q_heads % n_kv_heads == 0 and (n_q_heads / n_kv_heads) * 8 a
  * multiple of 16 and at most 128 (the attention's query rows per kv head
  * fill one 128-row tensor-core tile; at most 112 when head_dim is 256, for
- * shared memory); hidden, n_q_heads*head_dim, intermediate multiples of 256;
+ * shared memory); hidden, n_q_heads*head_dim, intermediate multiples of 256,
+ * hidden at most 8192;
  * vocab >= 2; 0 <= mask_token_id < vocab; n_taps >= 1; rope_theta > 0;
  * norm_eps >= 0; a known weight_type.  No device is touched. */
 int dflash_config_check(const dflash_config* cfg);

@@ -51,6 +51,7 @@ def test_config_check_rejects(lib):
         (dict(head_dim=96), D.DFLASH_ERR_UNSUPPORTED),
         (dict(n_q_heads=5, n_kv_heads=2), D.DFLASH_ERR_UNSUPPORTED),
         (dict(hidden=300), D.DFLASH_ERR_UNSUPPORTED),
+        (dict(hidden=8448), D.DFLASH_ERR_UNSUPPORTED),
         (dict(intermediate=100), D.DFLASH_ERR_UNSUPPORTED),
         (dict(n_layers=0), D.DFLASH_ERR_UNSUPPORTED),
         (dict(n_layers=9), D.DFLASH_ERR_UNSUPPORTED),
