@@ -183,71 +183,75 @@ cudaError_t launch_dequant(int wtype, const uint8_t* packed, int N, int K, float
 // widened to fp32; slots >= n_seq are zero.  Also validates the pass's
 // device-side scalars.
 
-__global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ EmbedArgs a) {
+constexpr int kEmbedThreads = 128;  // one 16-byte piece (4 columns) of a row per thread
+
+__global__ void __launch_bounds__(kEmbedThreads) embed_kernel(const __grid_constant__ EmbedArgs a) {
   const int s = blockIdx.x, i = blockIdx.y;
-  pdl_wait();
-  pdl_launch_dependents();
-  float* xr = a.x + static_cast<size_t>(s * 8 + i) * a.H;
-  if (s >= a.n_seq) {
-    for (int k = threadIdx.x; k < a.H; k += blockDim.x) xr[k] = 0.f;
-    return;
-  }
+  const int c = blockIdx.z * kEmbedThreads + static_cast<int>(threadIdx.x);  // 4-column piece of the row
+  const int H4 = a.H / 4;
+  const bool live = s < a.n_seq, in_row = c < H4;
+  // Before the dependent-launch wait only reads of what no kernel of this
+  // stream is still writing: the token id (written by the caller or by an
+  // earlier acceptance, complete before the previous kernel could release
+  // this one), the embedding row and the norm weights (constants).
   int tok = a.mask_id;
-  if (i == 0) {
+  bool bad_tok = false;
+  if (live && i == 0) {
     tok = a.anchor_tok[s];
     if (tok < 0 || tok >= a.vocab) {
-      if (threadIdx.x == 0) set_status(a.status, DFLASH_DEV_BAD_TOKEN);
+      bad_tok = true;
       tok = 0;
     }
-    if (threadIdx.x == 0) {
-      const int B = a.block_len[s];
-      if (B < DFLASH_MIN_BLOCK || B > DFLASH_MAX_BLOCK) set_status(a.status, DFLASH_DEV_BAD_BLOCK);
-      const int Bc = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
-      const int p = a.anchor_pos[s];
-      if (p < 0 || (!a.ring && static_cast<long long>(p) + Bc > a.cap)) set_status(a.status, DFLASH_DEV_CAPACITY);
-    }
   }
-  const uint16_t* er = a.embed + static_cast<size_t>(tok) * a.H;
-  if (a.xn == nullptr) {
-    for (int k = threadIdx.x; k < a.H; k += blockDim.x) xr[k] = bf16_bits_to_float(er[k]);
-    return;
+  uint2 e = make_uint2(0u, 0u);
+  float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (live && in_row) {
+    e = __ldg(reinterpret_cast<const uint2*>(a.embed + static_cast<size_t>(tok) * a.H) + c);
+    if (a.xn) wv = __ldg(reinterpret_cast<const float4*>(a.w_next) + c);
   }
-  // 4 columns per thread: the fp32 row, the BF16 hi/lo planes of x * w_next
-  // and the sum of squares of each 64-column group (16 consecutive lanes,
-  // fixed order)
+  pdl_wait();
+  pdl_launch_dependents();
+  if (live && i == 0 && blockIdx.z == 0 && threadIdx.x == 0) {
+    if (bad_tok) set_status(a.status, DFLASH_DEV_BAD_TOKEN);
+    const int B = a.block_len[s];
+    if (B < DFLASH_MIN_BLOCK || B > DFLASH_MAX_BLOCK) set_status(a.status, DFLASH_DEV_BAD_BLOCK);
+    const int Bc = B < DFLASH_MIN_BLOCK ? DFLASH_MIN_BLOCK : (B > DFLASH_MAX_BLOCK ? DFLASH_MAX_BLOCK : B);
+    const int p = a.anchor_pos[s];
+    if (p < 0 || (!a.ring && static_cast<long long>(p) + Bc > a.cap)) set_status(a.status, DFLASH_DEV_CAPACITY);
+  }
   const int n = s * 8 + i;
-  for (int c0 = 0; c0 < a.H / 4; c0 += blockDim.x) {
-    const int c = c0 + threadIdx.x;
-    float ss = 0.f;
-    if (c < a.H / 4) {
-      const uint2 e = *reinterpret_cast<const uint2*>(er + 4 * c);
-      const float4 v = make_float4(__uint_as_float(e.x << 16), __uint_as_float(e.x & 0xffff0000u),
-                                   __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xffff0000u));
-      reinterpret_cast<float4*>(xr)[c] = v;
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w_next) + c);
-      if (a.f16) {
-        *reinterpret_cast<uint2*>(static_cast<__half*>(a.xn) + xchunk_index(4 * c, n, 0, 8, a.ku, 1)) =
-            make_uint2(pack_f16x2(v.x * wv.x, v.y * wv.y), pack_f16x2(v.z * wv.z, v.w * wv.w));
-      } else {
-        uint2 hi, lo;
-        split_bf16x2(v.x * wv.x, v.y * wv.y, hi.x, lo.x);
-        split_bf16x2(v.z * wv.z, v.w * wv.w, hi.y, lo.y);
-        __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(a.xn);
-        *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 0, 8, a.ku, 2)) = hi;
-        *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 1, 8, a.ku, 2)) = lo;
-      }
-      ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  float4* xr = reinterpret_cast<float4*>(a.x + static_cast<size_t>(n) * a.H);
+  // the BF16 row widened to fp32 (zeros for slots >= n_seq)
+  const float4 v = make_float4(__uint_as_float(e.x << 16), __uint_as_float(e.x & 0xffff0000u),
+                               __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xffff0000u));
+  if (in_row) xr[c] = v;
+  if (!live || a.xn == nullptr) return;
+  // one slot: the BF16 hi/lo planes (or the FP16 plane) of x * w_next and the
+  // sum of squares of each 64-column group (16 consecutive lanes, fixed order)
+  if (in_row) {
+    if (a.f16) {
+      *reinterpret_cast<uint2*>(static_cast<__half*>(a.xn) + xchunk_index(4 * c, n, 0, 8, a.ku, 1)) =
+          make_uint2(pack_f16x2(v.x * wv.x, v.y * wv.y), pack_f16x2(v.z * wv.z, v.w * wv.w));
+    } else {
+      uint2 hi, lo;
+      split_bf16x2(v.x * wv.x, v.y * wv.y, hi.x, lo.x);
+      split_bf16x2(v.z * wv.z, v.w * wv.w, hi.y, lo.y);
+      __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(a.xn);
+      *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 0, 8, a.ku, 2)) = hi;
+      *reinterpret_cast<uint2*>(xb + xchunk_index(4 * c, n, 1, 8, a.ku, 2)) = lo;
     }
-#pragma unroll
-    for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if ((threadIdx.x & 15) == 0 && c < a.H / 4) a.ssq[(c / 16) * 8 + n] = ss;
   }
+  float ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int off = 8; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 15) == 0 && in_row) a.ssq[(c / 16) * 8 + n] = ss;
 }
 
 cudaError_t launch_embed(const EmbedArgs& a, int nt, cudaStream_t st) {
+  if (a.H % 64 != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nt, 8);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(nt, 8, (a.H / 4 + kEmbedThreads - 1) / kEmbedThreads);
+  cfg.blockDim = dim3(kEmbedThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
