@@ -558,6 +558,9 @@ int dflash_state_create(const dflash_model* m, int32_t n_slots, int32_t capacity
   STRY(dev_alloc(&s->q_ready, size_t(R) * nq * d * 2, &total));
   // activations for streamed-X GEMVs: two 16-bit planes (BF16 hi and lo, or FP16 in the first)
   STRY(dev_alloc(&s->attn_out, xchunk_elems(nq * d, R, 128, 2) * 2, &total));
+  // rows of a tile's unused slots are never written by a pass: keep them zero
+  if (cudaMemset(s->attn_out, 0, xchunk_elems(nq * d, R, 128, 2) * 2) != cudaSuccess)
+    return fail(cuda_fail(cudaGetLastError(), "cudaMemset attn_out"));
   STRY(dev_alloc(&s->hbuf, xchunk_elems(I, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->xnorm, xchunk_elems(H, R, 128, 2) * 2, &total));
   STRY(dev_alloc(&s->xn, xchunk_elems(H, 8, 128, 2) * 2, &total));  // largest for 128 inputs per unit

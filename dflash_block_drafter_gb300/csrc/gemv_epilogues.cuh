@@ -763,7 +763,9 @@ struct EpiArgmax {
           constexpr float LOG2E = 1.4426950408889634f;
           const int h = e & 1;
           if (!isfinite(v)) {
-            L.bad = 1;
+            // only rows of the pass's sequences count (tile t holds sequence
+            // t's 8 rows; the rows of a tile's unused slots carry no data)
+            if (t < n_seq) L.bad = 1;
           } else if (min_p > 0.f) {
             if (v > L.v[t][h]) {
               // a new maximum: rescale the running sum to it (0 from -inf)
