@@ -443,9 +443,10 @@ struct EpiHeads {
 
   // Cluster finishing of the 8-row pass: this CTA holds the complete sums of
   // local group gl of head g / gph.  Key and query heads need every group of
-  // the head (RMS over d, RoPE pairs (i, i + d/2)): each group's values go to
-  // slot gl of every group CTA's buffer ([gph][8 rows][64] floats, in
-  // distributed shared memory), and each CTA then writes its own 64 columns.
+  // the head (RMS over d, RoPE pairs (i, i + d/2)): each group's per-warp sums
+  // of squares go to slot gl of every group CTA's buffer and its values to
+  // slot gl of its RoPE partner's ([gph][8 rows][64] floats, in distributed
+  // shared memory), and each CTA then writes its own 64 columns.
   // Value heads write their columns straight away.
   template <int WT>
   __device__ bool group_cluster(const GemvArgs& ga, const Local& L, int g, int gl, int parts, int w, int lane,
@@ -476,10 +477,14 @@ struct EpiHeads {
       if (lane < 4) *reinterpret_cast<float2*>(mine + 512 + w * 8 + lane * 2) = make_float2(s0, s1);
     }
     if (exch) {
+      // every peer needs this group's sums of squares (the head's RMS); only
+      // the RoPE partner (the group half a head away) needs its values
+      const int partner = gl ^ (gph >> 1);
       for (int l2 = 0; l2 < gph; ++l2) {
         if (l2 == gl) continue;
         const uint32_t r = static_cast<uint32_t>(l2 * parts);
-        st_cluster_v4(mapa_shared(smem_u32(mine + t4), r), acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        if (l2 == partner)
+          st_cluster_v4(mapa_shared(smem_u32(mine + t4), r), acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
         if (lane < 4) {
           st_cluster_f32(mapa_shared(smem_u32(mine + 512 + w * 8 + lane * 2), r), s0);
           st_cluster_f32(mapa_shared(smem_u32(mine + 512 + w * 8 + lane * 2 + 1), r), s1);
