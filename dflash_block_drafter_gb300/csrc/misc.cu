@@ -271,10 +271,17 @@ constexpr int kNormThreads = 128, kNormV = 16;  // rows of up to 8192 floats
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(const __grid_constant__ NormArgs a) {
   const int r = blockIdx.x;
+  const int H4 = a.H >> 2;
+  // the norm weights (constants) before the dependent-launch wait
+  float4 w[kNormV];
+#pragma unroll
+  for (int i = 0; i < kNormV; ++i) {
+    const int k4 = static_cast<int>(threadIdx.x) + i * kNormThreads;
+    w[i] = k4 < H4 ? __ldg(reinterpret_cast<const float4*>(a.w) + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[kNormThreads / 32];
-  const int H4 = a.H >> 2;
   const bool valid = r < a.rows_valid;
   const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(r) * a.H);
   float4 v[kNormV];
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(const __grid
     const int k4 = static_cast<int>(threadIdx.x) + i * kNormThreads;
     if (k4 >= H4) break;
     const int k = 4 * k4;
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w) + k4);
+    const float4 w4 = w[i];
     const float y0 = v[i].x * rs * w4.x, y1 = v[i].y * rs * w4.y, y2 = v[i].z * rs * w4.z, y3 = v[i].w * rs * w4.w;
     // four consecutive inputs of one chunk row (KU is a multiple of 4)
     if (a.out_f16) {
