@@ -347,12 +347,13 @@ def _time_graph(fn, stream, G: int, n_rep: int) -> dict:
     return r
 
 
-def time_weight_type(wt: str, dev, peak: float, n_rep: int = 20) -> dict:
-    """Device-timed draft pass and draft cycle of the full geometry at an
-    8192-position context with the given backbone type (graph replays)."""
+def time_weight_type(wt: str, dev, peak: float, n_rep: int = 20, cfg_name: str = "full_bf16") -> dict:
+    """Device-timed draft pass and draft cycle of the full geometry (the
+    8192-position context, or the workload cfg_name names) with the given
+    backbone type (graph replays)."""
     import torch
     from dflash_block_drafter_gb300.runtime import DraftModel, DraftState, accept
-    cfg = synth.CONFIGS["full_bf16"].with_(weight_type=wt)
+    cfg = synth.CONFIGS[cfg_name].with_(weight_type=wt)
     ctx, B = cfg.ctx, cfg.block
     ck = synth.make_checkpoint(cfg, seed=0)
     model = DraftModel(cfg, ck, device=dev)
@@ -659,6 +660,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                     per[wt] = time_weight_type(wt, dev, peak)
         line["per_weight_type"] = per
         line["batched_mix"] = time_batched_mix(dev, peak)
+        lc = time_weight_type("q8_0", dev, peak, n_rep=10, cfg_name="long_q8_0")
+        lc["workload"] = ("long context: 262144 positions of pre-filled K/V (2.7 GB), Q8_0 backbone, "
+                          "block 8, fuse 8 per cycle")
+        line["long_context"] = lc
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in oracle_baseline(ckpt, cfg).items() if k != "seconds"}
         line["cpu_baseline"]["cpu_model"] = cpu_model()
