@@ -144,12 +144,6 @@ int dev_alloc(T** p, size_t bytes, size_t* total) {
     if (rc_ != DFLASH_OK) return rc_; \
   } while (0)
 
-size_t src_bytes(int wt, int rows, int k) {
-  if (wt == WT_BF16) return size_t(rows) * k * 2;
-  const int bs = wt == WT_Q8_0 ? 34 : (wt == WT_Q4_0 ? 18 : 22);
-  return size_t(rows) * (k / 32) * bs;
-}
-
 int alloc_packed(PackedMatrix& pm, int wt, int n, int k, size_t* total) {
   pm.wtype = wt;
   pm.n = n;
@@ -372,8 +366,8 @@ int dflash_config_check(const dflash_config* c) {
   if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta)) return DFLASH_ERR_INVALID_ARG;
   if (!(c->norm_eps >= 0.f) || !std::isfinite(c->norm_eps)) return DFLASH_ERR_INVALID_ARG;
   if (c->weight_type < DFLASH_WT_BF16 || c->weight_type > DFLASH_WT_Q4_0) return DFLASH_ERR_UNSUPPORTED;
-  // K/V arena rows and head rows must fit 32-bit tensor-map coordinates
-  if (static_cast<long long>(c->vocab) > 0x7fffffffLL) return DFLASH_ERR_UNSUPPORTED;
+  // (head rows fit 32-bit tensor-map coordinates: vocab is an int32; the K/V
+  // arena's rows are checked when a state is created)
   return DFLASH_OK;
 }
 

@@ -714,8 +714,6 @@ struct CombineArgs {
   unsigned long long* trace;  // diagnostic builds only (DFLASH_TRACE): per-CTA timestamps
 };
 
-constexpr int kCombineMaxC = 512;
-
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineArgs a) {
   __shared__ float smx[8][32];
   __shared__ float ssum[8][32];
